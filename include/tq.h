@@ -1,0 +1,219 @@
+/*
+ * tq.h -- C ABI of the GB300 (sm_103a) library for attention over a
+ * TurboQuant-compressed KV cache.
+ *
+ * Sources restated here (no code was taken from them):
+ *   [TQ#36]    llama-cpp-turboquant pull request #36, four commit messages:
+ *              "shuffle WHT" (SET_ROWS butterflies, stages h = 1..64),
+ *              "asymmetric D" (K head dim 192 with V head dim 128, padding),
+ *              "Q x centroid LUT" (per-step LUT of q[d] * centroid[c] for the
+ *              single-query decode; 4/8/16 centroids; 2 qs bytes + 1 signs byte
+ *              per 8 turbo3 elements), "VEC tuning" (results table; turbo2 7.5x).
+ *   [HIP#28]   atomic-llama-cpp-turboquant pull request #28, "HIP/turbo3:
+ *              graph-safe decode + inline-dequant TILE prefill": section
+ *              "1. Graph-safe decode" (no allocation while a stream is being
+ *              captured; decode with at most 2 query rows takes the VEC path),
+ *              section "2. Inline-dequant TILE prefill" (dequantise K/V while
+ *              loading tiles, never materialise f16 K/V), "Correctness".
+ *   [QSA#1821] "qsa_prompt_attn: int8 K/V prefetched in registers and sharing
+ *              one buffer": sections "What" and "Change" (prompt attention over
+ *              scattered int8 K/V rows with per-row scales).
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *     the library keeps no state and allocates nothing.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and may be captured into a CUDA graph.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns an error code and launches nothing.  A failed launch
+ *     returns TQ_ERR_CUDA.  Device-side checks (e.g. a cell id out of range)
+ *     write a tq_status value into a caller-provided device word and skip the
+ *     offending access; they never trap.
+ *   - All device buffers must be 16-byte aligned.
+ */
+#ifndef TQ_H
+#define TQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or shape       */
+  TQ_ERR_UNSUPPORTED = 2,   /* valid but not implemented combination            */
+  TQ_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small       */
+  TQ_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed             */
+  TQ_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up               */
+  TQ_ERR_DEVICE_CHECK = 6   /* a device-side range check rejected an input      */
+} tq_status;
+
+typedef enum { TQ_TURBO2 = 2, TQ_TURBO3 = 3, TQ_TURBO4 = 4 } tq_type;
+typedef enum { TQ_F32 = 0, TQ_F16 = 1, TQ_BF16 = 2 } tq_dtype;
+
+/* Decode kernel choice.  LUT: the pages' per-step Q x centroid shared-memory
+ * table ([TQ#36] "Q x centroid LUT").  MMA: codes unpacked in registers straight
+ * into tensor-core operand fragments.  AUTO picks MMA when it supports the
+ * shape, else LUT.  Both compute the same attention. */
+typedef enum { TQ_DECODE_AUTO = 0, TQ_DECODE_LUT = 1, TQ_DECODE_MMA = 2 } tq_decode_algo;
+
+typedef void *tq_stream; /* cudaStream_t */
+
+/* Codebook of one cache ([TQ#36] "Q x centroid LUT": 4, 8 or 16 centroids).
+ * sign_bits: the 128-entry +-1 diagonal S of the rotation; bit i of the
+ *            little-endian 128-bit value set means s_i = -1.
+ * centroids: n_centroids values, strictly ascending, exactly symmetric
+ *            (c[i] == -c[n-1-i]) and each exactly representable in binary16.
+ * tq_codebook_init fills the canonical table. */
+typedef struct tq_codebook {
+  uint32_t sign_bits[4];
+  int32_t n_centroids;
+  float centroids[16];
+} tq_codebook;
+
+/* One compressed cache (K or V) in three device planes, head-major:
+ *   norms  binary16 [n_kv_heads][n_cells][n_blocks]        block L2 norms
+ *   qs     uint8    [n_kv_heads][n_cells][n_blocks][32]    turbo2 / turbo3
+ *                   [n_kv_heads][n_cells][n_blocks][64]    turbo4
+ *   signs  uint8    [n_kv_heads][n_cells][n_blocks][16]    turbo3 only (else NULL)
+ * n_blocks = ceil(head_dim / 128); head_dim is the logical width (a partial last
+ * block is zero-padded before quantisation, [TQ#36] "asymmetric D").
+ * n_cells must be a positive multiple of 64.
+ * Codes are sign-magnitude: code k = s*(n/2) + j has value (s ? +1 : -1) *
+ * centroids[n/2 + j].  Bit layout of one 128-element block:
+ *   qs (turbo2/3): 8 little-endian u32 words; word w holds elements 16w..16w+15;
+ *      element 16w+i (i < 8) at bits 4i..4i+1, element 16w+8+i at bits 4i+2..4i+3
+ *      (turbo2: the 2-bit code; turbo3: the magnitude index j).
+ *   qs (turbo4): 16 words; word w holds elements 8w..8w+7, element 8w+i at
+ *      bits 4i..4i+3 (the 4-bit code).
+ *   signs (turbo3): 4 words; word u holds elements 32u..32u+31; element 32u+r at
+ *      bit 4(r%8) + 2 + r/8 for r < 16 and at bit 4((r-16)%8) + (r-16)/8 for r >= 16.
+ * Stored size: 2.125 / 3.125 / 4.125 bits per element (turbo2 / 3 / 4); turbo2
+ * is 7.5x smaller than f16 ([TQ#36] "VEC tuning"). */
+typedef struct tq_cache {
+  int32_t type;        /* tq_type */
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t n_blocks;
+  int64_t n_cells;
+  void *norms;         /* device */
+  void *qs;            /* device */
+  void *signs;         /* device, turbo3 only */
+} tq_cache;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *tq_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int tq_version(void);
+
+/* Host only.  Canonical codebook for `type`: the Lloyd-Max quantiser of
+ * N(0, 1) (Lloyd iteration in double precision) scaled by 1/sqrt(128), each
+ * centroid rounded to the nearest binary16 value; sign_bits copied in.
+ * Errors: TQ_ERR_INVALID_ARG for an unknown type or NULL pointers. */
+tq_status tq_codebook_init(int type, const uint32_t sign_bits[4], tq_codebook *out);
+
+/* Host only.  Bytes of the norms / qs / signs planes for a cache of this shape
+ * (signs = 0 unless turbo3).  Errors: TQ_ERR_INVALID_ARG. */
+tq_status tq_cache_plane_bytes(int type, int n_kv_heads, int head_dim, int64_t n_cells,
+                               size_t *norms_bytes, size_t *qs_bytes, size_t *signs_bytes);
+
+/* SET_ROWS, quantise-on-write ([TQ#36] "shuffle WHT"): for every row r and KV
+ * head h, each 128-element block x of src[r][h][:] (zero-padded to a multiple
+ * of 128) is written to cell cell_ids[r] as
+ *   norm  = binary16(|x|)                      (round to nearest even)
+ *   y     = H S x / (|x| sqrt(128))            H: 128-point Walsh-Hadamard
+ *   code  = nearest centroid of each y_i       (ties: the higher centroid)
+ * src      device, src_type (TQ_F32 / TQ_F16 / TQ_BF16) [n_rows][n_kv_heads][head_dim]
+ * cell_ids device int64 [n_rows]; distinct; each in [0, n_cells)
+ * dev_status device int32 or NULL: a row whose cell id is out of range is
+ *          skipped and TQ_ERR_DEVICE_CHECK is stored here.
+ * n_rows = 0 is a no-op.  Errors: TQ_ERR_INVALID_ARG, TQ_ERR_CUDA. */
+tq_status tq_set_rows(const tq_cache *dst, const tq_codebook *cb, const void *src, int src_type,
+                      const int64_t *cell_ids, int64_t n_rows, int32_t *dev_status,
+                      tq_stream stream);
+
+/* Bytes of workspace tq_fattn_decode needs for this shape (0 if the shape is
+ * invalid).  The workspace must be 256-byte aligned and zero-filled before its
+ * first use; every call leaves it ready for the next one (the split counters
+ * reset themselves), so it can be reused across calls and graph replays but
+ * not by two calls that run concurrently. */
+size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_heads,
+                                 int64_t kv_len);
+
+/* Single-query decode attention over cells 0..kv_len-1 ([TQ#36] "Q x centroid
+ * LUT", "VEC tuning"; [HIP#28] "1. Graph-safe decode"):
+ *   out[h][:] = softmax_t(scale * q[h] . k_t) v_t      k_t, v_t dequantised rows
+ * with query head h reading KV head h / (n_q_heads / n_kv_heads).  The key range
+ * is split across CTAs; each split keeps a running max/sum and the merge is a
+ * log-sum-exp combination done by the last CTA of each KV head.
+ * q    device f32 [n_q_heads][k->head_dim]
+ * out  device f32 [n_q_heads][v->head_dim]
+ * algo tq_decode_algo.  kv_len = 0 writes zeros.
+ * Errors: TQ_ERR_INVALID_ARG (shapes, kv_len > n_cells, codebooks),
+ *         TQ_ERR_UNSUPPORTED (algo cannot take this shape), TQ_ERR_WORKSPACE,
+ *         TQ_ERR_CUDA. */
+tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                          const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
+                          float scale, int algo, float *out, void *workspace,
+                          size_t workspace_bytes, tq_stream stream);
+
+/* Bytes of workspace tq_fattn_prefill needs (0 if the shape is invalid);
+ * same alignment and zero-fill rule as the decode workspace. */
+size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads,
+                                  int64_t kv_len);
+
+/* Multi-query (prefill / verify) attention with inline dequantisation
+ * ([HIP#28] "2. Inline-dequant TILE prefill"): packed K/V tiles are expanded
+ * to fp16 operand tiles in shared memory and multiplied on the tcgen05 tensor
+ * cores; no f16 copy of the cache is ever written to global memory.
+ *   out[i][h][:] = softmax_{t <= p_i}(scale * q[i][h] . k_t) v_t,
+ *   p_i = kv_len - nq + i when causal, else every t < kv_len.
+ * q    device, q_type (TQ_BF16, TQ_F16 or TQ_F32) [nq][n_q_heads][k->head_dim]
+ * out  device f32 [nq][n_q_heads][v->head_dim]
+ * Requires nq <= kv_len when causal.
+ * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                           const tq_codebook *cbv, const void *q, int q_type, int nq,
+                           int n_q_heads, int64_t kv_len, float scale, int causal, float *out,
+                           void *workspace, size_t workspace_bytes, tq_stream stream);
+
+/* Bytes of workspace tq_int8_prompt_attn needs (0 if the shape is invalid). */
+size_t tq_int8_prompt_attn_workspace(int nq, int n_q_heads, int n_kv_heads, int head_dim,
+                                     int64_t ctx);
+
+/* Prompt attention over an int8 KV cache with per-row scales whose rows are
+ * scattered over the cells ([QSA#1821] "What", "Change"):
+ *   k_t = k[cell_of_pos[t]][hk][:] * float(k_scale[cell_of_pos[t]][hk])   (v alike)
+ *   out[i][h][:] = softmax_{t <= p_i}(scale * q[i][h] . k_t) v_t,  p_i = ctx - nq + i
+ * (every t < ctx when causal = 0).
+ * k, v        device int8 [n_cells][n_kv_heads][head_dim]
+ * k_scale, v_scale device binary16 [n_cells][n_kv_heads]
+ * cell_of_pos device int32 [ctx], each in [0, n_cells)
+ * q           device binary16 [nq][n_q_heads][head_dim]
+ * out         device f32 [nq][n_q_heads][head_dim]
+ * head_dim must be 128.  A cell id out of range is read as a zero row and
+ * TQ_ERR_DEVICE_CHECK is stored in the workspace status word (tq_workspace_status).
+ * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+tq_status tq_int8_prompt_attn(const int8_t *k, const uint16_t *k_scale, const int8_t *v,
+                              const uint16_t *v_scale, int64_t n_cells, const int32_t *cell_of_pos,
+                              int64_t ctx, const uint16_t *q, int nq, int n_q_heads,
+                              int n_kv_heads, int head_dim, float scale, int causal, float *out,
+                              void *workspace, size_t workspace_bytes, tq_stream stream);
+
+/* Reads (and clears) the device status word kept in a workspace of the
+ * calls above: waits for `stream`, so it must not be called while the stream
+ * is being captured.  *status_out receives TQ_OK or the first device-side
+ * error (TQ_ERR_DEVICE_CHECK, TQ_ERR_TIMEOUT).  Errors: TQ_ERR_INVALID_ARG,
+ * TQ_ERR_CUDA. */
+tq_status tq_workspace_status(void *workspace, size_t workspace_bytes, int32_t *status_out,
+                              tq_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H */

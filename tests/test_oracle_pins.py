@@ -1,0 +1,346 @@
+"""Pins of the CPU oracle to facts outside itself: closed forms, published
+tables, invariants, brute force and special cases (no GPU needed)."""
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.integrate import quad
+
+import oracle as O
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_table(name):
+    rows = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                parts = line.split()
+                rows[parts[0]] = parts[1:]
+    return rows
+
+
+# --------------------------------------------------------------------- rotation
+
+def test_hadamard_orthogonal_and_symmetric():
+    H = O.hadamard()
+    assert np.array_equal(H @ H.T, 128 * np.eye(128))
+    assert np.array_equal(H, H.T)
+    assert set(np.unique(H)) == {-1.0, 1.0}
+
+
+def test_hadamard_matches_butterfly_recursion():
+    # column j of H is the butterfly transform of the unit vector e_j
+    H = O.hadamard()
+    eye = np.eye(128)
+    assert np.array_equal(O.butterfly_wht(eye), H)           # rows: transforms of e_j
+    # 7 stages h = 1..64 as printed on the page
+    facts = _read_table("page_format_facts.txt")
+    assert int(facts["wht_stages"][0]) == int(math.log2(128))
+
+
+def test_hadamard_small_known():
+    # Sylvester H_4 written out by hand
+    H4 = np.array([[1, 1, 1, 1], [1, -1, 1, -1], [1, 1, -1, -1], [1, -1, -1, 1]], float)
+    assert np.array_equal(O.hadamard(4), H4)
+
+
+def test_rotation_orthonormal_norm_preserving():
+    sb = W.sign_bits(1, W.S_SIGNS_K)
+    R = O.rotation(sb)
+    assert np.allclose(R @ R.T, np.eye(128), atol=1e-14)
+    S = np.diag(O.sign_vector(sb))
+    assert np.array_equal(S @ S, np.eye(128))
+    u = W.normal(3, 1, 128 * 50).reshape(50, 128)
+    assert np.allclose(np.linalg.norm(u @ R.T, axis=1), np.linalg.norm(u, axis=1), rtol=1e-14)
+
+
+def test_sign_bits_order():
+    sb = np.array([0b101, 0, 0, 1 << 31], dtype=np.uint32)
+    s = O.sign_vector(sb)
+    neg = np.nonzero(s < 0)[0].tolist()
+    assert neg == [0, 2, 127]
+
+
+# -------------------------------------------------------------------- codebooks
+
+@pytest.mark.parametrize("n", [4, 8, 16])
+def test_lloyd_max_matches_max_1960(n):
+    table = _read_table("lloyd_max_gaussian.txt")[str(n)]
+    dist, levels = float(table[0]), np.array([float(v) for v in table[1:]])
+    c = O.lloyd_max_normal(n)
+    assert np.allclose(c[n // 2:], levels, atol=6e-4)
+    assert abs(O.lloyd_max_distortion(c) - dist) / dist < 5e-4
+
+
+@pytest.mark.parametrize("n", [4, 8, 16])
+def test_lloyd_max_fixed_point_by_quadrature(n):
+    c = O.lloyd_max_normal(n)
+    assert np.allclose(c, -c[::-1], atol=1e-14)
+    t = np.concatenate(([-np.inf], 0.5 * (c[:-1] + c[1:]), [np.inf]))
+    pdf = lambda x: math.exp(-x * x / 2) / math.sqrt(2 * math.pi)
+    d = 0.0
+    for k in range(n):
+        m0 = quad(pdf, t[k], t[k + 1], epsabs=1e-14)[0]
+        m1 = quad(lambda x: x * pdf(x), t[k], t[k + 1], epsabs=1e-14)[0]
+        assert abs(m1 / m0 - c[k]) < 1e-10             # centroid condition
+        d += quad(lambda x: (x - c[k]) ** 2 * pdf(x), t[k], t[k + 1], epsabs=1e-14)[0]
+    assert abs(d - O.lloyd_max_distortion(c)) < 1e-12
+
+
+@pytest.mark.parametrize("t", [2, 3, 4])
+def test_canonical_codebook(t):
+    c = O.centroids(t)
+    facts = _read_table("page_format_facts.txt")
+    assert len(c) == int(facts[f"turbo{t}_centroids"][0])
+    assert np.all(np.diff(c) > 0)
+    assert np.array_equal(c, -c[::-1])
+    assert np.array_equal(c.astype(np.float16).astype(np.float64), c)
+    exact = O.lloyd_max_normal(len(c)) / math.sqrt(128)
+    assert np.max(np.abs(c - exact) / np.abs(exact)) <= 2.0 ** -11
+
+
+# --------------------------------------------------------------- codes, layout
+
+@pytest.mark.parametrize("t", [2, 3, 4])
+def test_code_mapping_roundtrip(t):
+    c = O.centroids(t)
+    n = len(c)
+    i = np.arange(n)
+    codes = O.index_to_code(i, n)
+    assert sorted(codes.tolist()) == list(range(n))
+    assert np.array_equal(O.code_to_value(codes, c), c)
+    # sign-magnitude: top bit = sign, low bits = magnitude rank
+    assert np.all((O.code_to_value(np.arange(n), c) > 0) == (np.arange(n) >= n // 2))
+
+
+@pytest.mark.parametrize("t", [2, 3, 4])
+def test_pack_unpack_roundtrip(t):
+    n = O.N_CENTROIDS[t]
+    codes = (W.bits(7, np.arange(64 * 128, dtype=np.uint64)) % np.uint64(n)).astype(np.int64)
+    codes = codes.reshape(64, 128)
+    qs, signs = O.pack_codes(codes, t)
+    assert qs.shape == (64, O.QS_BYTES[t])
+    assert np.array_equal(O.unpack_codes(qs, signs, t), codes)
+
+
+def test_bit_positions_by_hand():
+    def one(t, e, k):
+        codes = np.zeros((1, 128), np.int64)
+        codes[0, e] = k
+        qs, signs = O.pack_codes(codes, t)
+        return qs[0], (None if signs is None else signs[0])
+
+    qs, sg = one(3, 0, 7)            # j = 3, s = 1
+    assert qs[0] == 0x03 and sg[0] == 0x04
+    qs, sg = one(3, 8, 7)            # second half of word 0: bits 2..3, sign bit 3
+    assert qs[0] == 0x0C and sg[0] == 0x08
+    qs, sg = one(3, 5, 2)            # element 5: bits 20..21 -> byte 2 bits 4..5
+    assert qs[2] == 0x20 and not sg.any()
+    qs, sg = one(3, 13, 2)           # element 13 = 8 + 5: bits 22..23 -> byte 2 bits 6..7
+    assert qs[2] == 0x80 and not sg.any()
+    qs, sg = one(3, 16, 4)           # word 1, sign at bit 0 of signs word 0
+    assert qs[4] == 0x00 and sg[0] == 0x01
+    qs, sg = one(3, 24, 5)           # element 24: r = 24 -> bit 1 of signs word 0
+    assert qs[4] == 0x04 and sg[0] == 0x02
+    qs, sg = one(3, 127, 4)          # last element: signs word 3, r = 31 -> bit 4*7+1
+    assert sg[15] == 0x20
+    qs, _ = one(4, 9, 0xB)           # turbo4: word 1 nibble 1
+    assert qs[4] == 0xB0
+    qs, _ = one(2, 127, 3)           # turbo2: element 127 -> word 7, i = 7, bits 30..31
+    assert qs[31] == 0xC0
+
+
+def test_format_sizes_match_pages():
+    facts = _read_table("page_format_facts.txt")
+    assert O.bits_per_element(2) == 2.125
+    assert O.bits_per_element(3) == 3.125
+    assert O.bits_per_element(4) == 4.125
+    assert round(16 / O.bits_per_element(2), 1) == float(facts["turbo2_compression_vs_f16"][0])
+    per8 = (O.QS_BYTES[3] / 16, O.SIGN_BYTES / 16)
+    assert per8 == (float(facts["turbo3_qs_bytes_per_8"][0]), float(facts["turbo3_sign_bytes_per_8"][0]))
+
+
+# --------------------------------------------------------------------- encoder
+
+@pytest.mark.parametrize("t", [2, 3, 4])
+def test_brute_force_equals_threshold_search(t):
+    c = O.centroids(t)
+    y = W.normal(11, 2, 1_000_000) / math.sqrt(128)
+    mids = 0.5 * (c[:-1] + c[1:])
+    away = np.min(np.abs(y[:, None] - mids[None, :]), axis=1) > 1e-12
+    by_threshold = np.searchsorted(mids, y, side="right")        # y >= t  => upper cell
+    brute = O.nearest_centroid(y, c)
+    assert np.array_equal(brute[away], by_threshold[away])
+    assert np.array_equal(O.nearest_centroid(mids, c), np.arange(1, len(c)))   # exact ties -> upper
+    # the oracle's encoder on exact midpoints picks the upper centroid
+    sb = np.zeros(4, np.uint32)
+    x = np.zeros(128)
+    x[0] = 1.0                                  # y = (1/sqrt(128)) * H[:,0] = all +1/sqrt(128)
+    _, codes, y0 = O.quantize_blocks(x, sb, c)
+    assert np.allclose(y0, 1 / math.sqrt(128))
+
+
+def test_zero_block():
+    c = O.centroids(3)
+    nb, codes, y = O.quantize_blocks(np.zeros(128), np.zeros(4, np.uint32), c)
+    assert nb == 0 and np.all(y == 0)
+    # exact tie between -c4 and +c4 at 0 goes to the upper centroid: code s=1, j=0
+    assert np.all(codes == 4)
+    assert np.all(O.dequantize_blocks(nb, codes, np.zeros(4, np.uint32), c) == 0)
+
+
+@pytest.mark.parametrize("t", [2, 3, 4])
+def test_quantiser_distortion_matches_lloyd_max(t):
+    c = O.centroids(t)
+    sb = W.sign_bits(5, W.S_SIGNS_K)
+    x = W.normal(5, 1, 4000 * 128).reshape(4000, 128)
+    nb, codes, y = O.quantize_blocks(x, sb, c)
+    mse = np.mean((y - O.code_to_value(codes, c)) ** 2) * 128
+    d = O.lloyd_max_distortion(O.lloyd_max_normal(len(c)))
+    assert abs(mse - d) / d < 0.03
+    # full round trip: relative error of x_hat is the same distortion
+    xh = O.dequantize_blocks(nb, codes, sb, c)
+    rel = np.sum((xh - x) ** 2) / np.sum(x * x)
+    assert abs(rel - d) / d < 0.05
+
+
+def test_dequantize_structure():
+    c = O.centroids(3)
+    sb = W.sign_bits(9, W.S_SIGNS_V)
+    codes = (W.bits(3, np.arange(128, dtype=np.uint64)) % np.uint64(8)).astype(np.int64)
+    nb = np.array(np.float16(2.5)).view(np.uint16)
+    xh = O.dequantize_blocks(nb, codes, sb, c)
+    vals = O.code_to_value(codes, c)
+    assert abs(np.linalg.norm(xh) - 2.5 * np.linalg.norm(vals)) < 1e-12
+    assert np.allclose(O.rotation(sb) @ xh / 2.5, vals, atol=1e-14)
+
+
+def test_norm_is_fp16_rne():
+    x = np.zeros(128)
+    x[3] = 1.0 + 2.0 ** -11          # exactly half an fp16 ulp above 1 -> ties to even (1.0)
+    nb, _, _ = O.quantize_blocks(x, np.zeros(4, np.uint32), O.centroids(3))
+    assert nb == np.array(np.float16(1.0)).view(np.uint16)
+    x[3] = 1.0 + 3 * 2.0 ** -11      # 1.5 ulp -> rounds up to 1 + 2 ulp
+    nb, _, _ = O.quantize_blocks(x, np.zeros(4, np.uint32), O.centroids(3))
+    assert nb == np.array(np.float16(1.0 + 2.0 ** -9)).view(np.uint16)
+
+
+def test_set_rows_padding_and_cells():
+    c = O.centroids(3)
+    sb = W.sign_bits(2, W.S_SIGNS_K)
+    cache = O.empty_cache(3, 2, 192, 64)
+    src = W.normal(2, 3, 5 * 2 * 192).reshape(5, 2, 192)
+    cells = np.array([7, 0, 63, 12, 30])
+    O.set_rows(cache, src, cells, sb, c)
+    # block 1 of a 192-wide row = channels 128..191 followed by 64 zeros
+    blk = np.concatenate([src[2, 1, 128:], np.zeros(64)])
+    nb, codes, _ = O.quantize_blocks(blk, sb, c)
+    assert cache.norms[1, 63, 1] == nb
+    assert np.array_equal(O.unpack_codes(cache.qs[1, 63, 1], cache.signs[1, 63, 1], 3), codes)
+    assert not cache.qs[0, 1].any()                      # untouched cell
+
+
+# -------------------------------------------------------------------- attention
+
+def _loop_attention(q, k, v, scale):
+    # plain scalar loops with math.exp
+    out = []
+    for qi in q:
+        s = [scale * sum(a * b for a, b in zip(qi, kt)) for kt in k]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        z = sum(e)
+        out.append([sum(e[t] * v[t][d] for t in range(len(k))) / z for d in range(len(v[0]))])
+    return np.array(out)
+
+
+def test_attention_special_cases():
+    rng_q = W.normal(1, 1, 3 * 8).reshape(3, 8)
+    k = W.normal(1, 2, 5 * 8).reshape(5, 8)
+    v = W.normal(1, 3, 5 * 4).reshape(5, 4)
+    # one key -> output = that value row
+    assert np.allclose(O.softmax_attention(rng_q, k[:1], v[:1], 0.3), np.repeat(v[:1], 3, 0), atol=1e-15)
+    # equal scores (q = 0) -> mean of V
+    assert np.allclose(O.softmax_attention(np.zeros((1, 8)), k, v, 1.0), v.mean(0, keepdims=True), atol=1e-15)
+    # brute-force loops
+    assert np.allclose(O.softmax_attention(rng_q, k, v, 0.37), _loop_attention(rng_q, k, v, 0.37), atol=1e-13)
+    # empty key set -> zeros
+    assert np.all(O.softmax_attention(rng_q, k[:0], v[:0], 1.0) == 0)
+
+
+def test_causal_equals_prefix_attention():
+    q = W.normal(4, 1, 6 * 16).reshape(6, 16)
+    k = W.normal(4, 2, 10 * 16).reshape(10, 16)
+    v = W.normal(4, 3, 10 * 16).reshape(10, 16)
+    pos = np.arange(4, 10)
+    o = O.softmax_attention(q, k, v, 0.25, pos)
+    for i, p in enumerate(pos):
+        assert np.allclose(o[i], O.softmax_attention(q[i:i + 1], k[:p + 1], v[:p + 1], 0.25)[0], atol=1e-14)
+
+
+def test_split_lse_merge_equals_unsplit():
+    q = W.normal(6, 1, 2 * 32).reshape(2, 32) * 3
+    k = W.normal(6, 2, 100 * 32).reshape(100, 32)
+    v = W.normal(6, 3, 100 * 32).reshape(100, 32)
+    full = O.softmax_attention(q, k, v, 0.2)
+    parts = [O.lse_partial(q, k[a:b], v[a:b], 0.2) for a, b in [(0, 7), (7, 64), (64, 100)]]
+    assert np.allclose(O.lse_merge(parts), full, atol=1e-14)
+
+
+def test_decode_gqa_and_dequant_path():
+    shape = W.AttnShape("t", 2, 4, 128, 128, 70, seed=3)
+    c = O.centroids(3)
+    sk, sv = W.codebook_signs(shape)
+    kr, vr = W.kv_inputs(shape)
+    kc = O.empty_cache(3, 2, 128, 128)
+    vc = O.empty_cache(3, 2, 128, 128)
+    O.set_rows(kc, kr, np.arange(70), sk, c)
+    O.set_rows(vc, vr, np.arange(70), sv, c)
+    q = W.decode_query(shape)
+    out = O.decode(kc, vc, sk, sv, c, c, q, 70, 1 / math.sqrt(128))
+    kh = O.dequantize_cache(kc, sk, c, 70)
+    vh = O.dequantize_cache(vc, sv, c, 70)
+    for h in range(4):
+        ref = _loop_attention(q[h:h + 1], kh[h // 2], vh[h // 2], 1 / math.sqrt(128))
+        assert np.allclose(out[h], ref[0], atol=1e-12)
+    # quantised attention is close to unquantised attention (sanity, loose)
+    exact = np.stack([O.softmax_attention(q[h:h + 1], kr[:, h // 2], vr[:, h // 2], 1 / math.sqrt(128))[0]
+                      for h in range(4)])
+    assert O.nmse(out, exact) < 0.2
+
+
+def test_int8_dequantised_attention_and_permutation():
+    n_cells, hkv, d = 40, 2, 128
+    raw = W.gaussian_with_outliers(8, W.S_K, W.S_K_OUT, n_cells, hkv, d)
+    rawv = W.gaussian_with_outliers(8, W.S_V, W.S_V_OUT, n_cells, hkv, d)
+    ki, ks = W.int8_rows(raw)
+    vi, vs = W.int8_rows(rawv)
+    q = W.normal(8, W.S_Q, 5 * 4 * d).reshape(5, 4, d)
+    ident = np.arange(n_cells, dtype=np.int32)
+    o1 = O.int8_prompt_attn(ki, ks, vi, vs, ident, n_cells, q, 0.1)
+    # scatter the rows through a permutation: same logical content -> same output
+    perm = W.permutation(8, W.S_PERM, n_cells)            # cell_of_pos
+    ki2 = np.zeros_like(ki); ks2 = np.zeros_like(ks); vi2 = np.zeros_like(vi); vs2 = np.zeros_like(vs)
+    ki2[perm] = ki; ks2[perm] = ks; vi2[perm] = vi; vs2[perm] = vs
+    o2 = O.int8_prompt_attn(ki2, ks2, vi2, vs2, perm, n_cells, q, 0.1)
+    assert np.allclose(o1, o2, atol=1e-13)
+    # equals attention over q_int * scale computed with plain loops (one head, last query)
+    kk = [[float(ki[t, 0, j]) * float(np.float16(ks[t, 0].view(np.float16))) for j in range(d)] for t in range(n_cells)]
+    vv = [[float(vi[t, 0, j]) * float(np.float16(vs[t, 0].view(np.float16))) for j in range(d)] for t in range(n_cells)]
+    ref = _loop_attention(q[4:5, 1], kk, vv, 0.1)
+    assert np.allclose(o1[4, 1], ref[0], atol=1e-12)
+    # int8 rows reconstruct the raw values within half a quantisation step
+    recon = O.int8_dequantize(ki, ks)
+    step = ks.view(np.float16).astype(np.float64)
+    assert np.all(np.abs(recon - raw) <= 0.5 * step[..., None] * (1 + 1e-3) + 1e-3 * np.abs(raw))
+
+
+def test_nmse_definition():
+    b = np.array([1.0, 2.0, 2.0])
+    a = b + np.array([0.0, 0.3, 0.0])
+    assert abs(O.nmse(a, b) - 0.09 / 9.0) < 1e-15
