@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Benchmark of the compressed-KV-cache attention hot path on GB300.
+
+Workload (decode at 32K context): 8 KV heads x 32 query heads (GQA 4), head_dim
+128, 32768 cells, turbo3 K and V.  One step = T new tokens (default 64) through
+B independent layers (B caches sized so the working set exceeds 4x L2); each
+token-layer quantises the token's K and V rows into its cache (SET_ROWS) and
+runs the single-query decode attention over the 32768 cells.  The metric is
+decode-attention tokens per second for one layer (token-layer calls / s).
+
+Prints one JSON line.  --impl reference times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode attn tokens/s at 32K ctx (one layer, batch 1, turbo3 K/V, incl. SET_ROWS of the new token)"
+UNIT = "tokens/s"
+KV_LEN = 32768
+N_KV, N_Q, D = 8, 32, 128
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    p.add_argument("--algo", default="auto", choices=["auto", "lut", "mma"])
+    p.add_argument("--tokens-per-step", type=int, default=64)
+    p.add_argument("--no-extras", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def per_cache_bytes(tq_type=3):
+    per_block = {2: 34, 3: 50, 4: 66}[tq_type]
+    return 2 * N_KV * KV_LEN * per_block
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of the workload: n_heads of the 8 KV heads
+    (with their 4 query heads each); one step = SET_ROWS of the new token's K/V
+    rows, then decode over all 32768 cells.  Throughput is scaled to 8 heads."""
+
+    def __init__(self, n_heads=1):
+        import numpy as np
+        import oracle as O
+        import workloads as W
+        self.np, self.O = np, O
+        sh = W.decode_32k()
+        self.hs = hs = n_heads
+        k = W.gaussian_with_outliers(sh.seed, W.S_K, W.S_K_OUT, KV_LEN, N_KV, D)[:, :hs]
+        v = W.gaussian_with_outliers(sh.seed, W.S_V, W.S_V_OUT, KV_LEN, N_KV, D)[:, :hs]
+        self.sk, self.sv = W.codebook_signs(sh)
+        self.c = O.centroids(3)
+        self.kc = O.empty_cache(3, hs, D, KV_LEN)
+        self.vc = O.empty_cache(3, hs, D, KV_LEN)
+        O.set_rows(self.kc, W.to_f32(k), np.arange(KV_LEN), self.sk, self.c)
+        O.set_rows(self.vc, W.to_f32(v), np.arange(KV_LEN), self.sv, self.c)
+        self.q = W.to_f32(W.decode_query(sh))[: 4 * hs].astype(np.float64)
+        self.newk = W.to_f32(k[-1:])
+        self.newv = W.to_f32(v[-1:])
+
+    def step(self):
+        O, np = self.O, self.np
+        cell = np.array([KV_LEN - 1])
+        O.set_rows(self.kc, self.newk, cell, self.sk, self.c)
+        O.set_rows(self.vc, self.newv, cell, self.sv, self.c)
+        O.decode(self.kc, self.vc, self.sk, self.sv, self.c, self.c, self.q, KV_LEN, 1 / math.sqrt(D))
+
+    def timed(self, steps, budget_s):
+        done, t0 = 0, time.perf_counter()
+        while True:
+            self.step()
+            done += 1
+            el = time.perf_counter() - t0
+            if done >= steps or el >= budget_s:
+                break
+        return done / el * self.hs / N_KV, el, done
+
+    def describe(self, done):
+        return (f"{done} oracle steps (SET_ROWS of the new token + decode over 32768 cells) on "
+                f"{self.hs} of 8 KV heads, throughput scaled x{N_KV // self.hs}")
+
+
+def host_threads():
+    return int(os.environ.get("OMP_NUM_THREADS") or os.cpu_count() or 1)
+
+
+def run_reference(args):
+    rank, world, _ = dist_setup()
+    if rank != 0:
+        return
+    sample = OracleSample(1)
+    warm = max(0, args.warmup)
+    for _ in range(warm):
+        sample.step()
+    tok_s, el, done = sample.timed(max(1, args.steps), budget_s=90.0)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": done, "warmup": warm, "ms_per_step": 1000 * el / done, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode_32k", "kv_heads": N_KV, "q_heads": N_Q, "head_dim": D,
+                   "kv_len": KV_LEN, "type": "turbo3"},
+        "cpu_baseline": {"value": tok_s, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+                         "sample": sample.describe(done)},
+        "e2e": {"value": tok_s, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU path
+
+def run_tq(args):
+    import numpy as np
+    import torch
+
+    import quantized_kv_cache_tq_gb300 as tq
+    import workloads as W
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    algo = {"auto": tq.TQ_DECODE_AUTO, "lut": tq.TQ_DECODE_LUT, "mma": tq.TQ_DECODE_MMA}[args.algo]
+    sh = W.decode_32k()
+    sk, sv = W.codebook_signs(sh)
+    cbk, cbv = tq.codebook(3, sk), tq.codebook(3, sv)
+
+    # bulk quantisation of the whole cache (also timed as an extra: SET_ROWS at scale)
+    k_raw, v_raw = W.kv_inputs(sh)
+    k_src = torch.from_numpy(W.to_f32(k_raw)).to(dev)
+    v_src = torch.from_numpy(W.to_f32(v_raw)).to(dev)
+    del k_raw, v_raw
+    cells_all = torch.arange(KV_LEN, dtype=torch.int64, device=dev)
+    base_k = tq.TqCache(3, N_KV, D, KV_LEN, dev)
+    base_v = tq.TqCache(3, N_KV, D, KV_LEN, dev)
+    tq.set_rows(base_k, cbk, k_src, cells_all)
+    tq.set_rows(base_v, cbv, v_src, cells_all)
+    torch.cuda.synchronize()
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    cache_bytes = per_cache_bytes(3)
+    B = max(2, math.ceil(4 * l2 / cache_bytes))
+    ks, vs = [], []
+    for _ in range(B):
+        a, b = tq.TqCache(3, N_KV, D, KV_LEN, dev), tq.TqCache(3, N_KV, D, KV_LEN, dev)
+        for dst, src in ((a, base_k), (b, base_v)):
+            dst.norms.copy_(src.norms)
+            dst.qs.copy_(src.qs)
+            dst.signs.copy_(src.signs)
+        ks.append(a)
+        vs.append(b)
+
+    # per-layer inputs: query and the new token's K/V rows
+    q_all = torch.from_numpy(W.to_f32(W.normal(sh.seed, W.S_EXTRA, B * N_Q * D)).reshape(B, N_Q, D)).to(dev)
+    newk = torch.from_numpy(W.to_f32(W.normal(sh.seed, W.S_EXTRA + 1, B * N_KV * D)).reshape(B, 1, N_KV, D)).to(dev)
+    newv = torch.from_numpy(W.to_f32(W.normal(sh.seed, W.S_EXTRA + 2, B * N_KV * D)).reshape(B, 1, N_KV, D)).to(dev)
+    cell = torch.tensor([KV_LEN - 1], dtype=torch.int64, device=dev)
+    out = torch.empty((B, N_Q, D), dtype=torch.float32, device=dev)
+    ws_bytes = tq._lib.tq_fattn_decode_workspace(ks[0].c, vs[0].c, N_Q, KV_LEN)
+    ws = tq.workspace(ws_bytes, dev)
+    scale = 1.0 / math.sqrt(D)
+
+    def token(decode_only=False):
+        for b in range(B):
+            if not decode_only:
+                tq.set_rows(ks[b], cbk, newk[b], cell)
+                tq.set_rows(vs[b], cbv, newv[b], cell)
+            tq.fattn_decode(ks[b], vs[b], cbk, cbv, q_all[b], KV_LEN, scale, algo=algo, out=out[b], ws=ws)
+
+    def capture(fn):
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
+    g_token = capture(token)
+    g_decode = capture(lambda: token(decode_only=True))
+    T = args.tokens_per_step
+
+    def step():
+        for _ in range(T):
+            g_token.replay()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms = e0.elapsed_time(e1)
+        # dominant kernel alone: B decode launches per replay, distinct caches
+        R = 200
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(5):
+            g_decode.replay()
+        d0.record(stream)
+        for _ in range(R):
+            g_decode.replay()
+        d1.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(ms, world, dev)
+    dec_us = d0.elapsed_time(d1) * 1000.0 / (R * B)
+
+    calls = args.steps * T * B
+    value = calls * world / (ms / 1000.0)
+    dec_bytes = cache_bytes + 4 * (N_Q * D * 2)
+    achieved = dec_bytes / (dec_us * 1e-6) / 1e9
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    # e2e through the public API with host buffers: per step the T tokens' inputs go
+    # host->device from pinned memory and the last token's outputs come back
+    h_q = torch.empty((T, B, N_Q, D), dtype=torch.float32).pin_memory()
+    h_k = torch.empty((T, B, 1, N_KV, D), dtype=torch.float32).pin_memory()
+    h_v = torch.empty((T, B, 1, N_KV, D), dtype=torch.float32).pin_memory()
+    h_out = torch.empty((B, N_Q, D), dtype=torch.float32).pin_memory()
+    h_q.copy_(q_all.cpu().unsqueeze(0).expand(T, -1, -1, -1))
+    h_k.copy_(newk.cpu().unsqueeze(0).expand(T, -1, -1, -1, -1))
+    h_v.copy_(newv.cpu().unsqueeze(0).expand(T, -1, -1, -1, -1))
+    d_q = torch.empty((T, B, N_Q, D), dtype=torch.float32, device=dev)
+    d_k = torch.empty((T, B, 1, N_KV, D), dtype=torch.float32, device=dev)
+    d_v = torch.empty((T, B, 1, N_KV, D), dtype=torch.float32, device=dev)
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        for t in range(T):
+            q_all.copy_(d_q[t])
+            newk.copy_(d_k[t])
+            newv.copy_(d_v[t])
+            g_token.replay()
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    h2d = h_q.numel() * 4 + h_k.numel() * 4 + h_v.numel() * 4
+    d2h = h_out.numel() * 4
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        extras = run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(1)
+        sample.step()
+        tok_s, el, done = sample.timed(3, budget_s=15.0)
+        cpu = {"value": tok_s, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+               "sample": sample.describe(done)}
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "u8 codes; f16 tensor-core operands, f32 accumulate" if args.algo != "lut" else "u8 codes; f32",
+            "data": "synthetic",
+            "config": {"workload": "decode_32k", "kv_heads": N_KV, "q_heads": N_Q, "head_dim": D,
+                       "kv_len": KV_LEN, "type": "turbo3", "layers_cycled": B, "tokens_per_step": T,
+                       "algo": args.algo, "l2": f"working set {B} caches x {cache_bytes / 1e6:.1f} MB > 4x L2 "
+                                                 f"({l2 / 1e6:.0f} MB); no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "kernel": "decode",
+                         "kernel_us": dec_us, "bytes_per_launch": dec_bytes, "peak_source": peak_src},
+            "e2e": {"value": calls * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * calls,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def time_graph(torch, fn, reps=20, warm=3):
+    s = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(s)
+    for _ in range(reps):
+        fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps / 1000.0
+
+
+def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak):
+    """Other rows of the hot path, measured on their own workloads."""
+    ex = {}
+    # SET_ROWS over the whole 32K cache (K and V): read fp32 rows, write packed planes
+    def bulk():
+        tq.set_rows(base_k, cbk, k_src, cells_all)
+        tq.set_rows(base_v, cbv, v_src, cells_all)
+    t = time_graph(torch, bulk, reps=10)
+    nbytes = 2 * (k_src.numel() * 4 + N_KV * KV_LEN * 50) + 2 * KV_LEN * 8
+    ex["set_rows_bulk"] = {"workload": "32768 rows x 8 KV heads x 128, K and V, f32 -> turbo3",
+                           "ms": t * 1e3, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak}
+    return ex
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_tq(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -299,16 +299,20 @@ def set_rows(cache: Cache, src: np.ndarray, cell_ids: np.ndarray, sign_bits, cen
     """Quantise rows src [n_rows][H][D] into cells cell_ids (in place); returns
     the rotated values y [n_rows][H][nb][128] for boundary-distance checks.
     Cell ids must be distinct."""
-    src = np.asarray(src, dtype=np.float64)
-    blocks = _pad_blocks(src, cache.head_dim)                   # [n][H][nb][128]
-    norm_bits, codes, y = quantize_blocks(blocks, sign_bits, cents)
-    qs, signs = pack_codes(codes, cache.tq_type)
-    for r, cell in enumerate(np.asarray(cell_ids, dtype=np.int64)):
-        cache.norms[:, cell] = norm_bits[r]
-        cache.qs[:, cell] = qs[r]
+    src = np.asarray(src)
+    cell_ids = np.asarray(cell_ids, dtype=np.int64)
+    ys = []
+    for lo in range(0, src.shape[0], 2048):              # row batches bound the memory use
+        blocks = _pad_blocks(np.asarray(src[lo:lo + 2048], dtype=np.float64), cache.head_dim)
+        norm_bits, codes, y = quantize_blocks(blocks, sign_bits, cents)   # [n][H][nb][...]
+        qs, signs = pack_codes(codes, cache.tq_type)
+        cells = cell_ids[lo:lo + 2048]
+        cache.norms[:, cells] = norm_bits.transpose(1, 0, 2)
+        cache.qs[:, cells] = qs.transpose(1, 0, 2, 3)
         if signs is not None:
-            cache.signs[:, cell] = signs[r]
-    return y
+            cache.signs[:, cells] = signs.transpose(1, 0, 2, 3)
+        ys.append(y)
+    return np.concatenate(ys) if ys else np.zeros((0, cache.n_kv_heads, cache.n_blocks, QK))
 
 
 def dequantize_cache(cache: Cache, sign_bits, cents: np.ndarray, n: int, head: int | None = None):

@@ -1,0 +1,6 @@
+// turbo2 instantiation of the tensor-core decode kernel.
+#include "tq_decode_mma.cuh"
+
+namespace tq {
+cudaError_t launch_decode_mma_t2(const DecodeArgs &a, cudaStream_t s) { return mmadec::launch_type<2>(a, s); }
+}  // namespace tq

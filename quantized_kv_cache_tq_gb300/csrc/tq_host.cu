@@ -1,0 +1,345 @@
+// Host side of the C ABI: argument checks, workspace layout, codebook
+// construction and kernel dispatch.  Nothing here allocates device memory,
+// synchronises or reads device memory except tq_workspace_status, so every
+// compute call can be captured into a CUDA graph ([HIP#28] "1. Graph-safe
+// decode": the page's crash came from cudaMalloc/cudaFree during capture).
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+// ---------------------------------------------------------------- device info
+
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 152;
+  }
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+    cudaGetLastError();
+    v = 152;
+  }
+  cached[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int64_t kv_len,
+                                    int /*algo*/) {
+  DecodeWorkspaceLayout L;
+  const int target_ctas = 2 * sm_count();
+  const int per_head = (target_ctas + n_kv_heads - 1) / n_kv_heads;
+  int64_t chunk = (kv_len + per_head - 1) / per_head;
+  chunk = (chunk + 63) / 64 * 64;
+  if (chunk < 128) chunk = 128;
+  L.chunk = chunk;
+  L.n_splits = kv_len > 0 ? static_cast<int>((kv_len + chunk - 1) / chunk) : 1;
+  L.counters_off = kWsHeader;
+  L.part_off = L.counters_off + round_up(sizeof(int32_t) * n_kv_heads, 256);
+  const size_t stride = 2 + 128 * static_cast<size_t>(nbv);
+  L.total = L.part_off + round_up(sizeof(float) * n_q_heads * L.n_splits * stride, 256);
+  return L;
+}
+
+// ------------------------------------------------------------- binary16 / codebook
+
+// Nearest binary16 value of x (round to nearest, ties to even), as a double.
+static double round_to_binary16(double x) {
+  if (x == 0.0 || !isfinite(x)) return x;
+  const double ax = fabs(x);
+  int e = 0;
+  frexp(ax, &e);               // ax = m 2^e, m in [0.5, 1)
+  const int E = e - 1;         // ax in [2^E, 2^(E+1))
+  double q;
+  if (E < -14) q = nearbyint(ax * 0x1p24) * 0x1p-24;              // subnormal spacing
+  else q = nearbyint(ldexp(ax, 10 - E)) * ldexp(1.0, E - 10);    // 11 significant bits
+  if (q > 65504.0) q = INFINITY;
+  return copysign(q, x);
+}
+
+// P(a < X < b), X ~ N(0,1), from erfc on the side without cancellation.
+static double gauss_prob(double a, double b) {
+  const double r = 0.70710678118654752440;
+  if (a >= 0) return 0.5 * (erfc(a * r) - erfc(b * r));
+  if (b <= 0) return 0.5 * (erfc(-b * r) - erfc(-a * r));
+  return 1.0 - 0.5 * erfc(-a * r) - 0.5 * erfc(b * r);
+}
+
+static double gauss_pdf(double x) {
+  return isinf(x) ? 0.0 : exp(-0.5 * x * x) * 0.39894228040143267794;
+}
+
+// Lloyd-Max quantiser of N(0,1): thresholds at midpoints, centroids at the
+// conditional means E[X | cell], repeated to a fixed point.
+static void lloyd_max(int n, double *c) {
+  for (int k = 0; k < n; ++k) c[k] = (k - 0.5 * (n - 1)) * (4.0 / n);
+  double t[17];
+  for (int it = 0; it < 200000; ++it) {
+    t[0] = -INFINITY;
+    t[n] = INFINITY;
+    for (int k = 1; k < n; ++k) t[k] = 0.5 * (c[k - 1] + c[k]);
+    double delta = 0.0;
+    for (int k = 0; k < n; ++k) {
+      const double nk = (gauss_pdf(t[k]) - gauss_pdf(t[k + 1])) / gauss_prob(t[k], t[k + 1]);
+      delta = fmax(delta, fabs(nk - c[k]));
+      c[k] = nk;
+    }
+    if (delta < 1e-15) break;
+  }
+}
+
+static int n_centroids_of(int type) {
+  return type == TQ_TURBO2 ? 4 : type == TQ_TURBO3 ? 8 : type == TQ_TURBO4 ? 16 : 0;
+}
+
+static bool codebook_ok(const tq_codebook *cb, int type) {
+  const int n = n_centroids_of(type);
+  if (!cb || n == 0 || cb->n_centroids != n) return false;
+  for (int i = 0; i < n; ++i) {
+    const float c = cb->centroids[i];
+    if (!isfinite(c)) return false;
+    if (i + 1 < n && !(c < cb->centroids[i + 1])) return false;
+    if (c != -cb->centroids[n - 1 - i]) return false;
+    if (round_to_binary16(c) != static_cast<double>(c)) return false;
+  }
+  return cb->centroids[n / 2] > 0.f;
+}
+
+static DevCodebook to_dev(const tq_codebook *cb) {
+  DevCodebook d;
+  memset(&d, 0, sizeof(d));
+  for (int i = 0; i < 4; ++i) d.sign_bits[i] = cb->sign_bits[i];
+  d.n = cb->n_centroids;
+  for (int i = 0; i < cb->n_centroids && i < 16; ++i) d.c[i] = cb->centroids[i];
+  return d;
+}
+
+// ------------------------------------------------------------------ checks
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static tq_status check_cache(const tq_cache *c) {
+  if (!c) return TQ_ERR_INVALID_ARG;
+  if (n_centroids_of(c->type) == 0) return TQ_ERR_INVALID_ARG;
+  if (c->n_kv_heads <= 0 || c->head_dim <= 0 || c->head_dim % 8 != 0 || c->head_dim > 1 << 16)
+    return TQ_ERR_INVALID_ARG;
+  if (c->n_blocks != (c->head_dim + 127) / 128) return TQ_ERR_INVALID_ARG;
+  if (c->n_cells <= 0 || c->n_cells % 64 != 0) return TQ_ERR_INVALID_ARG;
+  if (!c->norms || !c->qs || !aligned16(c->norms) || !aligned16(c->qs)) return TQ_ERR_INVALID_ARG;
+  if (c->type == TQ_TURBO3 && (!c->signs || !aligned16(c->signs))) return TQ_ERR_INVALID_ARG;
+  return TQ_OK;
+}
+
+static tq_status map_cuda(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" {
+
+const char *tq_status_string(int status) {
+  switch (status) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_INVALID_ARG: return "invalid argument";
+    case TQ_ERR_UNSUPPORTED: return "unsupported combination";
+    case TQ_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case TQ_ERR_CUDA: return "CUDA runtime error";
+    case TQ_ERR_TIMEOUT: return "device-side wait timed out";
+    case TQ_ERR_DEVICE_CHECK: return "device-side input check failed";
+    default: return "unknown status";
+  }
+}
+
+int tq_version(void) { return 100; }
+
+tq_status tq_codebook_init(int type, const uint32_t sign_bits[4], tq_codebook *out) {
+  const int n = n_centroids_of(type);
+  if (n == 0 || !sign_bits || !out) return TQ_ERR_INVALID_ARG;
+  double c[16];
+  lloyd_max(n, c);
+  // enforce exact symmetry before rounding: average the mirrored pair
+  memset(out, 0, sizeof(*out));
+  for (int i = 0; i < 4; ++i) out->sign_bits[i] = sign_bits[i];
+  out->n_centroids = n;
+  for (int i = 0; i < n / 2; ++i) {
+    const double m = 0.5 * (c[n - 1 - i] - c[i]) / sqrt(128.0);
+    const float r = static_cast<float>(round_to_binary16(m));
+    out->centroids[n - 1 - i] = r;
+    out->centroids[i] = -r;
+  }
+  return TQ_OK;
+}
+
+tq_status tq_cache_plane_bytes(int type, int n_kv_heads, int head_dim, int64_t n_cells,
+                               size_t *norms_bytes, size_t *qs_bytes, size_t *signs_bytes) {
+  if (n_centroids_of(type) == 0 || n_kv_heads <= 0 || head_dim <= 0 || n_cells <= 0 ||
+      !norms_bytes || !qs_bytes || !signs_bytes)
+    return TQ_ERR_INVALID_ARG;
+  const size_t blocks = static_cast<size_t>(n_kv_heads) * n_cells * ((head_dim + 127) / 128);
+  *norms_bytes = blocks * 2;
+  *qs_bytes = blocks * (type == TQ_TURBO4 ? 64 : 32);
+  *signs_bytes = type == TQ_TURBO3 ? blocks * 16 : 0;
+  return TQ_OK;
+}
+
+tq_status tq_set_rows(const tq_cache *dst, const tq_codebook *cb, const void *src, int src_type,
+                      const int64_t *cell_ids, int64_t n_rows, int32_t *dev_status,
+                      tq_stream stream) {
+  tq_status st = check_cache(dst);
+  if (st != TQ_OK) return st;
+  if (!codebook_ok(cb, dst->type)) return TQ_ERR_INVALID_ARG;
+  if (src_type != TQ_F32 && src_type != TQ_F16 && src_type != TQ_BF16) return TQ_ERR_INVALID_ARG;
+  if (n_rows < 0) return TQ_ERR_INVALID_ARG;
+  if (n_rows == 0) return TQ_OK;
+  if (!src || !aligned16(src) || !cell_ids || (reinterpret_cast<uintptr_t>(cell_ids) & 7u))
+    return TQ_ERR_INVALID_ARG;
+  if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return TQ_ERR_INVALID_ARG;
+  const int64_t warps = n_rows * dst->n_kv_heads * dst->n_blocks;
+  if ((warps + 7) / 8 > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;
+  SetRowsArgs a;
+  a.src = src;
+  a.cell_ids = cell_ids;
+  a.dev_status = dev_status;
+  a.norms = static_cast<uint16_t *>(dst->norms);
+  a.qs = static_cast<uint8_t *>(dst->qs);
+  a.signs = static_cast<uint8_t *>(dst->signs);
+  a.n_rows = n_rows;
+  a.n_cells = dst->n_cells;
+  a.n_kv_heads = dst->n_kv_heads;
+  a.head_dim = dst->head_dim;
+  a.n_blocks = dst->n_blocks;
+  a.cb = to_dev(cb);
+  return map_cuda(launch_set_rows(dst->type, src_type, a, static_cast<cudaStream_t>(stream)));
+}
+
+static tq_status check_kv_pair(const tq_cache *k, const tq_cache *v, int n_q_heads, int64_t kv_len) {
+  tq_status st = check_cache(k);
+  if (st != TQ_OK) return st;
+  st = check_cache(v);
+  if (st != TQ_OK) return st;
+  if (k->n_kv_heads != v->n_kv_heads || k->n_cells != v->n_cells) return TQ_ERR_INVALID_ARG;
+  if (n_q_heads <= 0 || n_q_heads % k->n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+  if (kv_len < 0 || kv_len > k->n_cells) return TQ_ERR_INVALID_ARG;
+  return TQ_OK;
+}
+
+size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_heads,
+                                 int64_t kv_len) {
+  if (check_kv_pair(k, v, n_q_heads, kv_len) != TQ_OK) return 0;
+  return decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, TQ_DECODE_AUTO).total;
+}
+
+tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                          const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
+                          float scale, int algo, float *out, void *workspace,
+                          size_t workspace_bytes, tq_stream stream) {
+  tq_status st = check_kv_pair(k, v, n_q_heads, kv_len);
+  if (st != TQ_OK) return st;
+  if (!codebook_ok(cbk, k->type) || !codebook_ok(cbv, v->type)) return TQ_ERR_INVALID_ARG;
+  if (!q || !out || !aligned16(q) || !aligned16(out) || !isfinite(scale)) return TQ_ERR_INVALID_ARG;
+  if (algo != TQ_DECODE_AUTO && algo != TQ_DECODE_LUT && algo != TQ_DECODE_MMA)
+    return TQ_ERR_INVALID_ARG;
+  const int group = n_q_heads / k->n_kv_heads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kv_len == 0)
+    return map_cuda(cudaMemsetAsync(out, 0, sizeof(float) * n_q_heads * v->head_dim, s));
+  const bool mma_ok = decode_mma_supported(k->type, v->type, group, k->n_blocks, v->n_blocks);
+  const bool lut_ok = group <= 8 && k->n_blocks <= 2 && v->n_blocks <= 2;
+  int use = algo;
+  if (use == TQ_DECODE_AUTO) use = mma_ok ? TQ_DECODE_MMA : TQ_DECODE_LUT;
+  if ((use == TQ_DECODE_MMA && !mma_ok) || (use == TQ_DECODE_LUT && !lut_ok))
+    return TQ_ERR_UNSUPPORTED;
+  const DecodeWorkspaceLayout L = decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, use);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TQ_ERR_WORKSPACE;
+  if (workspace_bytes < L.total) return TQ_ERR_WORKSPACE;
+
+  DecodeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.kn = static_cast<const uint16_t *>(k->norms);
+  a.kqs = static_cast<const uint8_t *>(k->qs);
+  a.ksg = static_cast<const uint8_t *>(k->signs);
+  a.vn = static_cast<const uint16_t *>(v->norms);
+  a.vqs = static_cast<const uint8_t *>(v->qs);
+  a.vsg = static_cast<const uint8_t *>(v->signs);
+  a.q = q;
+  a.out = out;
+  a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.part_off);
+  a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.counters_off);
+  a.status = static_cast<int32_t *>(workspace);
+  a.n_cells = k->n_cells;
+  a.kv_len = kv_len;
+  a.chunk = L.chunk;
+  a.n_splits = L.n_splits;
+  a.n_kv_heads = k->n_kv_heads;
+  a.group = group;
+  a.dk = k->head_dim;
+  a.dv = v->head_dim;
+  a.nbk = k->n_blocks;
+  a.nbv = v->n_blocks;
+  a.part_stride = 2 + 128 * v->n_blocks;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.cbk = to_dev(cbk);
+  a.cbv = to_dev(cbv);
+  cudaError_t e = (use == TQ_DECODE_MMA) ? launch_decode_mma(k->type, v->type, a, s)
+                                         : launch_decode_lut(k->type, v->type, a, s);
+  return map_cuda(e);
+}
+
+size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads,
+                                  int64_t kv_len) {
+  (void)k; (void)v; (void)nq; (void)n_q_heads; (void)kv_len;
+  return 0;
+}
+
+tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                           const tq_codebook *cbv, const void *q, int q_type, int nq,
+                           int n_q_heads, int64_t kv_len, float scale, int causal, float *out,
+                           void *workspace, size_t workspace_bytes, tq_stream stream) {
+  (void)k; (void)v; (void)cbk; (void)cbv; (void)q; (void)q_type; (void)nq; (void)n_q_heads;
+  (void)kv_len; (void)scale; (void)causal; (void)out; (void)workspace; (void)workspace_bytes;
+  (void)stream;
+  return TQ_ERR_UNSUPPORTED;
+}
+
+size_t tq_int8_prompt_attn_workspace(int nq, int n_q_heads, int n_kv_heads, int head_dim,
+                                     int64_t ctx) {
+  (void)nq; (void)n_q_heads; (void)n_kv_heads; (void)head_dim; (void)ctx;
+  return 0;
+}
+
+tq_status tq_int8_prompt_attn(const int8_t *k, const uint16_t *k_scale, const int8_t *v,
+                              const uint16_t *v_scale, int64_t n_cells, const int32_t *cell_of_pos,
+                              int64_t ctx, const uint16_t *q, int nq, int n_q_heads,
+                              int n_kv_heads, int head_dim, float scale, int causal, float *out,
+                              void *workspace, size_t workspace_bytes, tq_stream stream) {
+  (void)k; (void)k_scale; (void)v; (void)v_scale; (void)n_cells; (void)cell_of_pos; (void)ctx;
+  (void)q; (void)nq; (void)n_q_heads; (void)n_kv_heads; (void)head_dim; (void)scale;
+  (void)causal; (void)out; (void)workspace; (void)workspace_bytes; (void)stream;
+  return TQ_ERR_UNSUPPORTED;
+}
+
+tq_status tq_workspace_status(void *workspace, size_t workspace_bytes, int32_t *status_out,
+                              tq_stream stream) {
+  if (!workspace || workspace_bytes < kWsHeader || !status_out) return TQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemsetAsync(workspace, 0, sizeof(v), s) != cudaSuccess)
+    return TQ_ERR_CUDA;
+  *status_out = v;
+  return TQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/tq.h"
+
+namespace tq {
+
+// Codebook as the kernels receive it (by value, in the launch parameters).
+struct DevCodebook {
+  uint32_t sign_bits[4];
+  int32_t n;
+  float c[16];
+};
+
+struct SetRowsArgs {
+  const void *src;
+  const int64_t *cell_ids;
+  int32_t *dev_status;
+  uint16_t *norms;
+  uint8_t *qs;
+  uint8_t *signs;
+  int64_t n_rows;
+  int64_t n_cells;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t n_blocks;
+  DevCodebook cb;
+};
+
+// Everything a decode kernel needs; the partial results of split s of query
+// head h live at part + (h * n_splits + s) * part_stride as
+// [m (log2 domain), l, o'[0 .. 128*nbv)] (o' unnormalised, rotated domain).
+struct DecodeArgs {
+  const uint16_t *kn;
+  const uint8_t *kqs;
+  const uint8_t *ksg;
+  const uint16_t *vn;
+  const uint8_t *vqs;
+  const uint8_t *vsg;
+  const float *q;
+  float *out;
+  float *part;
+  int32_t *counters;
+  int32_t *status;        // workspace status word (device-side errors)
+  int64_t n_cells;
+  int64_t kv_len;
+  int64_t chunk;
+  int32_t n_splits;
+  int32_t n_kv_heads;
+  int32_t group;          // query heads per KV head
+  int32_t dk, dv;         // logical head dims
+  int32_t nbk, nbv;       // 128-blocks of K / V rows
+  int32_t part_stride;    // floats per (head, split) partial
+  float scale_log2;       // softmax scale * log2(e)
+  DevCodebook cbk, cbv;
+};
+
+struct DecodeWorkspaceLayout {
+  size_t counters_off, part_off, total;
+  int n_splits;
+  int64_t chunk;
+};
+
+constexpr size_t kWsHeader = 256;   // status word lives at offset 0
+
+int sm_count();
+DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int64_t kv_len, int algo);
+
+cudaError_t launch_set_rows(int type, int src_type, const SetRowsArgs &a, cudaStream_t s);
+cudaError_t launch_decode_lut(int ktype, int vtype, const DecodeArgs &a, cudaStream_t s);
+bool decode_mma_supported(int ktype, int vtype, int group, int nbk, int nbv);
+cudaError_t launch_decode_mma(int ktype, int vtype, const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_decode_mma_t2(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_decode_mma_t3(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_decode_mma_t4(const DecodeArgs &a, cudaStream_t s);
+
+}  // namespace tq

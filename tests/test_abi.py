@@ -1,0 +1,123 @@
+"""C-ABI library checks that need no GPU: it loads, exports every declared
+symbol, and its host-side logic (codebook, sizes, argument checks) is right."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _lib():
+    try:
+        from quantized_kv_cache_tq_gb300 import _lib
+    except ImportError as e:
+        pytest.fail(f"libtq.so not built: {e}")
+    return _lib
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "tq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol():
+    L = _lib()
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L.lib, n), f"{n} not exported"
+    assert set(names) == set(L.EXPORTED)
+
+
+def test_nm_lists_symbols_as_extern_c():
+    import subprocess
+    L = _lib()
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in _declared():
+        assert n in syms
+
+
+@pytest.mark.parametrize("t", [2, 3, 4])
+def test_codebook_matches_oracle(t):
+    L = _lib()
+    sb = W.sign_bits(3, W.S_SIGNS_K)
+    cb = L.tq_codebook_init(t, sb)
+    n = O.N_CENTROIDS[t]
+    assert cb.n_centroids == n
+    assert list(cb.sign_bits) == [int(x) for x in sb]
+    lib_c = np.array(cb.centroids[:n], dtype=np.float64)
+    assert np.array_equal(lib_c, O.centroids(t))
+
+
+def test_plane_bytes():
+    L = _lib()
+    assert L.tq_cache_plane_bytes(3, 8, 128, 32768) == (8 * 32768 * 2, 8 * 32768 * 32, 8 * 32768 * 16)
+    assert L.tq_cache_plane_bytes(4, 16, 192, 64) == (16 * 64 * 2 * 2, 16 * 64 * 2 * 64, 0)
+    assert L.tq_cache_plane_bytes(2, 1, 128, 64)[2] == 0
+
+
+def test_status_strings():
+    L = _lib()
+    for s in range(7):
+        assert L.status_string(s)
+    assert L.status_string(0) == "ok"
+
+
+def _fake_cache(L, t=3, h=2, d=128, n=64, ptr=1 << 20):
+    return L.tq_cache(t, h, d, (d + 127) // 128, n, ptr, ptr + (1 << 16), ptr + (1 << 18))
+
+
+def test_host_argument_checks_reject_before_launch():
+    # every call below must be rejected on the host: no device is touched
+    L = _lib()
+    cb = L.tq_codebook_init(3, [1, 2, 3, 4])
+    good = _fake_cache(L)
+    bad_cells = _fake_cache(L, n=100)                 # not a multiple of 64
+    bad_blocks = L.tq_cache(3, 2, 128, 2, 64, 1 << 20, 1 << 21, 1 << 22)
+    misaligned = _fake_cache(L, ptr=(1 << 20) + 8)
+    no_signs = L.tq_cache(3, 2, 128, 1, 64, 1 << 20, 1 << 21, 0)
+    for c in (bad_cells, bad_blocks, misaligned, no_signs):
+        assert L.tq_set_rows(c, cb, 1 << 23, L.TQ_F32, 1 << 24, 4, None, None) == L.TQ_ERR_INVALID_ARG
+    # wrong codebook for the type, non-symmetric or non-binary16 centroids
+    cb2 = L.tq_codebook_init(2, [0, 0, 0, 0])
+    assert L.tq_set_rows(good, cb2, 1 << 23, L.TQ_F32, 1 << 24, 4, None, None) == L.TQ_ERR_INVALID_ARG
+    cb3 = L.tq_codebook_init(3, [0, 0, 0, 0])
+    cb3.centroids[0] = cb3.centroids[0] * 1.0001
+    assert L.tq_set_rows(good, cb3, 1 << 23, L.TQ_F32, 1 << 24, 4, None, None) == L.TQ_ERR_INVALID_ARG
+    # null source, bad dtype, negative rows; zero rows is a no-op
+    assert L.tq_set_rows(good, cb, None, L.TQ_F32, 1 << 24, 4, None, None) == L.TQ_ERR_INVALID_ARG
+    assert L.tq_set_rows(good, cb, 1 << 23, 7, 1 << 24, 4, None, None) == L.TQ_ERR_INVALID_ARG
+    assert L.tq_set_rows(good, cb, 1 << 23, L.TQ_F32, 1 << 24, -1, None, None) == L.TQ_ERR_INVALID_ARG
+    assert L.tq_set_rows(good, cb, 1 << 23, L.TQ_F32, 1 << 24, 0, None, None) == L.TQ_OK
+    # decode: kv_len beyond the cache, head-count mismatch, workspace too small
+    k, v = _fake_cache(L), _fake_cache(L)
+    assert L.tq_fattn_decode_workspace(k, v, 4, 65) == 0
+    assert L.tq_fattn_decode(k, v, cb, cb, 1 << 23, 4, 65, 0.1, 0, 1 << 24, 1 << 25, 1 << 20,
+                             None) == L.TQ_ERR_INVALID_ARG
+    assert L.tq_fattn_decode(k, v, cb, cb, 1 << 23, 3, 64, 0.1, 0, 1 << 24, 1 << 25, 1 << 20,
+                             None) == L.TQ_ERR_INVALID_ARG
+    need = L.tq_fattn_decode_workspace(k, v, 4, 64)
+    assert need > 0
+    assert L.tq_fattn_decode(k, v, cb, cb, 1 << 23, 4, 64, 0.1, 0, 1 << 24, 1 << 25, need - 1,
+                             None) == L.TQ_ERR_WORKSPACE
+    assert L.tq_fattn_decode(k, v, cb, cb, 1 << 23, 4, 64, 0.1, 0, 1 << 24, (1 << 25) + 16, need,
+                             None) == L.TQ_ERR_WORKSPACE
+    assert L.tq_fattn_decode(k, v, cb, cb, 1 << 23, 4, 64, 0.1, 9, 1 << 24, 1 << 25, need,
+                             None) == L.TQ_ERR_INVALID_ARG
+
+
+def test_decode_workspace_grows_with_splits():
+    L = _lib()
+    k = _fake_cache(L, h=8, n=32768)
+    small = L.tq_fattn_decode_workspace(k, k, 32, 512)
+    big = L.tq_fattn_decode_workspace(k, k, 32, 32768)
+    assert 0 < small < big
+    assert big % 256 == 0

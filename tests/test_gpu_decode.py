@@ -1,0 +1,132 @@
+"""Split-KV single-query decode on the GPU vs the f64 oracle, on the same
+oracle-quantised cache (max-abs <= 2e-3, NMSE <= 1e-6)."""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from tests._helpers import compare_outputs, oracle_cache, scale_of, upload
+
+pytestmark = pytest.mark.gpu
+
+ALGOS = ["lut", "mma"]
+
+
+def _algo(name):
+    import quantized_kv_cache_tq_gb300 as tq
+    return {"lut": tq.TQ_DECODE_LUT, "mma": tq.TQ_DECODE_MMA, "auto": tq.TQ_DECODE_AUTO}[name]
+
+
+def _setup(sh, ktype, vtype, n_rows=None):
+    k, v = W.kv_inputs(sh, n_rows)
+    sk, sv = W.codebook_signs(sh)
+    kc = oracle_cache(ktype, k, sk)
+    vc = oracle_cache(vtype, v, sv)
+    return kc, vc, sk, sv
+
+
+def _decode_pair(kc, vc, sk, sv, q, kv_len, algo):
+    import torch
+    import quantized_kv_cache_tq_gb300 as tq
+    gk, gv = upload(kc), upload(vc)
+    cbk, cbv = tq.codebook(kc.tq_type, sk), tq.codebook(vc.tq_type, sv)
+    out = tq.fattn_decode(gk, gv, cbk, cbv, torch.from_numpy(W.to_f32(q)).cuda(), kv_len,
+                          scale_of(kc.head_dim), algo=_algo(algo))
+    torch.cuda.synchronize()
+    ref = O.decode(kc, vc, sk, sv, O.centroids(kc.tq_type), O.centroids(vc.tq_type),
+                   W.to_f32(q).astype(np.float64), kv_len, scale_of(kc.head_dim))
+    return out.cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_tiny_decode(algo):
+    sh = W.tiny_decode()
+    kc, vc, sk, sv = _setup(sh, 3, 3)
+    q = W.decode_query(sh)
+    out, ref = _decode_pair(kc, vc, sk, sv, q, sh.kv_len, algo)
+    compare_outputs(out, ref)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("kv_len", [1, 63, 127, 129, 1000, 2049])
+def test_ragged_lengths(algo, kv_len):
+    sh = W.decode_32k()
+    kc, vc, sk, sv = _setup(sh, 3, 3, n_rows=2112)
+    q = W.decode_query(sh)
+    out, ref = _decode_pair(kc, vc, sk, sv, q, kv_len, algo)
+    compare_outputs(out, ref)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("types", [(2, 2), (4, 4), (3, 2), (2, 4)])
+def test_types(algo, types):
+    if algo == "mma" and types[0] != types[1]:
+        pytest.skip("the tensor-core decode takes K and V of one type (AUTO falls back to the LUT kernel)")
+    sh = W.decode_32k()
+    kc, vc, sk, sv = _setup(sh, types[0], types[1], n_rows=3000)
+    q = W.decode_query(sh)
+    out, ref = _decode_pair(kc, vc, sk, sv, q, 3000, algo)
+    compare_outputs(out, ref)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_asymmetric_192_128(algo):
+    sh = W.asym_8k()
+    kc, vc, sk, sv = _setup(sh, 3, 3, n_rows=1500)
+    q = W.decode_query(sh)
+    out, ref = _decode_pair(kc, vc, sk, sv, q, 1500, algo)
+    compare_outputs(out, ref)
+
+
+def test_kv_len_zero_gives_zeros():
+    import torch
+    import quantized_kv_cache_tq_gb300 as tq
+    sk = W.sign_bits(0, W.S_SIGNS_K)
+    gk, gv = tq.TqCache(3, 2, 128, 64), tq.TqCache(3, 2, 128, 64)
+    cb = tq.codebook(3, sk)
+    out = torch.full((4, 128), 7.0, device="cuda")
+    tq.fattn_decode(gk, gv, cb, cb, torch.ones(4, 128, device="cuda"), 0, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_full_decode_32k(algo):
+    # the full 32K-context workload: 8 KV heads x 32 query heads, turbo3 K and V
+    sh = W.decode_32k()
+    kc, vc, sk, sv = _setup(sh, 3, 3)
+    q = W.decode_query(sh)
+    out, ref = _decode_pair(kc, vc, sk, sv, q, sh.kv_len, algo)
+    err, nm = compare_outputs(out, ref)
+    print(f"decode 32K {algo}: max-abs {err:.2e} nmse {nm:.2e}")
+
+
+def test_graph_replay_and_workspace_reuse():
+    # captured into a CUDA graph; replays reuse the self-resetting workspace
+    import torch
+    import quantized_kv_cache_tq_gb300 as tq
+    sh = W.decode_32k()
+    kc, vc, sk, sv = _setup(sh, 3, 3, n_rows=4096)
+    gk, gv = upload(kc), upload(vc)
+    cbk, cbv = tq.codebook(3, sk), tq.codebook(3, sv)
+    q = torch.from_numpy(W.to_f32(W.decode_query(sh))).cuda()
+    ws = tq.workspace(tq._lib.tq_fattn_decode_workspace(gk.c, gv.c, 32, 4096))
+    out = torch.empty(32, 128, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        tq.fattn_decode(gk, gv, cbk, cbv, q, 4096, out=out, ws=ws)     # warm-up
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    first = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tq.fattn_decode(gk, gv, cbk, cbv, q, 4096, out=out, ws=ws)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, first)
+    ref = O.decode(kc, vc, sk, sv, O.centroids(3), O.centroids(3), q.cpu().numpy().astype(np.float64),
+                   4096, scale_of(128))
+    compare_outputs(out.cpu().numpy(), ref)
