@@ -118,4 +118,68 @@ __device__ __forceinline__ void set_status(int32_t *st, int32_t code) {
   if (st) atomicCAS(st, 0, code);
 }
 
+
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t s) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
+  return d;
+}
+
+// ---- register dequantisation of packed codes into binary16 values
+// A code nibble (3 bits for turbo2/3, 4 bits for turbo4) is used as a prmt
+// byte selector into tables holding the low / high bytes of the binary16 code
+// values, so four codes become two half2 registers in 4 byte permutes.
+// Byte tables of the binary16 code values: l0/l1 low bytes of values 0..3 / 4..7,
+// h0/h1 the high bytes.  turbo2/3: value of code k; turbo4: magnitude j (the sign
+// is applied separately from bit 3 of the code).
+struct Tab {
+  uint32_t l0, l1, h0, h1;
+};
+
+template <int T>
+__device__ __forceinline__ Tab make_tab(const DevCodebook &cb) {
+  constexpr int NC = TypeTraits<T>::NC;
+  uint32_t v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float f = 0.f;
+    if (T == 4) f = cb.c[8 + k];
+    else if (k < NC) f = code_value(cb.c, NC, k);
+    v[k] = __half_as_ushort(__float2half_rn(f));
+  }
+  Tab t;
+  t.l0 = (v[0] & 0xff) | (v[1] & 0xff) << 8 | (v[2] & 0xff) << 16 | (v[3] & 0xff) << 24;
+  t.l1 = (v[4] & 0xff) | (v[5] & 0xff) << 8 | (v[6] & 0xff) << 16 | (v[7] & 0xff) << 24;
+  t.h0 = (v[0] >> 8) | (v[1] >> 8) << 8 | (v[2] >> 8) << 16 | (v[3] >> 8) << 24;
+  t.h1 = (v[4] >> 8) | (v[5] >> 8) << 8 | (v[6] >> 8) << 16 | (v[7] >> 8) << 24;
+  return t;
+}
+
+// Four codes in the low 16 bits of `sel` (one per nibble) -> two half2 registers
+// (code0, code1) and (code2, code3).
+template <int T>
+__device__ __forceinline__ void dq4(uint32_t sel, const Tab &t, uint32_t &h01, uint32_t &h23) {
+  const uint32_t s = (T == 4) ? (sel & 0x7777u) : sel;
+  const uint32_t lo = prmt_b32(t.l0, t.l1, s);
+  uint32_t hi = prmt_b32(t.h0, t.h1, s);
+  if (T == 4) hi |= prmt_b32(0x80808080u, 0u, ((sel >> 1) & 0x4444u) | 0x3210u);   // sign bit 3 == 0 -> negative
+  h01 = prmt_b32(lo, hi, 0x5140u);
+  h23 = prmt_b32(lo, hi, 0x7362u);
+}
+
+// turbo2/3 selector words of one 16-element qs word: sel0 = elements 0..7,
+// sel1 = elements 8..15, one 3-bit code per nibble.  `sg` is the signs word of
+// the 32-element group, `odd` whether the qs word is the second of the group.
+template <int T>
+__device__ __forceinline__ void sel_words(uint32_t w, uint32_t sg, bool odd, uint32_t &sel0, uint32_t &sel1) {
+  sel0 = w & 0x33333333u;
+  sel1 = (w >> 2) & 0x33333333u;
+  if (T == 3) {
+    const uint32_t s0 = odd ? (sg << 2) : sg;
+    const uint32_t s1 = odd ? (sg << 1) : (sg >> 1);
+    sel0 |= s0 & 0x44444444u;
+    sel1 |= s1 & 0x44444444u;
+  }
+}
+
 }  // namespace tq

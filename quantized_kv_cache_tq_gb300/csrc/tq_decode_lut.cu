@@ -223,7 +223,7 @@ cudaError_t launch_kt_vt(const DecodeArgs &a, cudaStream_t s) {
   const LutSmem L = lut_smem<KT, VT>(a.group, a.nbk, a.nbv);
   // the merge reuses the table region: it must hold group * 128 * nbv floats
   size_t bytes = L.total;
-  const size_t merge_need = L.lut + sizeof(float) * a.group * QK * a.nbv;
+  const size_t merge_need = L.lut + sizeof(float) * merge_smem_floats(a.group, a.nbv, a.n_splits);
   if (merge_need > bytes) bytes = merge_need;
   cudaError_t e = cudaFuncSetAttribute(decode_lut_kernel<KT, VT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);

@@ -91,59 +91,6 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Byte tables of the binary16 code values: l0/l1 low bytes of values 0..3 / 4..7,
-// h0/h1 the high bytes.  turbo2/3: value of code k; turbo4: magnitude j (the sign
-// is applied separately from bit 3 of the code).
-struct Tab {
-  uint32_t l0, l1, h0, h1;
-};
-
-template <int T>
-__device__ __forceinline__ Tab make_tab(const DevCodebook &cb) {
-  constexpr int NC = TypeTraits<T>::NC;
-  uint32_t v[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    float f = 0.f;
-    if (T == 4) f = cb.c[8 + k];
-    else if (k < NC) f = code_value(cb.c, NC, k);
-    v[k] = __half_as_ushort(__float2half_rn(f));
-  }
-  Tab t;
-  t.l0 = (v[0] & 0xff) | (v[1] & 0xff) << 8 | (v[2] & 0xff) << 16 | (v[3] & 0xff) << 24;
-  t.l1 = (v[4] & 0xff) | (v[5] & 0xff) << 8 | (v[6] & 0xff) << 16 | (v[7] & 0xff) << 24;
-  t.h0 = (v[0] >> 8) | (v[1] >> 8) << 8 | (v[2] >> 8) << 16 | (v[3] >> 8) << 24;
-  t.h1 = (v[4] >> 8) | (v[5] >> 8) << 8 | (v[6] >> 8) << 16 | (v[7] >> 8) << 24;
-  return t;
-}
-
-// Four codes in the low 16 bits of `sel` (one per nibble) -> two half2 registers
-// (code0, code1) and (code2, code3).
-template <int T>
-__device__ __forceinline__ void dq4(uint32_t sel, const Tab &t, uint32_t &h01, uint32_t &h23) {
-  const uint32_t s = (T == 4) ? (sel & 0x7777u) : sel;
-  const uint32_t lo = prmt(t.l0, t.l1, s);
-  uint32_t hi = prmt(t.h0, t.h1, s);
-  if (T == 4) hi |= prmt(0x80808080u, 0u, ((sel >> 1) & 0x4444u) | 0x3210u);   // sign bit 3 == 0 -> negative
-  h01 = prmt(lo, hi, 0x5140u);
-  h23 = prmt(lo, hi, 0x7362u);
-}
-
-// turbo2/3 selector words of one 16-element qs word: sel0 = elements 0..7,
-// sel1 = elements 8..15, one 3-bit code per nibble.  `sg` is the signs word of
-// the 32-element group, `odd` whether the qs word is the second of the group.
-template <int T>
-__device__ __forceinline__ void sel_words(uint32_t w, uint32_t sg, bool odd, uint32_t &sel0, uint32_t &sel1) {
-  sel0 = w & 0x33333333u;
-  sel1 = (w >> 2) & 0x33333333u;
-  if (T == 3) {
-    const uint32_t s0 = odd ? (sg << 2) : sg;
-    const uint32_t s1 = odd ? (sg << 1) : (sg >> 1);
-    sel0 |= s0 & 0x44444444u;
-    sel1 |= s1 & 0x44444444u;
-  }
-}
-
 // K side: the 32 rotated dims 32c .. 32c+31 of one key block -> h[p] = half2 of
 // dims (32c + 2p, 32c + 2p + 1), p = 0..15.
 template <int T>
@@ -463,7 +410,7 @@ __global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
       part[2 + d] = 0.f;
       if (d == 0) { part[0] = -INFINITY; part[1] = 0.f; }
     }
-    decode_merge<NT>(a, hk, qrot);
+    decode_merge<NT>(a, hk, reinterpret_cast<float *>(stages));
     return;
   }
   float *wm = reinterpret_cast<float *>(stages);                 // [NW][G]
@@ -544,6 +491,10 @@ template <int T, int G, int NBK, int NBV>
 cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
   constexpr uint32_t bytes = smem_bytes<T, G, NBK, NBV>();
   static_assert(bytes <= 227 * 1024, "shared memory");
+  // the epilogue reuses the stage buffers: per-warp results + the split merge (<= 256 splits)
+  static_assert(STAGES * stage_layout<T, NBK, NBV>().bytes >=
+                    4 * (2 * NW * 4 + NW * G * 128 * NBV + 2 * G * 128 * NBV + 2 * G * 256),
+                "stage buffers too small for the epilogue");
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<T, G, NBK, NBV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;

@@ -38,7 +38,8 @@ DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int6
                                     int /*algo*/) {
   DecodeWorkspaceLayout L;
   const int target_ctas = 2 * sm_count();
-  const int per_head = (target_ctas + n_kv_heads - 1) / n_kv_heads;
+  int per_head = (target_ctas + n_kv_heads - 1) / n_kv_heads;
+  if (per_head > 256) per_head = 256;     // the merge stages <= 256 splits in shared memory
   int64_t chunk = (kv_len + per_head - 1) / per_head;
   chunk = (chunk + 63) / 64 * 64;
   if (chunk < 128) chunk = 128;
@@ -298,18 +299,56 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
 
 size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads,
                                   int64_t kv_len) {
-  (void)k; (void)v; (void)nq; (void)n_q_heads; (void)kv_len;
-  return 0;
+  if (check_kv_pair(k, v, n_q_heads, kv_len) != TQ_OK || nq < 0) return 0;
+  return kWsHeader;      // the status word; the kernel keeps everything else on chip
 }
 
 tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
                            const tq_codebook *cbv, const void *q, int q_type, int nq,
                            int n_q_heads, int64_t kv_len, float scale, int causal, float *out,
                            void *workspace, size_t workspace_bytes, tq_stream stream) {
-  (void)k; (void)v; (void)cbk; (void)cbv; (void)q; (void)q_type; (void)nq; (void)n_q_heads;
-  (void)kv_len; (void)scale; (void)causal; (void)out; (void)workspace; (void)workspace_bytes;
-  (void)stream;
-  return TQ_ERR_UNSUPPORTED;
+  tq_status st = check_kv_pair(k, v, n_q_heads, kv_len);
+  if (st != TQ_OK) return st;
+  if (!codebook_ok(cbk, k->type) || !codebook_ok(cbv, v->type)) return TQ_ERR_INVALID_ARG;
+  if (q_type != TQ_F32 && q_type != TQ_F16 && q_type != TQ_BF16) return TQ_ERR_INVALID_ARG;
+  if (nq < 0 || (causal && nq > kv_len) || !isfinite(scale)) return TQ_ERR_INVALID_ARG;
+  if (nq == 0) return TQ_OK;
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < kWsHeader)
+    return TQ_ERR_WORKSPACE;
+  const int group = n_q_heads / k->n_kv_heads;
+  if (!prefill_supported(k->type, v->type, group, k->n_blocks, v->n_blocks)) return TQ_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kv_len == 0)
+    return map_cuda(cudaMemsetAsync(out, 0, sizeof(float) * nq * n_q_heads * v->head_dim, s));
+  if (static_cast<int64_t>(nq) * group > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;
+  PrefillArgs a;
+  memset(&a, 0, sizeof(a));
+  a.kn = static_cast<const uint16_t *>(k->norms);
+  a.kqs = static_cast<const uint8_t *>(k->qs);
+  a.ksg = static_cast<const uint8_t *>(k->signs);
+  a.vn = static_cast<const uint16_t *>(v->norms);
+  a.vqs = static_cast<const uint8_t *>(v->qs);
+  a.vsg = static_cast<const uint8_t *>(v->signs);
+  a.q = q;
+  a.out = out;
+  a.status = static_cast<int32_t *>(workspace);
+  a.n_cells = k->n_cells;
+  a.kv_len = kv_len;
+  a.q_type = q_type;
+  a.nq = nq;
+  a.n_q_heads = n_q_heads;
+  a.n_kv_heads = k->n_kv_heads;
+  a.group = group;
+  a.dk = k->head_dim;
+  a.dv = v->head_dim;
+  a.nbk = k->n_blocks;
+  a.nbv = v->n_blocks;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.cbk = to_dev(cbk);
+  a.cbv = to_dev(cbv);
+  return map_cuda(launch_prefill(k->type, a, s));
 }
 
 size_t tq_int8_prompt_attn_workspace(int nq, int n_q_heads, int n_kv_heads, int head_dim,

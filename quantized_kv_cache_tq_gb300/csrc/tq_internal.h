@@ -59,6 +59,30 @@ struct DecodeArgs {
   DevCodebook cbk, cbv;
 };
 
+struct PrefillArgs {
+  const uint16_t *kn;
+  const uint8_t *kqs;
+  const uint8_t *ksg;
+  const uint16_t *vn;
+  const uint8_t *vqs;
+  const uint8_t *vsg;
+  const void *q;
+  float *out;
+  int32_t *status;
+  int64_t n_cells;
+  int64_t kv_len;
+  int32_t q_type;
+  int32_t nq;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t group;
+  int32_t dk, dv;
+  int32_t nbk, nbv;
+  int32_t causal;
+  float scale_log2;
+  DevCodebook cbk, cbv;
+};
+
 struct DecodeWorkspaceLayout {
   size_t counters_off, part_off, total;
   int n_splits;
@@ -77,5 +101,7 @@ cudaError_t launch_decode_mma(int ktype, int vtype, const DecodeArgs &a, cudaStr
 cudaError_t launch_decode_mma_t2(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode_mma_t3(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode_mma_t4(const DecodeArgs &a, cudaStream_t s);
+bool prefill_supported(int ktype, int vtype, int group, int nbk, int nbv);
+cudaError_t launch_prefill(int ktype, const PrefillArgs &a, cudaStream_t s);
 
 }  // namespace tq
