@@ -161,6 +161,25 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
                           float scale, int algo, float *out, void *workspace,
                           size_t workspace_bytes, tq_stream stream);
 
+/* tq_fattn_decode without a caller workspace, for callers that cannot
+ * allocate device memory (code inside an allocator or memory-pool callback, a
+ * runtime that has reserved all device memory up front, a plugin host that only
+ * passes input and output buffers).  The pages have no counterpart: this is an
+ * addition of this library.
+ * The split partials, counters and status word live in one fixed 4 MiB device
+ * array inside the library; every GPU that loads the library keeps those 4 MiB
+ * until the process exits.  Shapes whose decode workspace
+ * (tq_fattn_decode_workspace) exceeds 4 MiB return TQ_ERR_WORKSPACE and launch
+ * nothing.  The first call on a device looks up the array's address with that
+ * device current; make it before any stream capture.  Each call clears the
+ * counters and status word on `stream` before the kernel.  All calls share the
+ * array, so calls that overlap on the GPU (different streams) race and give
+ * wrong results.  Other arguments, results and errors as tq_fattn_decode. */
+tq_status tq_fattn_decode_noalloc(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                                  const tq_codebook *cbv, const float *q, int n_q_heads,
+                                  int64_t kv_len, float scale, int algo, float *out,
+                                  tq_stream stream);
+
 /* Bytes of workspace tq_fattn_prefill needs (0 if the shape is invalid);
  * same alignment and zero-fill rule as the decode workspace. */
 size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads,
