@@ -364,7 +364,8 @@ def run_tq(args):
 
     extras = {}
     if not args.no_extras and rank == 0:
-        extras = run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak)
+        extras = run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak,
+                            float(peaks.get("bf16_tflops", 1900.0)))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -416,7 +417,73 @@ def time_graph(torch, fn, reps=20, warm=3):
     return a.elapsed_time(b) / reps / 1000.0
 
 
-def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak):
+def _device_gaussian(torch, gen, shape, dev, outliers=True):
+    """N(0,1) on the device with 4 outlier channels per 128 scaled by 8 (per head)."""
+    x = torch.randn(shape, generator=gen, device=dev)
+    if outliers:
+        n_heads, dim = shape[-2], shape[-1]
+        n_out = max(1, round(4 * dim / 128))
+        for h in range(n_heads):
+            ch = torch.randperm(dim, generator=gen, device=dev)[:n_out]
+            x[..., h, ch] *= 8.0
+    return x
+
+
+def run_prefill_extra(tq, torch, dev, tflops_peak, nqs=(4096, 512)):
+    """Prefill over the 4K-context turbo3 cache (8 KV x 16 query heads, D = 256, causal)."""
+    import workloads as W
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20262)
+    L, HK, HQ, DD = 4096, 8, 16, 256
+    sh = W.prefill_4k()
+    sk, sv = W.codebook_signs(sh)
+    cbk, cbv = tq.codebook(3, sk), tq.codebook(3, sv)
+    kc, vc = tq.TqCache(3, HK, DD, L, dev), tq.TqCache(3, HK, DD, L, dev)
+    cells = torch.arange(L, dtype=torch.int64, device=dev)
+    tq.set_rows(kc, cbk, _device_gaussian(torch, gen, (L, HK, DD), dev), cells)
+    tq.set_rows(vc, cbv, _device_gaussian(torch, gen, (L, HK, DD), dev), cells)
+    res = {}
+    for nq in nqs:
+        q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty((nq, HQ, DD), device=dev)
+        ws = tq.workspace(256, dev)
+        t = time_graph(torch, lambda: tq.fattn_prefill(kc, vc, cbk, cbv, q, L, out=out, ws=ws), reps=5)
+        pairs = sum(min(L, L - nq + i + 1) for i in range(nq))
+        flop = 4.0 * DD * pairs * HQ
+        res[f"nq{nq}"] = {"ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
+                          "algorithmic_GFLOP": flop / 1e9}
+    return {"workload": "prefill_4k: 8 KV x 16 Q heads, D=256, 4096 cells, turbo3, causal, bf16 Q",
+            "flops": "4*D per visible (query, key) pair per query head; hi/lo fp16 operand splits not counted",
+            **res}
+
+
+def run_int8_extra(tq, torch, dev, tflops_peak, ctx=140000, nq=2048):
+    """int8 prompt attention: 8 KV x 32 Q heads, D = 128, 2048 queries over `ctx` scattered cells."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20264)
+    HK, HQ, DD = 8, 32, 128
+    res = {}
+    raw = _device_gaussian(torch, gen, (ctx, HK, DD), dev)
+    amax = raw.abs().amax(-1)
+    sk = (amax / 127).to(torch.float16)
+    k = torch.clamp(torch.round(raw / sk.float().unsqueeze(-1)), -127, 127).to(torch.int8)
+    raw = _device_gaussian(torch, gen, (ctx, HK, DD), dev)
+    sv = (raw.abs().amax(-1) / 127).to(torch.float16)
+    v = torch.clamp(torch.round(raw / sv.float().unsqueeze(-1)), -127, 127).to(torch.int8)
+    del raw
+    perm = torch.randperm(ctx, generator=gen, device=dev).to(torch.int32)
+    q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.float16)
+    out = torch.empty((nq, HQ, DD), device=dev)
+    ws = tq.workspace(256, dev)
+    t = time_graph(torch, lambda: tq.int8_prompt_attn(k, sk, v, sv, perm, ctx, q, out=out, ws=ws), reps=3)
+    pairs = sum(min(ctx, ctx - nq + i + 1) for i in range(nq))
+    flop = 4.0 * DD * pairs * HQ
+    return {"workload": f"int8_prompt: 8 KV x 32 Q heads, D=128, {nq} queries, ctx {ctx} scattered cells, fp16 Q",
+            "ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
+            "algorithmic_GFLOP": flop / 1e9}
+
+
+def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak, tflops_peak):
     """Other rows of the hot path, measured on their own workloads."""
     ex = {}
     # SET_ROWS over the whole 32K cache (K and V): read fp32 rows, write packed planes
@@ -427,6 +494,8 @@ def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv
     nbytes = 2 * (k_src.numel() * 4 + N_KV * KV_LEN * 50) + 2 * KV_LEN * 8
     ex["set_rows_bulk"] = {"workload": "32768 rows x 8 KV heads x 128, K and V, f32 -> turbo3",
                            "ms": t * 1e3, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak}
+    ex["prefill"] = run_prefill_extra(tq, torch, dev, tflops_peak)
+    ex["int8_prompt"] = run_int8_extra(tq, torch, dev, tflops_peak)
     return ex
 
 

@@ -351,23 +351,6 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   return map_cuda(launch_prefill(k->type, a, s));
 }
 
-size_t tq_int8_prompt_attn_workspace(int nq, int n_q_heads, int n_kv_heads, int head_dim,
-                                     int64_t ctx) {
-  (void)nq; (void)n_q_heads; (void)n_kv_heads; (void)head_dim; (void)ctx;
-  return 0;
-}
-
-tq_status tq_int8_prompt_attn(const int8_t *k, const uint16_t *k_scale, const int8_t *v,
-                              const uint16_t *v_scale, int64_t n_cells, const int32_t *cell_of_pos,
-                              int64_t ctx, const uint16_t *q, int nq, int n_q_heads,
-                              int n_kv_heads, int head_dim, float scale, int causal, float *out,
-                              void *workspace, size_t workspace_bytes, tq_stream stream) {
-  (void)k; (void)k_scale; (void)v; (void)v_scale; (void)n_cells; (void)cell_of_pos; (void)ctx;
-  (void)q; (void)nq; (void)n_q_heads; (void)n_kv_heads; (void)head_dim; (void)scale;
-  (void)causal; (void)out; (void)workspace; (void)workspace_bytes; (void)stream;
-  return TQ_ERR_UNSUPPORTED;
-}
-
 tq_status tq_workspace_status(void *workspace, size_t workspace_bytes, int32_t *status_out,
                               tq_stream stream) {
   if (!workspace || workspace_bytes < kWsHeader || !status_out) return TQ_ERR_INVALID_ARG;

@@ -11,7 +11,8 @@ Random numbers come from one counter-based generator, defined here once:
     key(seed, s)    mix64(mix64(seed) ^ (s * 0xD1B54A32D192ED03))
     bits(k, i)      mix64(k + (i + 1) * 0x9E3779B97F4A7C15)        (mod 2**64)
     uniform(k, i)   ((bits(k, i) >> 11) + 0.5) * 2**-53            in (0, 1)
-    normal(k, i)    sqrt(-2 ln uniform(k, 2i)) * cos(2 pi uniform(k, 2i+1))
+    normal(k, 2i)   sqrt(-2 ln uniform(k, 2i)) * cos(2 pi uniform(k, 2i+1))
+    normal(k, 2i+1) sqrt(-2 ln uniform(k, 2i)) * sin(2 pi uniform(k, 2i+1))
 
 Workload shapes (named after what they are):
 
@@ -90,16 +91,19 @@ def uniform(key: int, idx: np.ndarray) -> np.ndarray:
 
 
 def normal(seed: int, stream: int, n: int, chunk: int = 1 << 22) -> np.ndarray:
-    """n standard normal f64 values (Box-Muller, cosine branch only)."""
+    """n standard normal f64 values: pair i (values 2i, 2i+1) is the Box-Muller
+    pair r cos(t), r sin(t) with r = sqrt(-2 ln uniform(k, 2i)), t = 2 pi uniform(k, 2i+1)."""
     key = stream_key(seed, stream)
-    out = np.empty(n, dtype=np.float64)
-    for lo in range(0, n, chunk):
-        hi = min(n, lo + chunk)
+    n_pairs = (n + 1) // 2
+    out = np.empty(2 * n_pairs, dtype=np.float64)
+    for lo in range(0, n_pairs, chunk):
+        hi = min(n_pairs, lo + chunk)
         i = np.arange(lo, hi, dtype=np.uint64)
-        u1 = uniform(key, 2 * i)
-        u2 = uniform(key, 2 * i + np.uint64(1))
-        out[lo:hi] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
-    return out
+        r = np.sqrt(-2.0 * np.log(uniform(key, 2 * i)))
+        t = 2.0 * math.pi * uniform(key, 2 * i + np.uint64(1))
+        out[2 * lo:2 * hi:2] = r * np.cos(t)
+        out[2 * lo + 1:2 * hi:2] = r * np.sin(t)
+    return out[:n]
 
 
 def outlier_channels(seed: int, stream: int, n_heads: int, dim: int) -> np.ndarray:
