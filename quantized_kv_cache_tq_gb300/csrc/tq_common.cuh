@@ -156,10 +156,11 @@ __device__ __forceinline__ Tab make_tab(const DevCodebook &cb) {
 }
 
 // Four codes in the low 16 bits of `sel` (one per nibble) -> two half2 registers
-// (code0, code1) and (code2, code3).
+// (code0, code1) and (code2, code3).  prmt reads only bits 15:0 of its selector,
+// so the upper half of `sel` may hold anything.
 template <int T>
 __device__ __forceinline__ void dq4(uint32_t sel, const Tab &t, uint32_t &h01, uint32_t &h23) {
-  const uint32_t s = (T == 4) ? (sel & 0x7777u) : sel;
+  const uint32_t s = (T == 4) ? (sel & 0x7777u) : sel;      // turbo4: bit 3 is the sign
   const uint32_t lo = prmt_b32(t.l0, t.l1, s);
   uint32_t hi = prmt_b32(t.h0, t.h1, s);
   if (T == 4) hi |= prmt_b32(0x80808080u, 0u, ((sel >> 1) & 0x4444u) | 0x3210u);   // sign bit 3 == 0 -> negative

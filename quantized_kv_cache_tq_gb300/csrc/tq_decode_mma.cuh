@@ -5,7 +5,9 @@
 // shared-memory traffic per 0.39 B of HBM traffic, and the SMs' shared-memory
 // bandwidth is only ~5x HBM -- the LUT kernel is bound by shared memory at
 // several times the HBM time.  Here the packed codes go from HBM to shared
-// memory once (cp.async.bulk, 4-stage mbarrier ring) and each thread turns them
+// memory once (cp.async.bulk into a per-warp mbarrier ring; each warp streams
+// its own contiguous key range, so the main loop has no CTA barrier) and each
+// thread turns them
 // into fp16 mma.sync operand fragments with byte permutes: a code nibble is the
 // prmt selector into a 4-register table holding the low / high bytes of the
 // binary16 centroid values, so a centroid costs ~1.5 integer ops and feeds all
@@ -29,58 +31,14 @@
 #pragma once
 
 #include "tq_decode_common.cuh"
+#include "tq_tc.cuh"
 
 namespace tq {
 namespace mmadec {
 
 constexpr int NW = 8;                // warps per CTA
 constexpr int NT = NW * 32;
-constexpr int WKEYS = 16;            // keys per warp per tile
-constexpr int CKEYS = NW * WKEYS;    // keys per CTA tile (128)
-constexpr int STAGES = 4;
-constexpr long long kWaitLimit = 1ll << 22;
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-// bounded wait on phase `parity`; returns false if the limit was hit
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
-  for (long long it = 0; it < kWaitLimit; ++it) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
+constexpr int WK = 32;               // keys per warp per iteration (two mma key groups)
 
 __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -101,7 +59,7 @@ __device__ __forceinline__ void dq_chunk32(const uint8_t *qs_row, const uint8_t 
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      dq4<4>(ws[i] & 0xffffu, t, h[4 * i + 0], h[4 * i + 1]);
+      dq4<4>(ws[i], t, h[4 * i + 0], h[4 * i + 1]);
       dq4<4>(ws[i] >> 16, t, h[4 * i + 2], h[4 * i + 3]);
     }
   } else {
@@ -112,9 +70,9 @@ __device__ __forceinline__ void dq_chunk32(const uint8_t *qs_row, const uint8_t 
     for (int i = 0; i < 2; ++i) {
       uint32_t s0, s1;
       sel_words<T>(ws[i], sg, i == 1, s0, s1);
-      dq4<T>(s0 & 0xffffu, t, h[8 * i + 0], h[8 * i + 1]);
+      dq4<T>(s0, t, h[8 * i + 0], h[8 * i + 1]);
       dq4<T>(s0 >> 16, t, h[8 * i + 2], h[8 * i + 3]);
-      dq4<T>(s1 & 0xffffu, t, h[8 * i + 4], h[8 * i + 5]);
+      dq4<T>(s1, t, h[8 * i + 4], h[8 * i + 5]);
       dq4<T>(s1 >> 16, t, h[8 * i + 6], h[8 * i + 7]);
     }
   }
@@ -134,9 +92,9 @@ __device__ __forceinline__ void dq_pair16(uint32_t a0, uint32_t a1, uint32_t b0,
     const uint32_t ev = (sa[i] & 0x0F0F0F0Fu) | ((sb[i] & 0x0F0F0F0Fu) << 4);
     const uint32_t od = ((sa[i] >> 4) & 0x0F0F0F0Fu) | (sb[i] & 0xF0F0F0F0u);
     // ev nibbles: (k0 e0, k1 e0, k0 e2, k1 e2 | k0 e4, k1 e4, k0 e6, k1 e6)
-    dq4<T>(ev & 0xffffu, t, out[8 * i + 0], out[8 * i + 2]);
+    dq4<T>(ev, t, out[8 * i + 0], out[8 * i + 2]);
     dq4<T>(ev >> 16, t, out[8 * i + 4], out[8 * i + 6]);
-    dq4<T>(od & 0xffffu, t, out[8 * i + 1], out[8 * i + 3]);
+    dq4<T>(od, t, out[8 * i + 1], out[8 * i + 3]);
     dq4<T>(od >> 16, t, out[8 * i + 5], out[8 * i + 7]);
   }
 }
@@ -156,49 +114,68 @@ __device__ __forceinline__ void v_sel(const uint8_t *qs_row, const uint8_t *sg_r
   }
 }
 
-struct StageLayout {
-  uint32_t kqs, ksg, kn, vqs, vsg, vn, bytes;
+// Per-warp staging ring: every warp streams its own contiguous key range
+// (32 keys per iteration) through STAGES bulk-copy buffers, so the main loop
+// has no CTA-wide barrier at all.
+template <int T, int NBK, int NBV>
+struct WarpStage {
+  static constexpr uint32_t QSB = TypeTraits<T>::QSB, SGB = TypeTraits<T>::SGB;
+  static constexpr uint32_t KQS = 0;
+  static constexpr uint32_t KSG = KQS + WK * NBK * QSB;
+  static constexpr uint32_t KN = KSG + WK * NBK * SGB;
+  static constexpr uint32_t VQS = KN + WK * NBK * 2;
+  static constexpr uint32_t VSG = VQS + WK * NBV * QSB;
+  static constexpr uint32_t VN = VSG + WK * NBV * SGB;
+  static constexpr uint32_t BYTES = (VN + WK * NBV * 2 + 127) / 128 * 128;
+  static constexpr uint32_t TX = WK * (NBK + NBV) * (QSB + SGB + 2);
+  static constexpr int STAGES = (NW * 4 * BYTES <= 104 * 1024) ? 4 : (NW * 3 * BYTES <= 160 * 1024) ? 3 : 2;
+  static constexpr uint32_t RING = STAGES * BYTES;                    // per warp
+  static constexpr uint32_t PT = NW * RING;                           // P tiles [NW][NBV][8][WK] fp16
+  static constexpr uint32_t QR = PT + NW * NBV * 8 * WK * 2;          // rotated q (floats)
 };
 
-template <int T, int NBK, int NBV>
-__host__ __device__ constexpr StageLayout stage_layout() {
-  constexpr uint32_t QSB = TypeTraits<T>::QSB, SGB = TypeTraits<T>::SGB;
-  StageLayout s{};
-  uint32_t o = 0;
-  s.kqs = o; o += CKEYS * NBK * QSB;
-  s.ksg = o; o += CKEYS * NBK * SGB;
-  s.kn = o;  o += CKEYS * NBK * 2;
-  s.vqs = o; o += CKEYS * NBV * QSB;
-  s.vsg = o; o += CKEYS * NBV * SGB;
-  s.vn = o;  o += CKEYS * NBV * 2;
-  s.bytes = (o + 127) / 128 * 128;
-  return s;
-}
+template <int T, int G, int NBK, int NBV>
+struct WarpStageQ {
+  static constexpr uint32_t QC = WarpStage<T, NBK, NBV>::QR + G * 128 * NBK * 4;   // B columns fp16 [8][128 NBK]
+  static constexpr uint32_t TOTAL = QC + 8 * 128 * NBK * 2;
+};
 
 template <int T, int G, int NBK, int NBV>
 __host__ __device__ constexpr uint32_t smem_bytes() {
-  // stages + P tiles (per warp, per V block: 8 columns x 16 keys fp16) + rotated q
-  return STAGES * stage_layout<T, NBK, NBV>().bytes + NW * NBV * 8 * WKEYS * 2 + G * 128 * NBK * 4 + 64;
+  return WarpStageQ<T, G, NBK, NBV>::TOTAL;
+}
+
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <int T, int G, int NBK, int NBV>
 __global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
   static_assert(G == 1 || G == 2 || G == 4, "GQA group must be 1, 2 or 4");
-  constexpr StageLayout SL = stage_layout<T, NBK, NBV>();
+  using WS = WarpStage<T, NBK, NBV>;
+  using WQ = WarpStageQ<T, G, NBK, NBV>;
   constexpr int QSB = TypeTraits<T>::QSB, SGB = TypeTraits<T>::SGB;
+  constexpr int STAGES = WS::STAGES;
+  constexpr int DVP = 128 * NBV;
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char *stages = smem;
-  uint16_t *ptile = reinterpret_cast<uint16_t *>(smem + STAGES * SL.bytes);     // [NW][NBV][8][16]
-  float *qrot = reinterpret_cast<float *>(smem + STAGES * SL.bytes + NW * NBV * 8 * WKEYS * 2);
-  __shared__ __align__(8) uint64_t full[STAGES];
-  __shared__ int s_timeout;
+  __shared__ __align__(8) uint64_t full[NW][STAGES];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int hk = blockIdx.y, split = blockIdx.x;
   const int64_t t0 = static_cast<int64_t>(split) * a.chunk;
   const int64_t t1 = min(a.kv_len, t0 + a.chunk);
-  const int n_tiles = static_cast<int>((t1 - t0 + CKEYS - 1) / CKEYS);
+  // this warp's key range [w0, w1), a multiple of WK keys long except at t1
+  const int64_t per_warp = ((t1 - t0 + NW - 1) / NW + WK - 1) / WK * WK;
+  const int64_t w0 = t0 + warp * per_warp;
+  const int64_t w1 = min(t1, w0 + per_warp);
+  const int n_it = (w1 > w0) ? static_cast<int>((w1 - w0 + WK - 1) / WK) : 0;
+
+  unsigned char *ring = smem + warp * WS::RING;
+  uint16_t *pw = reinterpret_cast<uint16_t *>(smem + WS::PT) + warp * NBV * 8 * WK;
+  float *qrot = reinterpret_cast<float *>(smem + WS::QR);
 
   const uint8_t *kqs = a.kqs + static_cast<size_t>(hk) * a.n_cells * NBK * QSB;
   const uint8_t *ksg = SGB ? a.ksg + static_cast<size_t>(hk) * a.n_cells * NBK * SGB : nullptr;
@@ -207,63 +184,59 @@ __global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
   const uint8_t *vsg = SGB ? a.vsg + static_cast<size_t>(hk) * a.n_cells * NBV * SGB : nullptr;
   const uint16_t *vn = a.vn + static_cast<size_t>(hk) * a.n_cells * NBV;
 
-  auto issue = [&](int tile) {
-    const int64_t key0 = t0 + static_cast<int64_t>(tile) * CKEYS;
-    const int64_t left = a.n_cells - key0;                    // multiple of 64
-    const uint32_t nk = static_cast<uint32_t>(left < CKEYS ? left : CKEYS);
-    unsigned char *st = stages + (tile % STAGES) * SL.bytes;
-    uint64_t *bar = &full[tile % STAGES];
-    const uint32_t bytes = nk * (NBK * (QSB + SGB + 2) + NBV * (QSB + SGB + 2));
-    mbar_expect_tx(bar, bytes);
-    bulk_g2s(st + SL.kqs, kqs + key0 * NBK * QSB, nk * NBK * QSB, bar);
-    if (SGB) bulk_g2s(st + SL.ksg, ksg + key0 * NBK * SGB, nk * NBK * SGB, bar);
-    bulk_g2s(st + SL.kn, kn + key0 * NBK, nk * NBK * 2, bar);
-    bulk_g2s(st + SL.vqs, vqs + key0 * NBV * QSB, nk * NBV * QSB, bar);
-    if (SGB) bulk_g2s(st + SL.vsg, vsg + key0 * NBV * SGB, nk * NBV * SGB, bar);
-    bulk_g2s(st + SL.vn, vn + key0 * NBV, nk * NBV * 2, bar);
+  // lane 0 of the warp: bring iteration `it` (keys w0 + 32 it ..) into its stage
+  auto issue = [&](int it) {
+    const int64_t key0 = w0 + static_cast<int64_t>(it) * WK;          // multiple of 32, key0 + 32 <= n_cells
+    unsigned char *st = ring + (it % STAGES) * WS::BYTES;
+    uint64_t *bar = &full[warp][it % STAGES];
+    tc::mbar_expect_tx(bar, WS::TX);
+    tc::bulk_g2s(st + WS::KQS, kqs + key0 * NBK * QSB, WK * NBK * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + WS::KSG, ksg + key0 * NBK * SGB, WK * NBK * SGB, bar);
+    tc::bulk_g2s(st + WS::KN, kn + key0 * NBK, WK * NBK * 2, bar);
+    tc::bulk_g2s(st + WS::VQS, vqs + key0 * NBV * QSB, WK * NBV * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + WS::VSG, vsg + key0 * NBV * SGB, WK * NBV * SGB, bar);
+    tc::bulk_g2s(st + WS::VN, vn + key0 * NBV, WK * NBV * 2, bar);
   };
 
-  if (tid == 0) {
-    s_timeout = 0;
+  if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    for (int s = 0; s < STAGES; ++s) tc::mbar_init(&full[warp][s], 1);
+    tc::mbar_init_fence();
+    tc::fence_async_smem();
+    for (int i = 0; i < STAGES && i < n_it; ++i) issue(i);
+  }
+
+  // rotated queries (scale and log2(e) folded in) while the first tiles land, then
+  // the score mma's B columns as binary16: n < G q'_hi, G <= n < 2G q'_lo, else 0
+  rotate_queries<NT>(a, hk, qrot);
+  for (int i = lane; i < NBV * 8 * WK; i += 32) pw[i] = 0;
+  __syncthreads();
+  uint16_t *qcol = reinterpret_cast<uint16_t *>(smem + WQ::QC);              // [8][128*NBK]
+  for (int i = tid; i < 8 * 128 * NBK; i += NT) {
+    const int n = i / (128 * NBK), d = i % (128 * NBK);
+    float x = 0.f;
+    if (n < 2 * G) {
+      const float q = qrot[(n % G) * 128 * NBK + d];
+      const __half hi = __float2half_rn(q);
+      x = (n < G) ? __half2float(hi) : (q - __half2float(hi));
+    }
+    qcol[i] = __half_as_ushort(__float2half_rn(x));
   }
   __syncthreads();
-  if (tid == 0)
-    for (int i = 0; i < STAGES && i < n_tiles; ++i) issue(i);
 
-  // rotated queries (scale and log2(e) folded in) while the first tiles land
-  rotate_queries<NT>(a, hk, qrot);
-  for (int i = tid; i < NW * NBV * 8 * WKEYS; i += NT) ptile[i] = 0;
-  __syncthreads();
+  const Tab tab_k{a.tabk[0], a.tabk[1], a.tabk[2], a.tabk[3]};
+  const Tab tab_v{a.tabv[0], a.tabv[1], a.tabv[2], a.tabv[3]};
 
-  const Tab tab_k = make_tab<T>(a.cbk);
-  const Tab tab_v = make_tab<T>(a.cbv);
-
-  // B fragments of the score mma: column n = g holds q'_hi (n < G), q'_lo (G <= n < 2G) or 0
+  // B fragments: k-step kk of block b uses dims 32c + 4kk + {0,1} (b0) and + {2,3} (b1)
   uint32_t qb[NBK][8][2];
 #pragma unroll
   for (int b = 0; b < NBK; ++b)
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint16_t v[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int d = b * QK + 32 * c + 4 * kk + 2 * h + j;
-          float x = 0.f;
-          if (g < 2 * G) {
-            const float q = qrot[(g % G) * QK * NBK + d];
-            const __half hi = __float2half_rn(q);
-            x = (g < G) ? __half2float(hi) : (q - __half2float(hi));
-          }
-          v[j] = __half_as_ushort(__float2half_rn(x));
-        }
-        qb[b][kk][h] = v[0] | (static_cast<uint32_t>(v[1]) << 16);
-      }
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint2 v = *reinterpret_cast<const uint2 *>(qcol + g * 128 * NBK + b * QK + 32 * c + 4 * kk);
+      qb[b][kk][0] = v.x;
+      qb[b][kk][1] = v.y;
+    }
 
   float oacc[NBV][8][4];
 #pragma unroll
@@ -273,115 +246,137 @@ __global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) oacc[b][mt][i] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-
-  uint16_t *pw = ptile + warp * NBV * 8 * WKEYS;
+  const bool writer = (G == 4) ? (c < 2) : (c == 0);
+  const int hA = (G == 4) ? 2 * (c & 1) : 0;
+  const int nh = (G == 1) ? 1 : 2;
   bool timed_out = false;
 
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    if (!timed_out && !mbar_wait(&full[tile % STAGES], (tile / STAGES) & 1)) {
-      timed_out = true;
-      s_timeout = 1;
-    }
-    const unsigned char *st = stages + (tile % STAGES) * SL.bytes;
-    const int64_t key0 = t0 + static_cast<int64_t>(tile) * CKEYS + warp * WKEYS;
-    const int r0 = warp * WKEYS + g, r1 = r0 + 8;              // rows of this thread's keys
-    const bool ok0 = key0 + g < t1 && !timed_out, ok1 = key0 + g + 8 < t1 && !timed_out;
+  for (int it = 0; it < n_it; ++it) {
+    const bool ok = tc::mbar_wait(&full[warp][it % STAGES], (it / STAGES) & 1);
+    if (!__all_sync(0xffffffffu, ok)) { timed_out = true; break; }
+    const unsigned char *st = ring + (it % STAGES) * WS::BYTES;
+    const int64_t key0 = w0 + static_cast<int64_t>(it) * WK;
+    const uint16_t *knr = reinterpret_cast<const uint16_t *>(st + WS::KN);
+    const uint16_t *vnr = reinterpret_cast<const uint16_t *>(st + WS::VN);
 
-    if (key0 < t1 && !timed_out) {
-      // ---- scores: S^T[key][n], one accumulator per K block (own norm)
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- scores S^T[key][n] for two groups of 16 keys (rows grp*16 + g, + 8)
+    float s[2][4];
+#pragma unroll
+    for (int grp = 0; grp < 2; ++grp) {
+      const int r0 = grp * 16 + g, r1 = r0 + 8;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[grp][i] = 0.f;
 #pragma unroll
       for (int b = 0; b < NBK; ++b) {
         uint32_t ka0[16], ka1[16];
-        dq_chunk32<T>(st + SL.kqs + (r0 * NBK + b) * QSB, st + SL.ksg + (r0 * NBK + b) * SGB, c, tab_k, ka0);
-        dq_chunk32<T>(st + SL.kqs + (r1 * NBK + b) * QSB, st + SL.ksg + (r1 * NBK + b) * SGB, c, tab_k, ka1);
+        dq_chunk32<T>(st + WS::KQS + (r0 * NBK + b) * QSB, st + WS::KSG + (r0 * NBK + b) * SGB, c, tab_k, ka0);
+        dq_chunk32<T>(st + WS::KQS + (r1 * NBK + b) * QSB, st + WS::KSG + (r1 * NBK + b) * SGB, c, tab_k, ka1);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma16816(acc, ka0[2 * kk], ka1[2 * kk], ka0[2 * kk + 1], ka1[2 * kk + 1], qb[b][kk][0], qb[b][kk][1]);
-        const uint16_t *knr = reinterpret_cast<const uint16_t *>(st + SL.kn);
         const float n0 = __half2float(__ushort_as_half(knr[r0 * NBK + b]));
         const float n1 = __half2float(__ushort_as_half(knr[r1 * NBK + b]));
-        s[0] += n0 * acc[0];
-        s[1] += n0 * acc[1];
-        s[2] += n1 * acc[2];
-        s[3] += n1 * acc[3];
+        s[grp][0] = fmaf(n0, acc[0], s[grp][0]);
+        s[grp][1] = fmaf(n0, acc[1], s[grp][1]);
+        s[grp][2] = fmaf(n1, acc[2], s[grp][2]);
+        s[grp][3] = fmaf(n1, acc[3], s[grp][3]);
       }
-      // hi + lo columns -> full scores; thread then holds heads hA, hA+1 of keys g, g+8
+      // hi + lo columns -> full scores; the thread then holds heads hA, hA+1 of rows r0, r1
       if (G == 4) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], 2);
+        for (int i = 0; i < 4; ++i) s[grp][i] += __shfl_xor_sync(0xffffffffu, s[grp][i], 2);
       } else if (G == 2) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s[i] += __shfl_xor_sync(0xffffffffu, s[i], 1);
+        for (int i = 0; i < 4; ++i) s[grp][i] += __shfl_xor_sync(0xffffffffu, s[grp][i], 1);
       } else {
-        s[0] += s[1];
-        s[2] += s[3];
-        s[1] = s[0];
-        s[3] = s[2];
+        s[grp][0] += s[grp][1];
+        s[grp][2] += s[grp][3];
+        s[grp][1] = s[grp][0];
+        s[grp][3] = s[grp][2];
       }
-      if (!ok0) s[0] = s[1] = -INFINITY;
-      if (!ok1) s[2] = s[3] = -INFINITY;
+      if (key0 + r0 >= w1) s[grp][0] = s[grp][1] = -INFINITY;
+      if (key0 + r1 >= w1) s[grp][2] = s[grp][3] = -INFINITY;
+    }
 
-      // ---- online softmax per head (log2 domain); l kept per thread, reduced at the end
-      float p[4];
+    // ---- online softmax per head (log2 domain); the reference maximum is raised
+    // only when the running maximum grows by more than 2^8 (then O and l rescale)
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float tm = fmaxf(s[j], s[2 + j]);
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
-        const float mnew = fmaxf(m_run[j], tm);
-        const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(m_run[j] - mnew);
-        p[j] = (mnew == -INFINITY) ? 0.f : exp2f(s[j] - mnew);
-        p[2 + j] = (mnew == -INFINITY) ? 0.f : exp2f(s[2 + j] - mnew);
-        l_run[j] = l_run[j] * alpha + p[j] + p[2 + j];
-        m_run[j] = mnew;
-        // rescale the O' columns of this head (column 2c + j)
+    for (int j = 0; j < 2; ++j) {
+      float tm = fmaxf(fmaxf(s[0][j], s[0][2 + j]), fmaxf(s[1][j], s[1][2 + j]));
+      tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+      tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+      tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+      if (tm > m_run[j] + 8.f) {
+        const float fct = (m_run[j] == -INFINITY) ? 0.f : fast_ex2(m_run[j] - tm);
+        l_run[j] *= fct;
 #pragma unroll
         for (int b = 0; b < NBV; ++b)
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
-            oacc[b][mt][j] *= alpha;
-            oacc[b][mt][2 + j] *= alpha;
+            oacc[b][mt][j] *= fct;
+            oacc[b][mt][2 + j] *= fct;
           }
+        m_run[j] = tm;
       }
-
-      // ---- P' = p * |v| (per V block) as fp16 hi/lo columns of the per-warp tile [n][key]
-      const bool writer = (G == 4) ? (c < 2) : (c == 0);
-      const int hA = (G == 4) ? 2 * (c & 1) : 0;
-      const int nh = (G == 1) ? 1 : 2;
 #pragma unroll
-      for (int b = 0; b < NBV; ++b) {
-        const uint16_t *vnr = reinterpret_cast<const uint16_t *>(st + SL.vn);
-        const float v0 = ok0 ? __half2float(__ushort_as_half(vnr[r0 * NBV + b])) : 0.f;
-        const float v1 = ok1 ? __half2float(__ushort_as_half(vnr[r1 * NBV + b])) : 0.f;
-        if (writer) {
-          uint16_t *pt = pw + b * 8 * WKEYS;
+      for (int grp = 0; grp < 2; ++grp) {
+        s[grp][j] = fast_ex2(s[grp][j] - m_run[j]);           // -inf -> 0
+        s[grp][2 + j] = fast_ex2(s[grp][2 + j] - m_run[j]);
+        l_run[j] += s[grp][j] + s[grp][2 + j];
+      }
+    }
+
+    // ---- P' = p * |v| (per V block) as fp16 hi / lo columns of the per-warp tile [n][key]
+#pragma unroll
+    for (int b = 0; b < NBV; ++b) {
+      uint16_t *pt = pw + b * 8 * WK;
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp) {
+        const int r0 = grp * 16 + g, r1 = r0 + 8;
+        const float v0 = __half2float(__ushort_as_half(vnr[r0 * NBV + b]));
+        const float v1 = __half2float(__ushort_as_half(vnr[r1 * NBV + b]));
+        if (G == 4) {
+          // lanes c and c^2 hold the same scores: c < 2 writes the hi halves, c >= 2 the lo
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            // masked keys have p = 0 and may carry garbage norms: select the zero
+            const float x0 = s[grp][j] > 0.f ? s[grp][j] * v0 : 0.f;
+            const float x1 = s[grp][2 + j] > 0.f ? s[grp][2 + j] * v1 : 0.f;
+            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+            const int n = (c < 2) ? hA + j : G + hA + j;
+            pt[n * WK + r0] = __half_as_ushort(c < 2 ? h0 : __float2half_rn(x0 - __half2float(h0)));
+            pt[n * WK + r1] = __half_as_ushort(c < 2 ? h1 : __float2half_rn(x1 - __half2float(h1)));
+          }
+        } else if (writer) {
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             if (j < nh) {
-              const float x0 = p[j] * v0, x1 = p[2 + j] * v1;
+              const float x0 = s[grp][j] > 0.f ? s[grp][j] * v0 : 0.f;
+              const float x1 = s[grp][2 + j] > 0.f ? s[grp][2 + j] * v1 : 0.f;
               const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
               const int nhi = hA + j, nlo = G + hA + j;
-              pt[nhi * WKEYS + g] = __half_as_ushort(h0);
-              pt[nhi * WKEYS + g + 8] = __half_as_ushort(h1);
-              pt[nlo * WKEYS + g] = __half_as_ushort(__float2half_rn(x0 - __half2float(h0)));
-              pt[nlo * WKEYS + g + 8] = __half_as_ushort(__float2half_rn(x1 - __half2float(h1)));
+              pt[nhi * WK + r0] = __half_as_ushort(h0);
+              pt[nhi * WK + r1] = __half_as_ushort(h1);
+              pt[nlo * WK + r0] = __half_as_ushort(__float2half_rn(x0 - __half2float(h0)));
+              pt[nlo * WK + r1] = __half_as_ushort(__float2half_rn(x1 - __half2float(h1)));
             }
           }
         }
       }
-      __syncwarp();
+    }
+    __syncwarp();
 
-      // ---- O'^T[d][n] += V'^T[d][key] P'^T[key][n]
+    // ---- O'^T[d][n] += V'^T[d][key] P'^T[key][n]
 #pragma unroll
-      for (int b = 0; b < NBV; ++b) {
-        const uint32_t *pt32 = reinterpret_cast<const uint32_t *>(pw + b * 8 * WKEYS);
-        const uint32_t pb0 = pt32[g * (WKEYS / 2) + c], pb1 = pt32[g * (WKEYS / 2) + c + 4];
-        const int kr = warp * WKEYS;                 // first key row of this warp in the stage
+    for (int b = 0; b < NBV; ++b) {
+      const uint32_t *pt32 = reinterpret_cast<const uint32_t *>(pw + b * 8 * WK);
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp) {
+        const uint32_t pb0 = pt32[g * (WK / 2) + grp * 8 + c], pb1 = pt32[g * (WK / 2) + grp * 8 + c + 4];
+        const int kr = grp * 16;
         uint32_t s00, s01, s10, s11, s20, s21, s30, s31;
-        const uint8_t *vq = st + SL.vqs, *vs = st + SL.vsg;
+        const uint8_t *vq = st + WS::VQS, *vs = st + WS::VSG;
         v_sel<T>(vq + ((kr + 2 * c) * NBV + b) * QSB, vs + ((kr + 2 * c) * NBV + b) * SGB, g, s00, s01);
         v_sel<T>(vq + ((kr + 2 * c + 1) * NBV + b) * QSB, vs + ((kr + 2 * c + 1) * NBV + b) * SGB, g, s10, s11);
         v_sel<T>(vq + ((kr + 2 * c + 8) * NBV + b) * QSB, vs + ((kr + 2 * c + 8) * NBV + b) * SGB, g, s20, s21);
@@ -393,30 +388,14 @@ __global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
         for (int mt = 0; mt < 8; ++mt)
           mma16816(oacc[b][mt], lo[2 * mt], lo[2 * mt + 1], hi[2 * mt], hi[2 * mt + 1], pb0, pb1);
       }
-      __syncwarp();
     }
-    __syncthreads();
-    if (tid == 0 && tile + STAGES < n_tiles && !s_timeout) issue(tile + STAGES);
+    __syncwarp();
+    if (lane == 0 && it + STAGES < n_it) issue(it + STAGES);      // this stage is free again
   }
 
-  // ---- per-warp results -> shared memory (reusing the stage buffers), CTA merge
-  __syncthreads();
-  if (s_timeout) {
-    // a bounded wait gave up: report it and leave this split empty (weight 0 in the merge)
-    if (tid == 0) set_status(a.status, TQ_ERR_TIMEOUT);
-    for (int i = tid; i < G * 128 * NBV; i += NT) {
-      const int h = i / (128 * NBV), d = i % (128 * NBV);
-      float *part = a.part + (static_cast<size_t>(hk * G + h) * a.n_splits + split) * a.part_stride;
-      part[2 + d] = 0.f;
-      if (d == 0) { part[0] = -INFINITY; part[1] = 0.f; }
-    }
-    decode_merge<NT>(a, hk, reinterpret_cast<float *>(stages));
-    return;
-  }
-  float *wm = reinterpret_cast<float *>(stages);                 // [NW][G]
-  float *wl = wm + NW * 4;                                      // [NW][G]
-  float *wo = wl + NW * 4;                                      // [NW][G][128*NBV]
-  constexpr int DVP = 128 * NBV;
+  // ---- per-warp results -> this warp's ring (all its copies have landed), CTA merge
+  if (timed_out && lane == 0) set_status(a.status, TQ_ERR_TIMEOUT);
+  float *wbuf = reinterpret_cast<float *>(ring);                 // m[G], l[G], o[G][DVP]
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     float l = l_run[j];
@@ -425,7 +404,6 @@ __global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
     l += __shfl_xor_sync(0xffffffffu, l, 16);
     l_run[j] = l;
   }
-  // combine hi/lo output columns
 #pragma unroll
   for (int b = 0; b < NBV; ++b)
 #pragma unroll
@@ -437,30 +415,26 @@ __global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
         else if (G == 2) v += __shfl_xor_sync(0xffffffffu, v, 1);
         oacc[b][mt][i] = v;
       }
-  {
-    const bool writer = (G == 4) ? (c < 2) : (c == 0);
-    const int hA = (G == 4) ? 2 * (c & 1) : 0;
-    if (writer) {
+  if (writer) {
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int h = hA + j;
-        if (h < G) {
-          if (g == 0) {
-            wm[warp * 4 + h] = m_run[j];
-            wl[warp * 4 + h] = l_run[j];
-          }
-#pragma unroll
-          for (int b = 0; b < NBV; ++b)
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              // G == 1: columns 0 (hi) and 1 (lo) of head 0
-              const float top = (G == 1) ? oacc[b][mt][0] + oacc[b][mt][1] : oacc[b][mt][j];
-              const float bot = (G == 1) ? oacc[b][mt][2] + oacc[b][mt][3] : oacc[b][mt][2 + j];
-              float *o = wo + (warp * G + h) * DVP + b * 128 + 16 * g + 2 * mt;
-              o[0] = top;
-              o[1] = bot;
-            }
+    for (int j = 0; j < 2; ++j) {
+      const int h = hA + j;
+      if (h < G) {
+        if (g == 0) {
+          wbuf[h] = timed_out ? -INFINITY : m_run[j];
+          wbuf[G + h] = timed_out ? 0.f : l_run[j];
         }
+#pragma unroll
+        for (int b = 0; b < NBV; ++b)
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            // G == 1: columns 0 (hi) and 1 (lo) of head 0
+            const float top = (G == 1) ? oacc[b][mt][0] + oacc[b][mt][1] : oacc[b][mt][j];
+            const float bot = (G == 1) ? oacc[b][mt][2] + oacc[b][mt][3] : oacc[b][mt][2 + j];
+            float *o = wbuf + 2 * G + h * DVP + b * 128 + 16 * g + 2 * mt;
+            o[0] = timed_out ? 0.f : top;
+            o[1] = timed_out ? 0.f : bot;
+          }
       }
     }
   }
@@ -469,13 +443,14 @@ __global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
     const int h = i / DVP, d = i % DVP;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w * 4 + h]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, reinterpret_cast<const float *>(smem + w * WS::RING)[h]);
     float o = 0.f, l = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float f = (wm[w * 4 + h] == -INFINITY) ? 0.f : exp2f(wm[w * 4 + h] - M);
-      o += f * wo[(w * G + h) * DVP + d];
-      l += f * wl[w * 4 + h];
+      const float *wb = reinterpret_cast<const float *>(smem + w * WS::RING);
+      const float f = (wb[h] == -INFINITY) ? 0.f : exp2f(wb[h] - M);
+      o += f * wb[2 * G + h * DVP + d];
+      l += f * wb[G + h];
     }
     float *part = a.part + (static_cast<size_t>(hk * G + h) * a.n_splits + split) * a.part_stride;
     part[2 + d] = o;
@@ -484,17 +459,16 @@ __global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
       part[1] = l;
     }
   }
-  decode_merge<NT>(a, hk, wo + NW * G * DVP);
+  decode_merge<NT>(a, hk, reinterpret_cast<float *>(smem));
 }
 
 template <int T, int G, int NBK, int NBV>
 cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
   constexpr uint32_t bytes = smem_bytes<T, G, NBK, NBV>();
   static_assert(bytes <= 227 * 1024, "shared memory");
-  // the epilogue reuses the stage buffers: per-warp results + the split merge (<= 256 splits)
-  static_assert(STAGES * stage_layout<T, NBK, NBV>().bytes >=
-                    4 * (2 * NW * 4 + NW * G * 128 * NBV + 2 * G * 128 * NBV + 2 * G * 256),
-                "stage buffers too small for the epilogue");
+  // the epilogue: each warp's ring holds its results; the split merge reuses the front
+  static_assert(WarpStage<T, NBK, NBV>::RING >= 4 * (2 * G + G * 128 * NBV), "ring too small for the epilogue");
+  static_assert(NW * WarpStage<T, NBK, NBV>::RING >= 4 * (G * 128 * NBV + 2 * G * 256), "merge region");
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<T, G, NBK, NBV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;

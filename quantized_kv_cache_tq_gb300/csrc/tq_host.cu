@@ -116,6 +116,37 @@ static bool codebook_ok(const tq_codebook *cb, int type) {
   return cb->centroids[n / 2] > 0.f;
 }
 
+// binary16 bit pattern of a float that is exactly representable in binary16
+static uint16_t binary16_bits(float f) {
+  if (f == 0.f) return signbit(f) ? 0x8000 : 0;
+  uint16_t sign = f < 0 ? 0x8000 : 0;
+  double a = fabs(static_cast<double>(f));
+  int e = 0;
+  const double m = frexp(a, &e);           // a = m 2^e, m in [0.5, 1)
+  const int E = e - 1;                     // a in [2^E, 2^(E+1))
+  if (E < -14) return sign | static_cast<uint16_t>(nearbyint(a * 0x1p24));            // subnormal
+  const uint32_t mant = static_cast<uint32_t>(nearbyint((2.0 * m - 1.0) * 1024.0));
+  return sign | static_cast<uint16_t>(((E + 15) << 10) | mant);
+}
+
+void code_byte_tables(const tq_codebook *cb, int type, uint32_t t[4]) {
+  const int n = cb->n_centroids, half = n / 2;
+  uint16_t v[8];
+  for (int k = 0; k < 8; ++k) {
+    float f = 0.f;
+    if (type == TQ_TURBO4) f = cb->centroids[8 + k];                    // magnitudes
+    else if (k < n) f = (k & half) ? cb->centroids[half + (k & (half - 1))] : -cb->centroids[half + (k & (half - 1))];
+    v[k] = binary16_bits(f);
+  }
+  t[0] = t[1] = t[2] = t[3] = 0;
+  for (int k = 0; k < 4; ++k) {
+    t[0] |= static_cast<uint32_t>(v[k] & 0xff) << (8 * k);
+    t[1] |= static_cast<uint32_t>(v[4 + k] & 0xff) << (8 * k);
+    t[2] |= static_cast<uint32_t>(v[k] >> 8) << (8 * k);
+    t[3] |= static_cast<uint32_t>(v[4 + k] >> 8) << (8 * k);
+  }
+}
+
 static DevCodebook to_dev(const tq_codebook *cb) {
   DevCodebook d;
   memset(&d, 0, sizeof(d));
@@ -292,6 +323,8 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
   a.scale_log2 = scale * 1.4426950408889634f;
   a.cbk = to_dev(cbk);
   a.cbv = to_dev(cbv);
+  code_byte_tables(cbk, k->type, a.tabk);
+  code_byte_tables(cbv, v->type, a.tabv);
   cudaError_t e = (use == TQ_DECODE_MMA) ? launch_decode_mma(k->type, v->type, a, s)
                                          : launch_decode_lut(k->type, v->type, a, s);
   return map_cuda(e);

@@ -57,6 +57,7 @@ struct DecodeArgs {
   int32_t part_stride;    // floats per (head, split) partial
   float scale_log2;       // softmax scale * log2(e)
   DevCodebook cbk, cbv;
+  uint32_t tabk[4], tabv[4];   // binary16 byte tables of the code values (see code_byte_tables)
 };
 
 struct PrefillArgs {
@@ -92,6 +93,9 @@ struct DecodeWorkspaceLayout {
 constexpr size_t kWsHeader = 256;   // status word lives at offset 0
 
 int sm_count();
+// prmt byte tables of a codebook's binary16 code values: t[0], t[1] low bytes of
+// codes 0..3 / 4..7, t[2], t[3] high bytes (turbo4: magnitudes 0..7).
+void code_byte_tables(const tq_codebook *cb, int type, uint32_t t[4]);
 DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int64_t kv_len, int algo);
 
 cudaError_t launch_set_rows(int type, int src_type, const SetRowsArgs &a, cudaStream_t s);
