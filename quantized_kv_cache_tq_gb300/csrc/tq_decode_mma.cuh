@@ -36,8 +36,6 @@
 namespace tq {
 namespace mmadec {
 
-constexpr int NW = 8;                // warps per CTA
-constexpr int NT = NW * 32;
 constexpr int WK = 32;               // keys per warp per iteration (two mma key groups)
 
 __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -120,6 +118,10 @@ __device__ __forceinline__ void v_sel(const uint8_t *qs_row, const uint8_t *sg_r
 template <int T, int NBK, int NBV>
 struct WarpStage {
   static constexpr uint32_t QSB = TypeTraits<T>::QSB, SGB = TypeTraits<T>::SGB;
+  static constexpr uint32_t BYTES0 = (WK * (NBK + NBV) * (QSB + SGB + 2) + 127) / 128 * 128;
+  // warps per CTA (one CTA per SM): 16 when three stages of every warp fit, else 8
+  static constexpr int NW = (16 * 3 * BYTES0 <= 200 * 1024) ? 16 : 8;
+  static constexpr int NT = NW * 32;
   static constexpr uint32_t KQS = 0;
   static constexpr uint32_t KSG = KQS + WK * NBK * QSB;
   static constexpr uint32_t KN = KSG + WK * NBK * SGB;
@@ -128,7 +130,7 @@ struct WarpStage {
   static constexpr uint32_t VN = VSG + WK * NBV * SGB;
   static constexpr uint32_t BYTES = (VN + WK * NBV * 2 + 127) / 128 * 128;
   static constexpr uint32_t TX = WK * (NBK + NBV) * (QSB + SGB + 2);
-  static constexpr int STAGES = (NW * 4 * BYTES <= 104 * 1024) ? 4 : (NW * 3 * BYTES <= 160 * 1024) ? 3 : 2;
+  static constexpr int STAGES = (NW * 4 * BYTES <= 200 * 1024) ? 4 : (NW * 3 * BYTES <= 200 * 1024) ? 3 : 2;
   static constexpr uint32_t RING = STAGES * BYTES;                    // per warp
   static constexpr uint32_t PT = NW * RING;                           // P tiles [NW][NBV][8][WK] fp16
   static constexpr uint32_t QR = PT + NW * NBV * 8 * WK * 2;          // rotated q (floats)
@@ -152,9 +154,10 @@ __device__ __forceinline__ float fast_ex2(float x) {
 }
 
 template <int T, int G, int NBK, int NBV>
-__global__ void __launch_bounds__(NT, 2) decode_mma_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kernel(const DecodeArgs a) {
   static_assert(G == 1 || G == 2 || G == 4, "GQA group must be 1, 2 or 4");
   using WS = WarpStage<T, NBK, NBV>;
+  constexpr int NW = WS::NW, NT = WS::NT;
   using WQ = WarpStageQ<T, G, NBK, NBV>;
   constexpr int QSB = TypeTraits<T>::QSB, SGB = TypeTraits<T>::SGB;
   constexpr int STAGES = WS::STAGES;
@@ -468,12 +471,13 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
   static_assert(bytes <= 227 * 1024, "shared memory");
   // the epilogue: each warp's ring holds its results; the split merge reuses the front
   static_assert(WarpStage<T, NBK, NBV>::RING >= 4 * (2 * G + G * 128 * NBV), "ring too small for the epilogue");
-  static_assert(NW * WarpStage<T, NBK, NBV>::RING >= 4 * (G * 128 * NBV + 2 * G * 256), "merge region");
+  static_assert(WarpStage<T, NBK, NBV>::NW * WarpStage<T, NBK, NBV>::RING >= 4 * (G * 128 * NBV + 2 * G * 256),
+                "merge region");
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<T, G, NBK, NBV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_splits, a.n_kv_heads);
-  decode_mma_kernel<T, G, NBK, NBV><<<grid, NT, bytes, s>>>(a);
+  decode_mma_kernel<T, G, NBK, NBV><<<grid, WarpStage<T, NBK, NBV>::NT, bytes, s>>>(a);
   return cudaGetLastError();
 }
 

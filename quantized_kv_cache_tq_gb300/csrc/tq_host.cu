@@ -37,7 +37,7 @@ static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int64_t kv_len,
                                     int /*algo*/) {
   DecodeWorkspaceLayout L;
-  const int target_ctas = 2 * sm_count();
+  const int target_ctas = sm_count();           // one CTA per SM
   int per_head = (target_ctas + n_kv_heads - 1) / n_kv_heads;
   if (per_head > 256) per_head = 256;     // the merge stages <= 256 splits in shared memory
   int64_t chunk = (kv_len + per_head - 1) / per_head;
@@ -49,6 +49,28 @@ DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int6
   L.part_off = L.counters_off + round_up(sizeof(int32_t) * n_kv_heads, 256);
   const size_t stride = 2 + 128 * static_cast<size_t>(nbv);
   L.total = L.part_off + round_up(sizeof(float) * n_q_heads * L.n_splits * stride, 256);
+  return L;
+}
+
+// Key-range splits of a prefill launch: when the query tiles x KV heads do not
+// cover the SMs, each query tile's keys are split over up to 16 CTAs (at least
+// two key tiles each) and merged by the last one.
+PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t kv_len, int nbk, int nbv) {
+  PrefillWorkspaceLayout L;
+  const int64_t qt = (static_cast<int64_t>(nq) * group + 127) / 128;
+  const int64_t ctas = qt * n_kv_heads;
+  const int bn = (nbk == 2) ? 32 : 64;
+  const int64_t tiles = (kv_len + bn - 1) / bn;
+  int64_t sp = ctas > 0 ? (sm_count() + ctas - 1) / ctas : 1;
+  if (sp > 16) sp = 16;
+  if (sp > tiles / 2) sp = tiles / 2;
+  if (sp < 1) sp = 1;
+  L.n_split = static_cast<int>(sp);
+  L.counters_off = kWsHeader;
+  L.part_off = L.counters_off + round_up(sizeof(int32_t) * qt * n_kv_heads, 256);
+  L.total = L.part_off;
+  if (L.n_split > 1)
+    L.total += round_up(sizeof(float) * qt * n_kv_heads * L.n_split * 128 * (4 + 128 * static_cast<size_t>(nbv)), 256);
   return L;
 }
 
@@ -333,7 +355,7 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
 size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads,
                                   int64_t kv_len) {
   if (check_kv_pair(k, v, n_q_heads, kv_len) != TQ_OK || nq < 0) return 0;
-  return kWsHeader;      // the status word; the kernel keeps everything else on chip
+  return prefill_layout(nq, n_q_heads / k->n_kv_heads, k->n_kv_heads, kv_len, k->n_blocks, v->n_blocks).total;
 }
 
 tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
@@ -347,10 +369,11 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   if (nq < 0 || (causal && nq > kv_len) || !isfinite(scale)) return TQ_ERR_INVALID_ARG;
   if (nq == 0) return TQ_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < kWsHeader)
-    return TQ_ERR_WORKSPACE;
   const int group = n_q_heads / k->n_kv_heads;
   if (!prefill_supported(k->type, v->type, group, k->n_blocks, v->n_blocks)) return TQ_ERR_UNSUPPORTED;
+  const PrefillWorkspaceLayout L = prefill_layout(nq, group, k->n_kv_heads, kv_len, k->n_blocks, v->n_blocks);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
+    return TQ_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (kv_len == 0)
     return map_cuda(cudaMemsetAsync(out, 0, sizeof(float) * nq * n_q_heads * v->head_dim, s));
@@ -378,9 +401,14 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   a.nbk = k->n_blocks;
   a.nbv = v->n_blocks;
   a.causal = causal ? 1 : 0;
+  a.n_split = L.n_split;
+  a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.part_off);
+  a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.counters_off);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.cbk = to_dev(cbk);
   a.cbv = to_dev(cbv);
+  code_byte_tables(cbk, k->type, a.tabk);
+  code_byte_tables(cbv, v->type, a.tabv);
   return map_cuda(launch_prefill(k->type, a, s));
 }
 

@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
       float psum = 0.f;
 #pragma unroll
       for (int i = 0; i < BN; ++i) {
-        s[i] = (i < nvis) ? exp2f(s[i] - m_used) : 0.f;
+        s[i] = (i < nvis) ? tc::ex2(s[i] - m_used) : 0.f;
         psum += s[i];
       }
       l_sum += psum;

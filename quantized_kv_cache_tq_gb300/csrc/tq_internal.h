@@ -70,6 +70,8 @@ struct PrefillArgs {
   const void *q;
   float *out;
   int32_t *status;
+  float *part;            // split partials [q tile][kv head][split][128 rows][4 + 128 nbv]
+  int32_t *counters;      // [q tile][kv head], self-resetting
   int64_t n_cells;
   int64_t kv_len;
   int32_t q_type;
@@ -80,8 +82,10 @@ struct PrefillArgs {
   int32_t dk, dv;
   int32_t nbk, nbv;
   int32_t causal;
+  int32_t n_split;        // key-range splits per query tile
   float scale_log2;
   DevCodebook cbk, cbv;
+  uint32_t tabk[4], tabv[4];
 };
 
 struct DecodeWorkspaceLayout {
@@ -106,6 +110,11 @@ cudaError_t launch_decode_mma_t2(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode_mma_t3(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode_mma_t4(const DecodeArgs &a, cudaStream_t s);
 bool prefill_supported(int ktype, int vtype, int group, int nbk, int nbv);
+struct PrefillWorkspaceLayout {
+  int n_split;
+  size_t counters_off, part_off, total;
+};
+PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t kv_len, int nbk, int nbv);
 cudaError_t launch_prefill(int ktype, const PrefillArgs &a, cudaStream_t s);
 
 }  // namespace tq

@@ -4,37 +4,34 @@
 // is loaded into on-chip tiles, never write an f16 copy of the cache).
 //
 // One CTA = one KV head x 128 query rows (128/G queries x the G query heads of
-// the GQA group, row r = query (r / G), head (r % G)), looping over key tiles of
-// BN = 64 keys (32 when a 256-dim head leaves too little shared memory):
-//   1. cp.async.bulk brings the tile's packed K/V planes into a 2-deep ring;
-//   2. all threads expand them with byte permutes into binary16 centroid tiles
-//      (exact values; block norms are kept aside as floats);
-//   3. one thread issues S_b = Q'_b K'_b^T per 128-dim block b (M=128, N=BN,
-//      K=128) into tensor memory;
-//   4. one thread per row reads S, forms s = sum_b |k_b| S_b, applies the causal
-//      mask, the online softmax (log2 domain, running max raised only when it
-//      grows by more than 2^8, then O is rescaled in tensor memory), and writes
-//      P'_b = p * |v_b| as binary16;
-//   5. one thread issues O_b += P'_b V'_b (M=128, N=128, K=BN) into tensor memory.
-// Precision: Q' and P' are each split into binary16 hi + lo parts (x = hi + lo
-// with lo = fp16(x - hi)) and both halves go through the tensor cores, so S and
-// O carry ~22 significant bits; K' and V' are binary16-exact centroids.  One
-// fp16 rounding of Q' or P' alone moves outputs by up to ~1e-2 on these
-// workloads, beyond the 2e-3 absolute tolerance.
-// The epilogue divides by the softmax sum, rotates each 128-dim block back
-// (o = S H o' / sqrt(128), in registers) and stores fp32 rows.
+// the GQA group, row r = query (r / G), head (r % G)) x one range of key tiles
+// (BN = 64 keys, 32 for 256-dim heads).  Warp roles, connected by mbarriers
+// only (no CTA barrier inside the key loop):
+//   control warp (one thread): cp.async.bulk of the packed K/V planes into a
+//     3-stage ring; issues S_j = Q'K'_j^T into tensor memory, then
+//     O += P'_{j-1} V'_{j-1} -- the tensor cores compute S_j while the softmax
+//     warps work on tile j-1;
+//   4 dequant warps: expand tile j into binary16 K'/V' tiles (exact centroid
+//     values; double buffered; one key-block row per thread);
+//   4 softmax warps (one query row per thread, TMEM lanes 0..127): read S_j,
+//     form s = sum_b |k_b| S_b, apply the causal mask and the online softmax
+//     (log2 domain; the reference maximum is raised only when the row maximum
+//     grows by more than 2^8, then O is rescaled in tensor memory), and write
+//     P'_b = p |v_b| as binary16 hi + lo straight into tensor memory over S_j,
+//     where the PV mma reads it as its A operand.
+// Precision: Q' and P' are split into binary16 hi + lo parts and both go
+// through the tensor cores; K'/V' are exact; accumulation is fp32.
+// Few query tiles (short prompts, verify batches) split the key range over
+// several CTAs; the last CTA to finish a query tile merges the partial
+// (max, sum, O) rows (4 + 128 nbv floats each) with log-sum-exp weights.
+// Epilogue: o = S H (O / l) / sqrt(128) per 128-dim block (V codebook), fp32.
 //
-// Q is rotated into the K codebook's domain on load (q' = H S q / sqrt(128),
-// softmax scale and log2(e) folded in); S = q'.k' = q.k because the rotation is
-// orthogonal, and O accumulates in the V codebook's rotated domain.
-//
-// Shared-memory operand tiles (SWIZZLE_NONE core matrices of 8 rows x 16 B):
-//   Q'_b  A, K-major   [d/8][row/8]  LBO 2048 (along d)   SBO 128 (along rows)
-//   K'_b  B, K-major   [key/8][d/8]  LBO 128  (along d)   SBO 2048 (along keys)
-//   V'_b  B, MN-major  [key/8][d/8]  LBO 2048 (along keys) SBO 128 (along d)
-//   P'_b  A, K-major   [key/8][row/8] LBO 2048 (along keys) SBO 128 (along rows)
-// (hi and lo copies of Q' and P' side by side).
-// K' and V' share one physical layout: a core matrix is 8 keys x 8 dims.
+// Shared-memory operands (SWIZZLE_NONE core matrices of 8 rows x 16 B):
+//   Q'_b (hi, lo)  A, K-major   [d/8][row/8]   LBO 2048 (along d)    SBO 128
+//   K'_b           B, K-major   [key/8][d/8]   LBO 128 (along d)     SBO 2048
+//   V'_b           B, MN-major  [key/8][d/8]   LBO 2048 (along keys) SBO 128
+// Tensor memory (fp32 columns): O_b at 128 b; per buffer S_b at BN b, aliased by
+// P'_(b, part) at (2b + part) BN/2 (fp16 pairs, row = lane).
 #pragma once
 
 #include "tq_common.cuh"
@@ -43,22 +40,22 @@
 namespace tq {
 namespace pf {
 
-constexpr int BM = 128;     // query rows per CTA (TMEM lanes)
-constexpr int NT = 256;     // threads
+constexpr int BM = 128;          // query rows per CTA (TMEM lanes)
+constexpr int NWARP = 9;         // 0-3 softmax, 4-7 dequant, 8 control
+constexpr int NT = NWARP * 32;
+constexpr int STAGES = 3;
 constexpr float kLazyRescale = 8.f;   // log2 units
 
 template <int T, int NBK, int NBV>
-struct Smem {
-  static constexpr int BN = (NBK == 2) ? 32 : 64;                    // keys per tile
+struct Cfg {
+  static constexpr int BN = (NBK == 2) ? 32 : 64;
   static constexpr int QSB = TypeTraits<T>::QSB, SGB = TypeTraits<T>::SGB;
-  static constexpr uint32_t QBLK = 32768;                            // 128 rows x 128 dims fp16
-  static constexpr uint32_t KBLK = BN * 256;                         // BN keys x 128 dims fp16
-  static constexpr uint32_t PBLK = BN * 256;                         // 128 rows x BN keys fp16
-  static constexpr uint32_t Q = 0;                                   // hi [NBK], lo [NBK]
-  static constexpr uint32_t K = Q + 2 * NBK * QBLK;
-  static constexpr uint32_t V = K + NBK * KBLK;
-  static constexpr uint32_t P = V + NBV * KBLK;                      // hi [NBV], lo [NBV]
-  // packed staging ring: per stage K qs, K signs, K norms, V qs, V signs, V norms
+  static constexpr uint32_t QBLK = 32768;                  // 128 rows x 128 dims fp16
+  static constexpr uint32_t TBLK = BN * 256;               // BN keys x 128 dims fp16
+  static constexpr uint32_t KVBUF = (NBK + NBV) * TBLK;    // one K'/V' buffer
+  static constexpr uint32_t Q = 0;                         // [part][NBK] blocks
+  static constexpr uint32_t KV = Q + 2 * NBK * QBLK;       // 2 buffers: K'_b then V'_b
+  // packed staging ring: K qs, K signs, K norms, V qs, V signs, V norms
   static constexpr uint32_t S_KQS = 0;
   static constexpr uint32_t S_KSG = S_KQS + BN * NBK * QSB;
   static constexpr uint32_t S_KN = S_KSG + BN * NBK * SGB;
@@ -66,35 +63,101 @@ struct Smem {
   static constexpr uint32_t S_VSG = S_VQS + BN * NBV * QSB;
   static constexpr uint32_t S_VN = S_VSG + BN * NBV * SGB;
   static constexpr uint32_t STAGE = (S_VN + BN * NBV * 2 + 127) / 128 * 128;
-  static constexpr uint32_t STG = P + 2 * NBV * PBLK;                // 2 stages
-  static constexpr uint32_t NRM = STG + 2 * STAGE;                   // floats [BN][NBK + NBV]
-  static constexpr uint32_t TOTAL = NRM + BN * (NBK + NBV) * 4;
-  static constexpr uint32_t TX = BN * (NBK + NBV) * (QSB + SGB + 2);  // bytes per stage copy
-  // tensor memory: O_b at columns 128 b, S_b at S_COL + BN b
-  static constexpr uint32_t S_COL = NBV * 128;
-  static constexpr int TMEM_COLS = (NBV * 128 + NBK * BN <= 256) ? 256 : 512;
+  static constexpr uint32_t STG = KV + 2 * KVBUF;
+  static constexpr uint32_t NRM = STG + STAGES * STAGE;    // floats [2][BN][NBK + NBV]
+  static constexpr uint32_t TOTAL = NRM + 2 * BN * (NBK + NBV) * 4;
+  static constexpr uint32_t TX = BN * (NBK + NBV) * (QSB + SGB + 2);
+  // tensor memory
+  static constexpr uint32_t SPW = (NBK > NBV ? NBK : NBV) * BN;   // columns per S/P' buffer
+  static constexpr uint32_t SP0 = NBV * 128;
+  static constexpr uint32_t COLS_NEEDED = NBV * 128 + 2 * SPW;
+  static constexpr int TMEM_COLS = COLS_NEEDED <= 256 ? 256 : 512;
+  static constexpr int DVP = 128 * NBV;
 };
 
 __device__ __forceinline__ long long i64min(long long x, long long y) { return x < y ? x : y; }
 __device__ __forceinline__ long long i64max(long long x, long long y) { return x > y ? x : y; }
 
+// tcgen05.mma with the A operand in tensor memory
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc)));
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const uint32_t *r);
+template <>
+__device__ __forceinline__ void tmem_st<16>(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void tmem_st<32>(uint32_t taddr, const uint32_t *r) {
+  tc::tmem_st32(taddr, r);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+struct Bars {
+  uint64_t full[STAGES];   // packed tile staged (tx)
+  uint64_t dq[2];          // K'/V' tile expanded (4 dequant warps)
+  uint64_t sf[2];          // S_j computed (mma commit)
+  uint64_t pf[2];          // P'_j written (4 softmax warps)
+  uint64_t pv[2];          // PV_j computed (mma commit)
+};
+
+// o = S H o' / sqrt(128) of one 128-dim block held by one thread, stored as fp32
+__device__ __forceinline__ void rotate_store_block(float o[128], float scale, const DevCodebook &cbv, float *dst,
+                                                   int dmax, bool store) {
+#pragma unroll
+  for (int hb = 1; hb < 128; hb <<= 1)
+#pragma unroll
+    for (int i = 0; i < 128; ++i)
+      if (!(i & hb)) {
+        const float x = o[i], y = o[i | hb];
+        o[i] = x + y;
+        o[i | hb] = x - y;
+      }
+#pragma unroll
+  for (int i = 0; i < 128; i += 4) {
+    float4 w;
+    w.x = ((cbv.sign_bits[i >> 5] >> ((i + 0) & 31)) & 1u) ? -o[i] * scale : o[i] * scale;
+    w.y = ((cbv.sign_bits[i >> 5] >> ((i + 1) & 31)) & 1u) ? -o[i + 1] * scale : o[i + 1] * scale;
+    w.z = ((cbv.sign_bits[i >> 5] >> ((i + 2) & 31)) & 1u) ? -o[i + 2] * scale : o[i + 2] * scale;
+    w.w = ((cbv.sign_bits[i >> 5] >> ((i + 3) & 31)) & 1u) ? -o[i + 3] * scale : o[i + 3] * scale;
+    if (store && i + 4 <= dmax) *reinterpret_cast<float4 *>(dst + i) = w;
+  }
+}
+
 template <int T, int NBK, int NBV>
 __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
-  using SM = Smem<T, NBK, NBV>;
-  constexpr int QSB = SM::QSB, SGB = SM::SGB, BN = SM::BN;
+  using C = Cfg<T, NBK, NBV>;
+  constexpr int BN = C::BN, QSB = C::QSB, SGB = C::SGB, DVP = C::DVP;
   extern __shared__ __align__(1024) unsigned char smem[];
-  __shared__ __align__(8) uint64_t full[2];
-  __shared__ __align__(8) uint64_t bar_s, bar_pv;
+  __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_slot;
+  __shared__ int s_fail;
+  __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hk = blockIdx.y;
+  const int hk = blockIdx.y, split = blockIdx.z, n_split = gridDim.z;
   const int G = a.group;
-  const int q0 = blockIdx.x * (BM / G);                       // first query of this CTA
+  const int q0 = blockIdx.x * (BM / G);
   const int q_last = min(a.nq, q0 + BM / G) - 1;
-  const int64_t pos0 = a.kv_len - a.nq;                        // position of query 0 (causal)
+  const int64_t pos0 = a.kv_len - a.nq;
   const int64_t kv_hi = a.causal ? i64min(a.kv_len, pos0 + q_last + 1) : a.kv_len;
-  const int n_tiles = static_cast<int>((kv_hi + BN - 1) / BN);
+  const int tiles_all = static_cast<int>((kv_hi + BN - 1) / BN);
+  const int t_lo = static_cast<int>(static_cast<long long>(tiles_all) * split / n_split);
+  const int t_hi = static_cast<int>(static_cast<long long>(tiles_all) * (split + 1) / n_split);
+  const int n_tiles = t_hi - t_lo;
 
   const uint8_t *kqs = a.kqs + static_cast<size_t>(hk) * a.n_cells * NBK * QSB;
   const uint8_t *ksg = SGB ? a.ksg + static_cast<size_t>(hk) * a.n_cells * NBK * SGB : nullptr;
@@ -103,38 +166,38 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
   const uint8_t *vsg = SGB ? a.vsg + static_cast<size_t>(hk) * a.n_cells * NBV * SGB : nullptr;
   const uint16_t *vn = a.vn + static_cast<size_t>(hk) * a.n_cells * NBV;
 
-  auto issue = [&](int tile) {
-    unsigned char *st = smem + SM::STG + (tile & 1) * SM::STAGE;
-    uint64_t *bar = &full[tile & 1];
-    const int64_t key0 = static_cast<int64_t>(tile) * BN;
-    tc::mbar_expect_tx(bar, SM::TX);
-    tc::bulk_g2s(st + SM::S_KQS, kqs + key0 * NBK * QSB, BN * NBK * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + SM::S_KSG, ksg + key0 * NBK * SGB, BN * NBK * SGB, bar);
-    tc::bulk_g2s(st + SM::S_KN, kn + key0 * NBK, BN * NBK * 2, bar);
-    tc::bulk_g2s(st + SM::S_VQS, vqs + key0 * NBV * QSB, BN * NBV * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + SM::S_VSG, vsg + key0 * NBV * SGB, BN * NBV * SGB, bar);
-    tc::bulk_g2s(st + SM::S_VN, vn + key0 * NBV, BN * NBV * 2, bar);
+  auto issue = [&](int j) {       // local tile j -> stage j % STAGES
+    unsigned char *st = smem + C::STG + (j % STAGES) * C::STAGE;
+    uint64_t *bar = &bars.full[j % STAGES];
+    const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
+    tc::mbar_expect_tx(bar, C::TX);
+    tc::bulk_g2s(st + C::S_KQS, kqs + key0 * NBK * QSB, BN * NBK * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + C::S_KSG, ksg + key0 * NBK * SGB, BN * NBK * SGB, bar);
+    tc::bulk_g2s(st + C::S_KN, kn + key0 * NBK, BN * NBK * 2, bar);
+    tc::bulk_g2s(st + C::S_VQS, vqs + key0 * NBV * QSB, BN * NBV * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + C::S_VSG, vsg + key0 * NBV * SGB, BN * NBV * SGB, bar);
+    tc::bulk_g2s(st + C::S_VN, vn + key0 * NBV, BN * NBV * 2, bar);
   };
 
-  if (warp == 0) tc::tmem_alloc<SM::TMEM_COLS>(&tmem_slot);
-  if (tid == 0) {
-    tc::mbar_init(&full[0], 1);
-    tc::mbar_init(&full[1], 1);
-    tc::mbar_init(&bar_s, 1);
-    tc::mbar_init(&bar_pv, 1);
+  if (warp == 0) tc::tmem_alloc<C::TMEM_COLS>(&tmem_slot);
+  if (tid == NT - 32) {
+    s_fail = 0;
+    for (int s = 0; s < STAGES; ++s) tc::mbar_init(&bars.full[s], 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bars.dq[b], 4);
+      tc::mbar_init(&bars.sf[b], 1);
+      tc::mbar_init(&bars.pf[b], 4);
+      tc::mbar_init(&bars.pv[b], 1);
+    }
     tc::mbar_init_fence();
+    tc::fence_async_smem();
+    for (int i = 0; i < STAGES && i < n_tiles; ++i) issue(i);
   }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_slot;
-  if (tid == 0)
-    for (int i = 0; i < 2 && i < n_tiles; ++i) issue(i);
 
-  // ---- Q' = fp16(q rotated per block, scale * log2(e) / sqrt(128) folded in)
+  // ---- Q' = q rotated per block (scale * log2(e) / sqrt(128) folded in), binary16 hi + lo
   {
     const float f = a.scale_log2 * kInvSqrtQK;
-    for (int pr = warp; pr < BM * NBK; pr += NT / 32) {
+    for (int pr = warp; pr < BM * NBK; pr += NWARP) {
       const int r = pr % BM, b = pr / BM;
       const int qi = q0 + r / G, h = hk * G + r % G;
       float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -160,127 +223,197 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float x = v[k] * f;
-        const __half h = __float2half_rn(x);
-        hb[k] = __half_as_ushort(h);
-        lb[k] = __half_as_ushort(__float2half_rn(x - __half2float(h)));
+        const __half hh = __float2half_rn(x);
+        hb[k] = __half_as_ushort(hh);
+        lb[k] = __half_as_ushort(__float2half_rn(x - __half2float(hh)));
       }
-      const uint32_t off = b * SM::QBLK + ((d0 >> 3) * 16 + (r >> 3)) * 128 + (r & 7) * 16 + (d0 & 7) * 2;
-      *reinterpret_cast<uint2 *>(smem + SM::Q + off) =
+      const uint32_t off = b * C::QBLK + ((d0 >> 3) * 16 + (r >> 3)) * 128 + (r & 7) * 16 + (d0 & 7) * 2;
+      *reinterpret_cast<uint2 *>(smem + C::Q + off) =
           make_uint2(hb[0] | (static_cast<uint32_t>(hb[1]) << 16), hb[2] | (static_cast<uint32_t>(hb[3]) << 16));
-      *reinterpret_cast<uint2 *>(smem + SM::Q + NBK * SM::QBLK + off) =
+      *reinterpret_cast<uint2 *>(smem + C::Q + NBK * C::QBLK + off) =
           make_uint2(lb[0] | (static_cast<uint32_t>(lb[1]) << 16), lb[2] | (static_cast<uint32_t>(lb[3]) << 16));
     }
   }
-
-  const Tab tab_k = make_tab<T>(a.cbk);
-  const Tab tab_v = make_tab<T>(a.cbv);
-  constexpr uint32_t ID_S = tc::idesc_f16(BM, SM::BN, false, false);
-  constexpr uint32_t ID_PV = tc::idesc_f16(BM, 128, false, true);
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
   const uint32_t sbase = tc::smem_u32(smem);
+  float *nrm = reinterpret_cast<float *>(smem + C::NRM);
 
-  // softmax state of row `tid` (threads 0..127)
-  const int row = tid;
+  // softmax state (warps 0..3: row = tid)
+  const int row = tid & (BM - 1);
   const int row_q = q0 + row / G;
-  const bool row_ok = tid < BM && row_q < a.nq;
-  const int64_t row_end = a.causal ? (pos0 + row_q + 1) : a.kv_len;      // keys < row_end visible
+  const bool row_ok = warp < 4 && row_q < a.nq;
+  const int64_t row_end = a.causal ? (pos0 + row_q + 1) : a.kv_len;
   float m_used = -INFINITY, l_sum = 0.f;
-  float *nrm = reinterpret_cast<float *>(smem + SM::NRM);                 // [BN][NBK + NBV]
-  bool failed = false;
 
-  for (int tile = 0; tile < n_tiles && !failed; ++tile) {
-    const unsigned char *st = smem + SM::STG + (tile & 1) * SM::STAGE;
-    bool ok = tc::mbar_wait(&full[tile & 1], (tile >> 1) & 1);
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-
-    // ---- expand the packed tile into binary16 K' / V' tiles
-    for (int it = tid; it < (NBK + NBV) * BN * 16; it += NT) {
-      const int bb = it / (BN * 16), rem = it % (BN * 16);
-      const int dc = rem / BN, key = rem % BN;
-      const bool is_v = bb >= NBK;
-      const int b = is_v ? bb - NBK : bb;
-      const int nb = is_v ? NBV : NBK;
-      const uint8_t *qrow = st + (is_v ? SM::S_VQS : SM::S_KQS) + (key * nb + b) * QSB;
-      uint32_t sel;
-      if (T == 4) {
-        sel = reinterpret_cast<const uint32_t *>(qrow)[dc];
-      } else {
-        const uint32_t w = reinterpret_cast<const uint32_t *>(qrow)[dc >> 1];
-        uint32_t sg = 0;
-        if (T == 3) sg = reinterpret_cast<const uint32_t *>(st + (is_v ? SM::S_VSG : SM::S_KSG) + (key * nb + b) * SGB)[dc >> 2];
-        uint32_t s0, s1;
-        sel_words<T>(w, sg, ((dc >> 1) & 1) != 0, s0, s1);
-        sel = (dc & 1) ? s1 : s0;
+  if (warp == 8) {
+    // ===================== control: copies and mma issue =====================
+    if (lane == 0) {
+      constexpr uint32_t ID_S = tc::idesc_f16(BM, BN, false, false);
+      constexpr uint32_t ID_PV = tc::idesc_f16(BM, 128, false, true);
+      auto issue_pv = [&](int j) {
+        const uint32_t pbuf = tmem + C::SP0 + (j & 1) * C::SPW;
+        const uint32_t vbuf = sbase + C::KV + (j & 1) * C::KVBUF + NBK * C::TBLK;
+#pragma unroll
+        for (int b = 0; b < NBV; ++b)
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < BN / 16; ++ks) {
+              const uint64_t bd = tc::sdesc(vbuf + b * C::TBLK + ks * 4096, 2048, 128);
+              mma_f16_ta(tmem + b * 128, pbuf + (2 * b + part) * (BN / 2) + ks * 8, bd, ID_PV,
+                         j > 0 || part > 0 || ks > 0);
+            }
+        tc::mma_commit(&bars.pv[j & 1]);
+      };
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        ok = tc::mbar_wait(&bars.dq[j & 1], (j >> 1) & 1);
+        if (ok && j >= 2) ok = tc::mbar_wait(&bars.pv[j & 1], ((j - 2) >> 1) & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t sbuf = tmem + C::SP0 + (j & 1) * C::SPW;
+        const uint32_t kbuf = sbase + C::KV + (j & 1) * C::KVBUF;
+#pragma unroll
+        for (int b = 0; b < NBK; ++b)
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t ad = tc::sdesc(sbase + C::Q + (part * NBK + b) * C::QBLK + ks * 4096, 2048, 128);
+              const uint64_t bd = tc::sdesc(kbuf + b * C::TBLK + ks * 256, 128, 2048);
+              tc::mma_f16(sbuf + b * BN, ad, bd, ID_S, part > 0 || ks > 0);
+            }
+        tc::mma_commit(&bars.sf[j & 1]);
+        if (j + STAGES < n_tiles) issue(j + STAGES);           // the stage of tile j was consumed
+        if (j >= 1) {
+          ok = tc::mbar_wait(&bars.pf[(j - 1) & 1], ((j - 1) >> 1) & 1);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_pv(j - 1);
+        }
       }
-      const Tab &tb = is_v ? tab_v : tab_k;
-      uint4 o;
-      dq4<T>(sel & 0xffffu, tb, o.x, o.y);
-      dq4<T>(sel >> 16, tb, o.z, o.w);
-      *reinterpret_cast<uint4 *>(smem + (is_v ? SM::V : SM::K) + b * SM::KBLK + ((key >> 3) * 16 + dc) * 128 +
-                                 (key & 7) * 16) = o;
+      if (ok && n_tiles > 0) {
+        const int j = n_tiles - 1;
+        ok = tc::mbar_wait(&bars.pf[j & 1], (j >> 1) & 1);
+        if (ok) {
+          tc::fence_after_sync();
+          issue_pv(j);
+        }
+      }
+      if (!ok) s_fail = 1;
     }
-    for (int i = tid; i < BN * (NBK + NBV); i += NT) {
-      const int key = i / (NBK + NBV), j = i % (NBK + NBV);
-      const uint16_t *np = reinterpret_cast<const uint16_t *>(st + (j < NBK ? SM::S_KN : SM::S_VN));
-      const float n = (j < NBK) ? __half2float(__ushort_as_half(np[key * NBK + j]))
-                                : __half2float(__ushort_as_half(np[key * NBV + (j - NBK)]));
-      nrm[key * (NBK + NBV) + j] = n;
-    }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    if (tid == 0) {
-      if (tile + 2 < n_tiles) issue(tile + 2);              // staging stage is free again
+  } else if (warp >= 4) {
+    // ===================== dequant: one key-block row per thread =====================
+    const int dt = tid - 128;                                  // 0..127
+    const Tab tab_k{a.tabk[0], a.tabk[1], a.tabk[2], a.tabk[3]};
+    const Tab tab_v{a.tabv[0], a.tabv[1], a.tabv[2], a.tabv[3]};
+    for (int j = 0; j < n_tiles; ++j) {
+      bool ok = tc::mbar_wait(&bars.full[j % STAGES], (j / STAGES) & 1);
+      if (ok && j >= 2) ok = tc::mbar_wait(&bars.pv[j & 1], ((j - 2) >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { s_fail = 1; break; }
+      tc::fence_after_sync();
+      const unsigned char *st = smem + C::STG + (j % STAGES) * C::STAGE;
+      unsigned char *buf = smem + C::KV + (j & 1) * C::KVBUF;
+      for (int r = dt; r < (NBK + NBV) * BN; r += 128) {
+        const bool is_v = r >= NBK * BN;
+        const int rr = is_v ? r - NBK * BN : r;
+        const int b = rr / BN, key = rr % BN;
+        const int nb = is_v ? NBV : NBK;
+        const Tab &tb = is_v ? tab_v : tab_k;
+        const uint8_t *qrow = st + (is_v ? C::S_VQS : C::S_KQS) + (key * nb + b) * QSB;
+        unsigned char *dst = buf + (is_v ? NBK + b : b) * C::TBLK + (key >> 3) * 2048 + (key & 7) * 16;
+        if (T == 4) {
 #pragma unroll
-      for (int b = 0; b < NBK; ++b)
+          for (int w4 = 0; w4 < 4; ++w4) {
+            const uint4 w = reinterpret_cast<const uint4 *>(qrow)[w4];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int part = 0; part < 2; ++part)                     // q'_hi, then q'_lo
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t ad =
-                tc::sdesc(sbase + SM::Q + (part * NBK + b) * SM::QBLK + ks * 4096, 2048, 128);
-            const uint64_t bd = tc::sdesc(sbase + SM::K + b * SM::KBLK + ks * 256, 128, 2048);
-            tc::mma_f16(tmem + SM::S_COL + b * BN, ad, bd, ID_S, part > 0 || ks > 0);
+            for (int i = 0; i < 4; ++i) {
+              uint4 o;
+              dq4<4>(ws[i], tb, o.x, o.y);
+              dq4<4>(ws[i] >> 16, tb, o.z, o.w);
+              *reinterpret_cast<uint4 *>(dst + (4 * w4 + i) * 128) = o;
+            }
           }
-      tc::mma_commit(&bar_s);
+        } else {
+          uint32_t sgw[4] = {0u, 0u, 0u, 0u};
+          if (T == 3) {
+            const uint4 sg4 =
+                *reinterpret_cast<const uint4 *>(st + (is_v ? C::S_VSG : C::S_KSG) + (key * nb + b) * SGB);
+            sgw[0] = sg4.x; sgw[1] = sg4.y; sgw[2] = sg4.z; sgw[3] = sg4.w;
+          }
+#pragma unroll
+          for (int hq = 0; hq < 2; ++hq) {
+            const uint4 w = reinterpret_cast<const uint4 *>(qrow)[hq];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int wi = 4 * hq + i;                       // qs word: elements 16 wi ..
+              uint32_t s0, s1;
+              sel_words<T>(ws[i], sgw[wi >> 1], (wi & 1) != 0, s0, s1);
+              uint4 o0, o1;
+              dq4<T>(s0, tb, o0.x, o0.y);
+              dq4<T>(s0 >> 16, tb, o0.z, o0.w);
+              dq4<T>(s1, tb, o1.x, o1.y);
+              dq4<T>(s1 >> 16, tb, o1.z, o1.w);
+              *reinterpret_cast<uint4 *>(dst + (2 * wi) * 128) = o0;
+              *reinterpret_cast<uint4 *>(dst + (2 * wi + 1) * 128) = o1;
+            }
+          }
+        }
+        const uint16_t *np = reinterpret_cast<const uint16_t *>(st + (is_v ? C::S_VN : C::S_KN));
+        nrm[(j & 1) * BN * (NBK + NBV) + key * (NBK + NBV) + (is_v ? NBK + b : b)] =
+            __half2float(__ushort_as_half(np[key * nb + b]));
+      }
+      tc::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.dq[j & 1]);
     }
-    ok = tc::mbar_wait(&bar_s, tile & 1);
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-    tc::fence_after_sync();
-
-    // ---- softmax: one thread per row (warps 0..3 own TMEM lanes 0..127)
-    if (warp < 4) {
-      const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+  } else {
+    // ===================== softmax: one query row per thread =====================
+    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = tc::mbar_wait(&bars.sf[j & 1], (j >> 1) & 1);
+      if (ok) ok = tc::mbar_wait(&bars.dq[j & 1], (j >> 1) & 1);     // norms of tile j are written
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc::fence_after_sync();
+      const uint32_t sbuf = tmem + lane_off + C::SP0 + (j & 1) * C::SPW;
+      const float *nr = nrm + (j & 1) * BN * (NBK + NBV);
       float s[BN];
 #pragma unroll
       for (int i = 0; i < BN; ++i) s[i] = 0.f;
+      {
+        uint32_t r0[NBK * BN];                                 // all S columns, one wait
 #pragma unroll
-      for (int b = 0; b < NBK; ++b)
+        for (int c0 = 0; c0 < NBK * BN; c0 += 32) tc::tmem_ld32(sbuf + c0, r0 + c0);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t r0[32];
-          tc::tmem_ld32(tmem + lane_off + SM::S_COL + b * BN + c0, r0);
-          tc::tmem_wait_ld();
+        for (int b = 0; b < NBK; ++b)
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            s[c0 + i] = fmaf(nrm[(c0 + i) * (NBK + NBV) + b], __uint_as_float(r0[i]), s[c0 + i]);
-        }
-      const int64_t key0 = static_cast<int64_t>(tile) * BN;
+          for (int i = 0; i < BN; ++i) s[i] = fmaf(nr[i * (NBK + NBV) + b], __uint_as_float(r0[b * BN + i]), s[i]);
+      }
+      const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
       const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(BN, row_end - key0))) : 0;
       float mt = -INFINITY;
 #pragma unroll
       for (int i = 0; i < BN; ++i)
         if (i < nvis) mt = fmaxf(mt, s[i]);
-      // raise the reference maximum only when the row max grew by more than 2^8;
-      // the tensor-memory rescale is warp-collective, so lanes that need none use 1
       const bool raise = mt > m_used + kLazyRescale || (m_used == -INFINITY && mt > -INFINITY);
       const float fct = (raise && m_used != -INFINITY) ? exp2f(m_used - mt) : 1.f;
       if (raise) m_used = mt;
       if (__any_sync(0xffffffffu, fct != 1.f)) {
+        // O must be stable: wait for the PV mma of the previous tile
+        bool okp = (j == 0) || tc::mbar_wait(&bars.pv[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        if (!__all_sync(0xffffffffu, okp)) { ok = false; break; }
+        tc::fence_after_sync();
         l_sum *= fct;
 #pragma unroll
-        for (int c = 0; c < NBV * 128; c += 32) {
+        for (int c = 0; c < DVP; c += 32) {
           uint32_t r[32];
           tc::tmem_ld32(tmem + lane_off + c, r);
           tc::tmem_wait_ld();
@@ -288,115 +421,163 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * fct);
           tc::tmem_st32(tmem + lane_off + c, r);
         }
-        tc::tmem_wait_st();
       }
       float psum = 0.f;
 #pragma unroll
       for (int i = 0; i < BN; ++i) {
-        s[i] = (i < nvis) ? exp2f(s[i] - m_used) : 0.f;
+        s[i] = (i < nvis) ? tc::ex2(s[i] - m_used) : 0.f;
         psum += s[i];
       }
       l_sum += psum;
+      // P'_(b, hi/lo) into tensor memory over S_j: row = lane, fp16 pairs of keys
 #pragma unroll
-      for (int b = 0; b < NBV; ++b)
+      for (int b = 0; b < NBV; ++b) {
+        uint32_t ph[BN / 2], pl[BN / 2];
 #pragma unroll
-        for (int kc = 0; kc < BN / 8; ++kc) {
-          uint32_t wh[4], wl[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int k0 = kc * 8 + 2 * j;
-            // masked keys may carry garbage norms: select, never multiply, a zero
-            const float x0 = s[k0] > 0.f ? s[k0] * nrm[k0 * (NBK + NBV) + NBK + b] : 0.f;
-            const float x1 = s[k0 + 1] > 0.f ? s[k0 + 1] * nrm[(k0 + 1) * (NBK + NBV) + NBK + b] : 0.f;
-            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-            wh[j] = __half_as_ushort(h0) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-            wl[j] = __half_as_ushort(__float2half_rn(x0 - __half2float(h0))) |
-                    (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x1 - __half2float(h1)))) << 16);
-          }
-          const uint32_t off = b * SM::PBLK + (kc * 16 + (row >> 3)) * 128 + (row & 7) * 16;
-          *reinterpret_cast<uint4 *>(smem + SM::P + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-          *reinterpret_cast<uint4 *>(smem + SM::P + NBV * SM::PBLK + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        for (int i = 0; i < BN / 2; ++i) {
+          const int k0 = 2 * i;
+          // masked keys may carry garbage norms: select, never multiply, a zero
+          const float x0 = s[k0] > 0.f ? s[k0] * nr[k0 * (NBK + NBV) + NBK + b] : 0.f;
+          const float x1 = s[k0 + 1] > 0.f ? s[k0 + 1] * nr[(k0 + 1) * (NBK + NBV) + NBK + b] : 0.f;
+          const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+          ph[i] = __half_as_ushort(h0) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+          pl[i] = __half_as_ushort(__float2half_rn(x0 - __half2float(h0))) |
+                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x1 - __half2float(h1)))) << 16);
         }
+        tmem_st<BN / 2>(sbuf + (2 * b) * (BN / 2), ph);
+        tmem_st<BN / 2>(sbuf + (2 * b + 1) * (BN / 2), pl);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.pf[j & 1]);
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    if (tid == 0) {
-#pragma unroll
-      for (int b = 0; b < NBV; ++b)
-#pragma unroll
-        for (int part = 0; part < 2; ++part)                     // P'_hi, then P'_lo
-#pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks) {
-            const uint64_t ad = tc::sdesc(sbase + SM::P + (part * NBV + b) * SM::PBLK + ks * 4096, 2048, 128);
-            const uint64_t bd = tc::sdesc(sbase + SM::V + b * SM::KBLK + ks * 4096, 2048, 128);
-            tc::mma_f16(tmem + b * 128, ad, bd, ID_PV, tile > 0 || part > 0 || ks > 0);
-          }
-      tc::mma_commit(&bar_pv);
+    // the last PV must be complete before O is read
+    if (ok && n_tiles > 0) {
+      const int j = n_tiles - 1;
+      ok = tc::mbar_wait(&bars.pv[j & 1], (j >> 1) & 1);
+      ok = __all_sync(0xffffffffu, ok);
+      tc::fence_after_sync();
     }
-    ok = tc::mbar_wait(&bar_pv, tile & 1);
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-    tc::fence_after_sync();
+    if (!ok) s_fail = 1;
   }
 
-  if (failed) {
-    if (tid == 0) set_status(a.status, TQ_ERR_TIMEOUT);
-  } else if (warp < 4) {                 // warp-uniform: tensor-memory loads are collective
-    // ---- epilogue: o = S H (O / l) / sqrt(128) per 128-dim block, fp32 rows
-    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-    const float inv = (l_sum > 0.f ? 1.f / l_sum : 0.f) * kInvSqrtQK;
-    const int h = hk * G + row % G;
-    float *orow = a.out + (static_cast<size_t>(row_ok ? row_q : 0) * a.n_q_heads + h) * a.dv;
+  // ===================== epilogue =====================
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const bool failed = s_fail != 0;
+  if (failed && tid == 0) set_status(a.status, TQ_ERR_TIMEOUT);
+  const int h_row = hk * G + row % G;
+  float *orow = a.out + (static_cast<size_t>(row_ok ? row_q : 0) * a.n_q_heads + h_row) * a.dv;
+
+  if (n_split == 1) {
+    if (warp < 4 && !failed) {
+      const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+      const float inv = (l_sum > 0.f ? 1.f / l_sum : 0.f) * kInvSqrtQK;
 #pragma unroll 1
-    for (int b = 0; b < NBV; ++b) {
-      float o[128];
+      for (int b = 0; b < NBV; ++b) {
+        float o[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld32(tmem + lane_off + b * 128 + 32 * c, r);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = n_tiles > 0 ? __uint_as_float(r[i]) : 0.f;
+        }
+        rotate_store_block(o, inv, a.cbv, orow + b * 128, a.dv - b * 128, row_ok);
+      }
+    }
+  } else {
+    // split key range: store (m, l, O) of every row; the last CTA of this query tile merges
+    const size_t tile_id = static_cast<size_t>(blockIdx.x) * a.n_kv_heads + hk;
+    const size_t stride = 4 + DVP;             // m, l, 2 pad floats: O rows stay 16-byte aligned
+    float *part = a.part + (tile_id * n_split + split) * BM * stride;
+    if (warp < 4) {
+      const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+      float *pr = part + static_cast<size_t>(row) * stride;
+      const bool has = !failed && n_tiles > 0;
+      pr[0] = has ? m_used : -INFINITY;
+      pr[1] = has ? l_sum : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < DVP; c += 32) {
         uint32_t r[32];
-        tc::tmem_ld32(tmem + lane_off + b * 128 + 32 * c, r);
+        tc::tmem_ld32(tmem + lane_off + c, r);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[32 * c + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4 *>(pr + 4 + c + i) =
+              has ? make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                                __uint_as_float(r[i + 3]))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-#pragma unroll
-      for (int hb = 1; hb < 128; hb <<= 1)
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (!(i & hb)) {
-            const float x = o[i], y = o[i | hb];
-            o[i] = x + y;
-            o[i | hb] = x - y;
-          }
-      const int dmax = a.dv - b * 128;
-#pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        float4 w;
-        w.x = ((a.cbv.sign_bits[i >> 5] >> ((i + 0) & 31)) & 1u) ? -o[i] * inv : o[i] * inv;
-        w.y = ((a.cbv.sign_bits[i >> 5] >> ((i + 1) & 31)) & 1u) ? -o[i + 1] * inv : o[i + 1] * inv;
-        w.z = ((a.cbv.sign_bits[i >> 5] >> ((i + 2) & 31)) & 1u) ? -o[i + 2] * inv : o[i + 2] * inv;
-        w.w = ((a.cbv.sign_bits[i >> 5] >> ((i + 3) & 31)) & 1u) ? -o[i + 3] * inv : o[i + 3] * inv;
-        if (row_ok && i + 4 <= dmax) *reinterpret_cast<float4 *>(orow + b * 128 + i) = w;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(&a.counters[tile_id], 1) == n_split - 1);
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      const float *base = a.part + tile_id * n_split * BM * stride;
+      float *wts = reinterpret_cast<float *>(smem + C::STG);        // [BM][n_split] weights / L
+      float *acc = reinterpret_cast<float *>(smem + C::Q);          // [BM][DVP] merged rows
+      if (tid < min(BM, (a.nq - q0) * G)) {
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < n_split; ++s2)
+          M = fmaxf(M, __ldcg(base + (static_cast<size_t>(s2) * BM + tid) * stride));
+        float L = 0.f;
+        for (int s2 = 0; s2 < n_split; ++s2) {
+          const float *p = base + (static_cast<size_t>(s2) * BM + tid) * stride;
+          const float m = __ldcg(p);
+          const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+          wts[tid * n_split + s2] = w;
+          L += w * __ldcg(p + 1);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int s2 = 0; s2 < n_split; ++s2) wts[tid * n_split + s2] *= inv;
       }
+      __syncthreads();
+      const int rows_valid = min(BM, (a.nq - q0) * G);          // rows of queries < nq
+      for (int i = tid; i < rows_valid * DVP; i += NT) {
+        const int r = i / DVP, d = i % DVP;
+        float o = 0.f;
+        for (int s2 = 0; s2 < n_split; ++s2)
+          o += wts[r * n_split + s2] * __ldcg(base + (static_cast<size_t>(s2) * BM + r) * stride + 4 + d);
+        acc[i] = o;
+      }
+      __syncthreads();
+      if (warp < 4) {
+#pragma unroll 1
+        for (int b = 0; b < NBV; ++b) {
+          float o[128];
+#pragma unroll
+          for (int i = 0; i < 128; ++i) o[i] = acc[row * DVP + b * 128 + i];
+          rotate_store_block(o, kInvSqrtQK, a.cbv, orow + b * 128, a.dv - b * 128, row_ok);
+        }
+      }
+      if (tid == 0) a.counters[tile_id] = 0;
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc<SM::TMEM_COLS>(tmem);
+  if (warp == 0) tc::tmem_dealloc<C::TMEM_COLS>(tmem);
 }
 
 template <int T, int NBK, int NBV>
 cudaError_t launch_one(const PrefillArgs &a, cudaStream_t s) {
-  using SM = Smem<T, NBK, NBV>;
-  static_assert(SM::TOTAL <= 227 * 1024, "shared memory");
+  using C = Cfg<T, NBK, NBV>;
+  static_assert(C::TOTAL <= 227 * 1024, "shared memory");
+  static_assert(C::COLS_NEEDED <= 512, "tensor memory");
+  static_assert(C::BN % 16 == 0 && C::BN <= 64, "key tile");
+  // the merge reuses the Q region for BM x DVP floats and the staging ring for the weights
+  static_assert(2 * NBK * C::QBLK >= BM * C::DVP * 4, "merge buffer");
+  static_assert(STAGES * C::STAGE >= BM * 16 * 4, "merge weights");
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, NBK, NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SM::TOTAL);
+                                       (int)C::TOTAL);
   if (e != cudaSuccess) return e;
-  const int rows = a.nq * a.group;
-  dim3 grid((rows + BM - 1) / BM, a.n_kv_heads);
-  static_assert(SM::BN % 16 == 0 && SM::BN <= 64, "key tile");
-  prefill_kernel<T, NBK, NBV><<<grid, NT, SM::TOTAL, s>>>(a);
+  dim3 grid((a.nq * a.group + BM - 1) / BM, a.n_kv_heads, a.n_split);
+  prefill_kernel<T, NBK, NBV><<<grid, NT, C::TOTAL, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -110,14 +110,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
 }
 
 // Bounded wait for phase `parity` of `bar`; false if the limit was reached.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit = 1ll << 24) {
+// Each try_wait may suspend the thread for up to ~20 us (suspend-time hint), so a
+// waiting warp does not spin on the issue slots its neighbours need; the
+// iteration limit bounds the whole wait to well under a minute.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long limit = 1ll << 20) {
   const uint32_t a = smem_u32(bar);
   for (long long it = 0; it < limit; ++it) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(a), "r"(parity)
+        : "r"(a), "r"(parity), "r"(20000u)
         : "memory");
     if (ok) return true;
   }
@@ -131,6 +134,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {   // 2^x (approximate, ~2 ulp); -inf -> 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
