@@ -446,7 +446,7 @@ def run_prefill_extra(tq, torch, dev, tflops_peak, nqs=(4096, 512)):
     for nq in nqs:
         q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.bfloat16)
         out = torch.empty((nq, HQ, DD), device=dev)
-        ws = tq.workspace(256, dev)
+        ws = tq.workspace(tq._lib.tq_fattn_prefill_workspace(kc.c, vc.c, nq, HQ, L), dev)
         t = time_graph(torch, lambda: tq.fattn_prefill(kc, vc, cbk, cbv, q, L, out=out, ws=ws), reps=5)
         pairs = sum(min(L, L - nq + i + 1) for i in range(nq))
         flop = 4.0 * DD * pairs * HQ
@@ -474,7 +474,7 @@ def run_int8_extra(tq, torch, dev, tflops_peak, ctx=140000, nq=2048):
     perm = torch.randperm(ctx, generator=gen, device=dev).to(torch.int32)
     q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.float16)
     out = torch.empty((nq, HQ, DD), device=dev)
-    ws = tq.workspace(256, dev)
+    ws = tq.workspace(tq._lib.tq_int8_prompt_attn_workspace(nq, HQ, HK, DD, ctx), dev)
     t = time_graph(torch, lambda: tq.int8_prompt_attn(k, sk, v, sv, perm, ctx, q, out=out, ws=ws), reps=3)
     pairs = sum(min(ctx, ctx - nq + i + 1) for i in range(nq))
     flop = 4.0 * DD * pairs * HQ

@@ -6,6 +6,13 @@
 
 namespace tq {
 
+// 2^x for x <= 0 (split weights), approximate to a few ulp.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Floats of shared memory decode_merge needs.
 __host__ __device__ inline int merge_smem_floats(int group, int nbv, int n_splits) {
   return group * QK * nbv + 2 * group * n_splits;
@@ -18,67 +25,53 @@ __host__ __device__ inline int merge_smem_floats(int group, int nbv, int n_split
 //   o = S H o' / sqrt(128)   (R^T for R = H S / sqrt(128)),
 // writes out[h][0 .. dv) and resets the counter so the next launch (or graph
 // replay) finds it at zero.  No CTA ever waits for another one.
-// The split maxima and sums are staged in shared memory first and the partial
-// outputs are read with independent loads, so the merge costs a few L2 round
-// trips.  `smem` must hold merge_smem_floats(group, nbv, n_splits) floats.
+// Each warp merges 32 consecutive outputs of one head, 16 splits at a time:
+// lane s < 16 holds split s's maximum and sum, every lane loads its output's
+// values of the 16 splits at once (one L2 round trip per 16 splits).
+// `smem` must hold merge_smem_floats(group, nbv, n_splits) floats.
 template <int NT>
 __device__ void decode_merge(const DecodeArgs &a, int hk, float *smem) {
   __shared__ int s_last;
-  __threadfence();
+  // the CTA's partial stores are ordered before the counter update by the CTA
+  // barrier plus thread 0's release fence; the last CTA's acquire fence orders
+  // its loads of the other partials after it
   __syncthreads();
   if (threadIdx.x == 0) {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     const int prev = atomicAdd(&a.counters[hk], 1);
     s_last = (prev == a.n_splits - 1);
+    if (s_last) asm volatile("fence.acq_rel.gpu;" ::: "memory");
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 
   const int G = a.group, ns = a.n_splits, dvp = QK * a.nbv;
   const int stride = a.part_stride;
   float *orot = smem;                     // [G][dvp]
-  float *wt = smem + G * dvp;             // [G][ns]: m_s, then the weights
-  float *ls = wt + G * ns;                // [G][ns]
   const float *base = a.part + static_cast<size_t>(hk) * G * ns * stride;
-  for (int i = threadIdx.x; i < G * ns; i += NT) {
-    wt[i] = __ldcg(base + static_cast<size_t>(i) * stride);
-    ls[i] = __ldcg(base + static_cast<size_t>(i) * stride + 1);
-  }
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int g = warp; g < G; g += NT / 32) {
-    float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, wt[g * ns + s]);
-    M = warp_max(M);
-    float L = 0.f;
-    for (int s = lane; s < ns; s += 32) {
-      const float m = wt[g * ns + s];
-      L += (m == -INFINITY) ? 0.f : ls[g * ns + s] * exp2f(m - M);
-    }
-    L = warp_sum(L);
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    __syncwarp();
-    for (int s = lane; s < ns; s += 32) {
-      const float m = wt[g * ns + s];
-      wt[g * ns + s] = (m == -INFINITY) ? 0.f : exp2f(m - M) * inv;
-    }
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < G * dvp; i += NT) {
-    const int g = i / dvp, d = i % dvp;
-    const float *p = base + static_cast<size_t>(g) * ns * stride + 2 + d;
-    const float *w = wt + g * ns;
-    float o = 0.f;
-    int s = 0;
-    for (; s + 8 <= ns; s += 8) {
-      float v[8];
+  for (int i0 = warp * 32; i0 < G * dvp; i0 += NT) {     // dvp is a multiple of 32: one head per warp pass
+    const int i = i0 + lane, g = i / dvp, d = i % dvp;
+    const float *p = base + static_cast<size_t>(g) * ns * stride;
+    float M = -INFINITY, L = 0.f, o = 0.f;
+    for (int s0 = 0; s0 < ns; s0 += 16) {
+      const int n = min(16, ns - s0);
+      const float *ps = p + static_cast<size_t>(s0) * stride;
+      const float ms = (lane < n) ? __ldcg(ps + static_cast<size_t>(lane) * stride) : -INFINITY;
+      const float ls = (lane < n) ? __ldcg(ps + static_cast<size_t>(lane) * stride + 1) : 0.f;
+      float ov[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = __ldcg(p + static_cast<size_t>(s + j) * stride);
+      for (int j = 0; j < 16; ++j) ov[j] = (j < n) ? __ldcg(ps + static_cast<size_t>(j) * stride + 2 + d) : 0.f;
+      const float Mn = fmaxf(M, warp_max(ms));
+      const float f = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
+      const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - Mn);
+      L = L * f + warp_sum(w * ls);
+      o *= f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o += w[s + j] * v[j];
+      for (int j = 0; j < 16; ++j) o = fmaf(__shfl_sync(0xffffffffu, w, j), ov[j], o);
+      M = Mn;
     }
-    for (; s < ns; ++s) o += w[s] * __ldcg(p + static_cast<size_t>(s) * stride);
-    orot[i] = o;
+    orot[i] = (L > 0.f) ? o / L : 0.f;
   }
   __syncthreads();
 
@@ -102,27 +95,38 @@ __device__ void decode_merge(const DecodeArgs &a, int hk, float *smem) {
   if (threadIdx.x == 0) a.counters[hk] = 0;
 }
 
-// Rotate the query heads of KV head hk into the K codebook's domain and fold in
-// the softmax scale:  q'_g = scale * log2(e) * H S q_g / sqrt(128), per block.
-// Zero-pads q beyond dk.  Writes qrot[g * 128*nbk + d].
+// Query block wb = g * nbk + b (head hk * group + g, dims 128 b ..): lane i
+// loads dims 4i .. 4i+3 of the block, zero beyond dk.
+__device__ __forceinline__ void load_query_block(const DecodeArgs &a, int hk, int wb, int lane, float v[4]) {
+  const int g = wb / a.nbk, b = wb % a.nbk;
+  const float *q = a.q + static_cast<size_t>(hk * a.group + g) * a.dk;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int d = b * QK + 4 * lane + r;
+    v[r] = (d < a.dk) ? q[d] : 0.f;
+  }
+}
+
+// Rotate a loaded query block into the K codebook's domain and fold in the
+// softmax scale:  q'_g = scale * log2(e) * H S q_g / sqrt(128).
+// Writes qrot[g * 128*nbk + d].
+__device__ __forceinline__ void rotate_query_block(const DecodeArgs &a, int wb, int lane, float v[4], float *qrot) {
+  const int g = wb / a.nbk, b = wb % a.nbk;
+  const float f = a.scale_log2 * kInvSqrtQK;
+  apply_signs(v, a.cbk, lane);
+  wht128_warp(v, lane);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) qrot[g * QK * a.nbk + b * QK + 4 * lane + r] = v[r] * f;
+}
+
+// All query heads of KV head hk, one block per warp at a time.
 template <int NT>
 __device__ void rotate_queries(const DecodeArgs &a, int hk, float *qrot) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int dkp = QK * a.nbk;
-  const float f = a.scale_log2 * kInvSqrtQK;
   for (int wb = warp; wb < a.group * a.nbk; wb += NT / 32) {
-    const int g = wb / a.nbk, b = wb % a.nbk;
-    const float *q = a.q + static_cast<size_t>(hk * a.group + g) * a.dk;
     float v[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int d = b * QK + 4 * lane + r;
-      v[r] = (d < a.dk) ? q[d] : 0.f;
-    }
-    apply_signs(v, a.cbk, lane);
-    wht128_warp(v, lane);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) qrot[g * dkp + b * QK + 4 * lane + r] = v[r] * f;
+    load_query_block(a, hk, wb, lane, v);
+    rotate_query_block(a, wb, lane, v, qrot);
   }
 }
 

@@ -118,19 +118,30 @@ __device__ __forceinline__ void v_sel(const uint8_t *qs_row, const uint8_t *sg_r
 template <int T, int NBK, int NBV>
 struct WarpStage {
   static constexpr uint32_t QSB = TypeTraits<T>::QSB, SGB = TypeTraits<T>::SGB;
-  static constexpr uint32_t BYTES0 = (WK * (NBK + NBV) * (QSB + SGB + 2) + 127) / 128 * 128;
-  // warps per CTA (one CTA per SM): 16 when three stages of every warp fit, else 8
+  static constexpr uint32_t KEYB = (NBK + NBV) * (QSB + SGB + 2);      // packed bytes per key (K and V)
+  static constexpr uint32_t BYTES0 = (WK * KEYB + 127) / 128 * 128;
+  // warps per CTA (one CTA per SM): 16 when three 32-key stages of every warp fit, else 8
   static constexpr int NW = (16 * 3 * BYTES0 <= 200 * 1024) ? 16 : 8;
   static constexpr int NT = NW * 32;
+  // P tiles, rotated q and the B columns (sized for a group of 4) beside the rings
+  static constexpr uint32_t EXTRA = NW * NBV * 8 * WK * 2 + 4 * 128 * NBK * 4 + 8 * 128 * NBK * 2;
+  static constexpr uint32_t BUDGET = 222 * 1024;
+  // A stage holds SUB groups of 32 keys (fewer, larger bulk copies: the copy count,
+  // not the bytes, limits how fast the copies are issued).  Two 64-key stages per
+  // warp where they fit, else 32-key stages, as many as fit (up to 4).
+  static constexpr uint32_t bytes_of(int keys) { return (keys * KEYB + 127) / 128 * 128; }
+  static constexpr int SUB = (NW * 2 * bytes_of(2 * WK) + EXTRA <= BUDGET) ? 2 : 1;
+  static constexpr int SK = SUB * WK;                                   // keys per stage
   static constexpr uint32_t KQS = 0;
-  static constexpr uint32_t KSG = KQS + WK * NBK * QSB;
-  static constexpr uint32_t KN = KSG + WK * NBK * SGB;
-  static constexpr uint32_t VQS = KN + WK * NBK * 2;
-  static constexpr uint32_t VSG = VQS + WK * NBV * QSB;
-  static constexpr uint32_t VN = VSG + WK * NBV * SGB;
-  static constexpr uint32_t BYTES = (VN + WK * NBV * 2 + 127) / 128 * 128;
-  static constexpr uint32_t TX = WK * (NBK + NBV) * (QSB + SGB + 2);
-  static constexpr int STAGES = (NW * 4 * BYTES <= 200 * 1024) ? 4 : (NW * 3 * BYTES <= 200 * 1024) ? 3 : 2;
+  static constexpr uint32_t KSG = KQS + SK * NBK * QSB;
+  static constexpr uint32_t KN = KSG + SK * NBK * SGB;
+  static constexpr uint32_t VQS = KN + SK * NBK * 2;
+  static constexpr uint32_t VSG = VQS + SK * NBV * QSB;
+  static constexpr uint32_t VN = VSG + SK * NBV * SGB;
+  static constexpr uint32_t BYTES = bytes_of(SK);
+  static constexpr int STAGES = (SUB == 2) ? 2
+                                : (NW * 4 * BYTES + EXTRA <= BUDGET) ? 4
+                                : (NW * 3 * BYTES + EXTRA <= BUDGET) ? 3 : 2;
   static constexpr uint32_t RING = STAGES * BYTES;                    // per warp
   static constexpr uint32_t PT = NW * RING;                           // P tiles [NW][NBV][8][WK] fp16
   static constexpr uint32_t QR = PT + NW * NBV * 8 * WK * 2;          // rotated q (floats)
@@ -153,6 +164,72 @@ __device__ __forceinline__ float fast_ex2(float x) {
   return y;
 }
 
+// Split merge inside a cluster (one cluster of n_splits CTAs per KV head): each
+// CTA's partial m[G], l[G], o'[G][128 NBV] sits at `cpart` in its own shared
+// memory.  Output block (head g, V block b) is merged by CTA rank (g NBV + b)
+// mod n_splits: thread t reads the n_splits partials of dim t over distributed
+// shared memory (one round trip), forms o' = sum_s o'_s 2^(m_s - M) / L,
+// then a warp rotates the block back (o = S H o' / sqrt(128)) and stores it.
+// `scratch` holds 128 floats of this CTA's shared memory.  The second cluster
+// barrier keeps every CTA's partial alive until all reads are done.
+template <int G, int NBV, int NT>
+__device__ void cluster_merge(const DecodeArgs &a, int hk, const float *cpart, float *scratch) {
+  constexpr int DVP = 128 * NBV, MAXS = 16;
+  const uint32_t rank = tc::cluster_rank();
+  const int ns = a.n_splits;                          // == cluster size, <= MAXS
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t base = tc::smem_u32(cpart);
+  tc::cluster_sync();
+  for (int wb = static_cast<int>(rank); wb < G * NBV; wb += ns) {
+    const int g = wb / NBV, b = wb % NBV;
+    const int t = threadIdx.x;
+    if (t < 128) {
+      float m[MAXS], l[MAXS], o[MAXS];
+#pragma unroll
+      for (int s = 0; s < MAXS; ++s) {
+        m[s] = -INFINITY;
+        l[s] = 0.f;
+        o[s] = 0.f;
+        if (s < ns) {
+          const uint32_t r = tc::dsmem_addr(base, static_cast<uint32_t>(s));
+          m[s] = tc::dsmem_ld(r + 4u * g);
+          l[s] = tc::dsmem_ld(r + 4u * (G + g));
+          o[s] = tc::dsmem_ld(r + 4u * (2 * G + g * DVP + b * 128 + t));
+        }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int s = 0; s < MAXS; ++s) M = fmaxf(M, m[s]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int s = 0; s < MAXS; ++s) {
+        const float w = (m[s] == -INFINITY) ? 0.f : fast_exp2(m[s] - M);
+        L = fmaf(w, l[s], L);
+        O = fmaf(w, o[s], O);
+      }
+      scratch[t] = (L > 0.f) ? O / L : 0.f;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float v[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) v[r] = scratch[4 * lane + r];
+      wht128_warp(v, lane);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) v[r] *= kInvSqrtQK;
+      apply_signs(v, a.cbv, lane);
+      float *out = a.out + static_cast<size_t>(hk * G + g) * a.dv;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int d = b * 128 + 4 * lane + r;
+        if (d < a.dv) out[d] = v[r];
+      }
+    }
+    __syncthreads();
+  }
+  tc::cluster_sync();
+}
+
 template <int T, int G, int NBK, int NBV>
 __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kernel(const DecodeArgs a) {
   static_assert(G == 1 || G == 2 || G == 4, "GQA group must be 1, 2 or 4");
@@ -170,11 +247,13 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   const int hk = blockIdx.y, split = blockIdx.x;
   const int64_t t0 = static_cast<int64_t>(split) * a.chunk;
   const int64_t t1 = min(a.kv_len, t0 + a.chunk);
-  // this warp's key range [w0, w1), a multiple of WK keys long except at t1
-  const int64_t per_warp = ((t1 - t0 + NW - 1) / NW + WK - 1) / WK * WK;
-  const int64_t w0 = t0 + warp * per_warp;
-  const int64_t w1 = min(t1, w0 + per_warp);
-  const int n_it = (w1 > w0) ? static_cast<int>((w1 - w0 + WK - 1) / WK) : 0;
+  // this warp's key range [w0, w1): the CTA's groups of WK keys dealt out evenly
+  // (warps differ by at most one group)
+  const int n_grp = (t1 > t0) ? static_cast<int>((t1 - t0 + WK - 1) / WK) : 0;
+  const int gb = warp * n_grp / NW, ge = (warp + 1) * n_grp / NW;
+  const int64_t w0 = t0 + static_cast<int64_t>(gb) * WK;
+  const int64_t w1 = min(t1, t0 + static_cast<int64_t>(ge) * WK);
+  const int n_it = ge - gb;
 
   unsigned char *ring = smem + warp * WS::RING;
   uint16_t *pw = reinterpret_cast<uint16_t *>(smem + WS::PT) + warp * NBV * 8 * WK;
@@ -187,31 +266,41 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   const uint8_t *vsg = SGB ? a.vsg + static_cast<size_t>(hk) * a.n_cells * NBV * SGB : nullptr;
   const uint16_t *vn = a.vn + static_cast<size_t>(hk) * a.n_cells * NBV;
 
-  // lane 0 of the warp: bring iteration `it` (keys w0 + 32 it ..) into its stage
-  auto issue = [&](int it) {
-    const int64_t key0 = w0 + static_cast<int64_t>(it) * WK;          // multiple of 32, key0 + 32 <= n_cells
-    unsigned char *st = ring + (it % STAGES) * WS::BYTES;
-    uint64_t *bar = &full[warp][it % STAGES];
-    tc::mbar_expect_tx(bar, WS::TX);
-    tc::bulk_g2s(st + WS::KQS, kqs + key0 * NBK * QSB, WK * NBK * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + WS::KSG, ksg + key0 * NBK * SGB, WK * NBK * SGB, bar);
-    tc::bulk_g2s(st + WS::KN, kn + key0 * NBK, WK * NBK * 2, bar);
-    tc::bulk_g2s(st + WS::VQS, vqs + key0 * NBV * QSB, WK * NBV * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + WS::VSG, vsg + key0 * NBV * SGB, WK * NBV * SGB, bar);
-    tc::bulk_g2s(st + WS::VN, vn + key0 * NBV, WK * NBV * 2, bar);
+  // lane 0 of the warp: bring stage si (groups SUB si .. of this warp, keys
+  // w0 + SK si ..) into ring slot si % STAGES; a last stage may hold fewer groups
+  const int n_st = (n_it + WS::SUB - 1) / WS::SUB;
+  auto issue = [&](int si) {
+    const int64_t key0 = w0 + static_cast<int64_t>(si) * WS::SK;      // multiple of 32
+    const int nk = min(WS::SUB, n_it - si * WS::SUB) * WK;              // key0 + nk <= n_cells
+    unsigned char *st = ring + (si % STAGES) * WS::BYTES;
+    uint64_t *bar = &full[warp][si % STAGES];
+    tc::mbar_expect_tx(bar, nk * WS::KEYB);
+    tc::bulk_g2s(st + WS::KQS, kqs + key0 * NBK * QSB, nk * NBK * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + WS::KSG, ksg + key0 * NBK * SGB, nk * NBK * SGB, bar);
+    tc::bulk_g2s(st + WS::KN, kn + key0 * NBK, nk * NBK * 2, bar);
+    tc::bulk_g2s(st + WS::VQS, vqs + key0 * NBV * QSB, nk * NBV * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + WS::VSG, vsg + key0 * NBV * SGB, nk * NBV * SGB, bar);
+    tc::bulk_g2s(st + WS::VN, vn + key0 * NBV, nk * NBV * 2, bar);
   };
 
+  // The query loads go out before any bulk copy: issued after them they would
+  // queue behind this CTA's ~200 KB of key/value traffic.  One query block per
+  // warp (NW >= G * NBK).
+  static_assert(NW >= G * NBK, "one query block per warp");
+  float qv[4] = {0.f, 0.f, 0.f, 0.f};
+  if (warp < G * NBK) load_query_block(a, hk, warp, lane, qv);
+  __syncthreads();
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) tc::mbar_init(&full[warp][s], 1);
     tc::mbar_init_fence();
     tc::fence_async_smem();
-    for (int i = 0; i < STAGES && i < n_it; ++i) issue(i);
+    if (n_st > 0) issue(0);          // the other stages once the prologue is done
   }
 
   // rotated queries (scale and log2(e) folded in) while the first tiles land, then
   // the score mma's B columns as binary16: n < G q'_hi, G <= n < 2G q'_lo, else 0
-  rotate_queries<NT>(a, hk, qrot);
+  if (warp < G * NBK) rotate_query_block(a, warp, lane, qv, qrot);
   for (int i = lane; i < NBV * 8 * WK; i += 32) pw[i] = 0;
   __syncthreads();
   uint16_t *qcol = reinterpret_cast<uint16_t *>(smem + WQ::QC);              // [8][128*NBK]
@@ -226,6 +315,8 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     qcol[i] = __half_as_ushort(__float2half_rn(x));
   }
   __syncthreads();
+  if (lane == 0)
+    for (int i = 1; i < STAGES && i < n_st; ++i) issue(i);
 
   const Tab tab_k{a.tabk[0], a.tabk[1], a.tabk[2], a.tabk[3]};
   const Tab tab_v{a.tabv[0], a.tabv[1], a.tabv[2], a.tabv[3]};
@@ -255,12 +346,17 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   bool timed_out = false;
 
   for (int it = 0; it < n_it; ++it) {
-    const bool ok = tc::mbar_wait(&full[warp][it % STAGES], (it / STAGES) & 1);
-    if (!__all_sync(0xffffffffu, ok)) { timed_out = true; break; }
-    const unsigned char *st = ring + (it % STAGES) * WS::BYTES;
+    const int si = it / WS::SUB, j = it % WS::SUB;             // stage, 32-key group inside it
+    if (j == 0) {
+      const bool ok = tc::mbar_wait(&full[warp][si % STAGES], (si / STAGES) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { timed_out = true; break; }
+    }
+    const unsigned char *st = ring + (si % STAGES) * WS::BYTES;
     const int64_t key0 = w0 + static_cast<int64_t>(it) * WK;
-    const uint16_t *knr = reinterpret_cast<const uint16_t *>(st + WS::KN);
-    const uint16_t *vnr = reinterpret_cast<const uint16_t *>(st + WS::VN);
+    const unsigned char *skq = st + WS::KQS + j * WK * NBK * QSB, *sks = st + WS::KSG + j * WK * NBK * SGB;
+    const unsigned char *svq = st + WS::VQS + j * WK * NBV * QSB, *svs = st + WS::VSG + j * WK * NBV * SGB;
+    const uint16_t *knr = reinterpret_cast<const uint16_t *>(st + WS::KN) + j * WK * NBK;
+    const uint16_t *vnr = reinterpret_cast<const uint16_t *>(st + WS::VN) + j * WK * NBV;
 
     // ---- scores S^T[key][n] for two groups of 16 keys (rows grp*16 + g, + 8)
     float s[2][4];
@@ -272,8 +368,8 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
 #pragma unroll
       for (int b = 0; b < NBK; ++b) {
         uint32_t ka0[16], ka1[16];
-        dq_chunk32<T>(st + WS::KQS + (r0 * NBK + b) * QSB, st + WS::KSG + (r0 * NBK + b) * SGB, c, tab_k, ka0);
-        dq_chunk32<T>(st + WS::KQS + (r1 * NBK + b) * QSB, st + WS::KSG + (r1 * NBK + b) * SGB, c, tab_k, ka1);
+        dq_chunk32<T>(skq + (r0 * NBK + b) * QSB, sks + (r0 * NBK + b) * SGB, c, tab_k, ka0);
+        dq_chunk32<T>(skq + (r1 * NBK + b) * QSB, sks + (r1 * NBK + b) * SGB, c, tab_k, ka1);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -379,7 +475,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
         const uint32_t pb0 = pt32[g * (WK / 2) + grp * 8 + c], pb1 = pt32[g * (WK / 2) + grp * 8 + c + 4];
         const int kr = grp * 16;
         uint32_t s00, s01, s10, s11, s20, s21, s30, s31;
-        const uint8_t *vq = st + WS::VQS, *vs = st + WS::VSG;
+        const uint8_t *vq = svq, *vs = svs;
         v_sel<T>(vq + ((kr + 2 * c) * NBV + b) * QSB, vs + ((kr + 2 * c) * NBV + b) * SGB, g, s00, s01);
         v_sel<T>(vq + ((kr + 2 * c + 1) * NBV + b) * QSB, vs + ((kr + 2 * c + 1) * NBV + b) * SGB, g, s10, s11);
         v_sel<T>(vq + ((kr + 2 * c + 8) * NBV + b) * QSB, vs + ((kr + 2 * c + 8) * NBV + b) * SGB, g, s20, s21);
@@ -393,7 +489,8 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
       }
     }
     __syncwarp();
-    if (lane == 0 && it + STAGES < n_it) issue(it + STAGES);      // this stage is free again
+    // the stage is free again after its last group
+    if (lane == 0 && (j == WS::SUB - 1 || it == n_it - 1) && si + STAGES < n_st) issue(si + STAGES);
   }
 
   // ---- per-warp results -> this warp's ring (all its copies have landed), CTA merge
@@ -442,6 +539,11 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     }
   }
   __syncthreads();
+  // CTA partial over the warps.  Launched as one cluster per KV head (cluster
+  // size == n_splits) the partial stays in this CTA's shared memory for the
+  // cluster merge; otherwise it goes to the workspace for the last-CTA merge.
+  const bool in_cluster = tc::cluster_size() == static_cast<uint32_t>(a.n_splits);
+  float *cpart = reinterpret_cast<float *>(smem + WS::PT);      // m[G], l[G], o'[G][DVP]
   for (int i = tid; i < G * DVP; i += NT) {
     const int h = i / DVP, d = i % DVP;
     float M = -INFINITY;
@@ -451,18 +553,27 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
       const float *wb = reinterpret_cast<const float *>(smem + w * WS::RING);
-      const float f = (wb[h] == -INFINITY) ? 0.f : exp2f(wb[h] - M);
+      const float f = (wb[h] == -INFINITY) ? 0.f : fast_exp2(wb[h] - M);
       o += f * wb[2 * G + h * DVP + d];
       l += f * wb[G + h];
     }
-    float *part = a.part + (static_cast<size_t>(hk * G + h) * a.n_splits + split) * a.part_stride;
-    part[2 + d] = o;
-    if (d == 0) {
-      part[0] = M;
-      part[1] = l;
+    if (in_cluster) {
+      cpart[2 * G + i] = o;
+      if (d == 0) {
+        cpart[h] = M;
+        cpart[G + h] = l;
+      }
+    } else {
+      float *part = a.part + (static_cast<size_t>(hk * G + h) * a.n_splits + split) * a.part_stride;
+      part[2 + d] = o;
+      if (d == 0) {
+        part[0] = M;
+        part[1] = l;
+      }
     }
   }
-  decode_merge<NT>(a, hk, reinterpret_cast<float *>(smem));
+  if (in_cluster) cluster_merge<G, NBV, NT>(a, hk, cpart, qrot);
+  else decode_merge<NT>(a, hk, reinterpret_cast<float *>(smem));
 }
 
 template <int T, int G, int NBK, int NBV>
@@ -473,12 +584,30 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
   static_assert(WarpStage<T, NBK, NBV>::RING >= 4 * (2 * G + G * 128 * NBV), "ring too small for the epilogue");
   static_assert(WarpStage<T, NBK, NBV>::NW * WarpStage<T, NBK, NBV>::RING >= 4 * (G * 128 * NBV + 2 * G * 256),
                 "merge region");
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<T, G, NBK, NBV>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  static_assert(WarpStage<T, NBK, NBV>::QR - WarpStage<T, NBK, NBV>::PT >= 4 * (2 * G + G * 128 * NBV),
+                "P-tile region too small for the CTA partial");
+  auto kern = decode_mma_kernel<T, G, NBK, NBV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.n_splits, a.n_kv_heads);
-  decode_mma_kernel<T, G, NBK, NBV><<<grid, WarpStage<T, NBK, NBV>::NT, bytes, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_splits, a.n_kv_heads);
+  cfg.blockDim = dim3(WarpStage<T, NBK, NBV>::NT);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  // one cluster per KV head, all resident together (else the last-CTA merge)
+  const int want = min(a.n_kv_heads, max(1, sm_count() / a.n_splits));
+  if (a.n_splits > 1 && cluster_merge_ok(reinterpret_cast<const void *>(kern), a.n_splits,
+                                         WarpStage<T, NBK, NBV>::NT, bytes, want)) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.n_splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 template <int T>

@@ -8,6 +8,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "tq_internal.h"
 
@@ -34,12 +35,58 @@ int sm_count() {
 
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Whether `kern` can run as clusters of `csize` CTAs (threads, smem each) with
+// at least `want` clusters resident at once.  Cached per device and kernel.
+bool cluster_merge_ok(const void *kern, int csize, int threads, size_t smem, int want) {
+  struct Entry {
+    int dev, csize, want;
+    const void *kern;
+    bool ok;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int n_cache = 0;
+  if (csize < 2 || csize > 16) return false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].dev == dev && cache[i].kern == kern && cache[i].csize == csize && cache[i].want == want)
+      return cache[i].ok;
+  bool ok = true;
+  if (csize > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    ok = false;
+  if (ok) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(csize, want);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    ok = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= want;
+  }
+  cudaGetLastError();
+  if (n_cache < 64) cache[n_cache++] = Entry{dev, csize, want, kern, ok};
+  return ok;
+}
+
 DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int64_t kv_len,
                                     int /*algo*/) {
   DecodeWorkspaceLayout L;
-  const int target_ctas = sm_count();           // one CTA per SM
+  // about one CTA per SM (with at most 16 splits per KV head the splits run as
+  // one thread-block cluster and merge on chip, see the decode kernels)
+  const int target_ctas = sm_count();
   int per_head = (target_ctas + n_kv_heads - 1) / n_kv_heads;
-  if (per_head > 256) per_head = 256;     // the merge stages <= 256 splits in shared memory
+  if (per_head > 256) per_head = 256;
   int64_t chunk = (kv_len + per_head - 1) / per_head;
   chunk = (chunk + 63) / 64 * 64;
   if (chunk < 128) chunk = 128;

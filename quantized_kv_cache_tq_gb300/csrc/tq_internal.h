@@ -97,6 +97,7 @@ struct DecodeWorkspaceLayout {
 constexpr size_t kWsHeader = 256;   // status word lives at offset 0
 
 int sm_count();
+bool cluster_merge_ok(const void *kern, int csize, int threads, size_t smem, int want);
 // prmt byte tables of a codebook's binary16 code values: t[0], t[1] low bytes of
 // codes 0..3 / 4..7, t[2], t[3] high bytes (turbo4: magnitudes 0..7).
 void code_byte_tables(const tq_codebook *cb, int type, uint32_t t[4]);

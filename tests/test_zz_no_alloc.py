@@ -51,10 +51,10 @@ def test_noalloc_matches_workspace_decode_twice():
 def test_noalloc_rejects_oversized_shape():
     import quantized_kv_cache_tq_gb300 as tq
     from quantized_kv_cache_tq_gb300 import _lib
-    # 128 query heads of width 256 over one KV head: the split partials exceed 4 MiB
+    # 512 query heads of width 256 over one KV head: the split partials exceed 4 MiB
     gk, gv = tq.TqCache(3, 1, 256, 1 << 16), tq.TqCache(3, 1, 256, 1 << 16)
     cb = tq.codebook(3, [1, 2, 3, 4])
-    need = _lib.tq_fattn_decode_workspace(gk.c, gv.c, 128, 1 << 16)
+    need = _lib.tq_fattn_decode_workspace(gk.c, gv.c, 512, 1 << 16)
     assert need > (4 << 20)
-    st = _lib.tq_fattn_decode_noalloc(gk.c, gv.c, cb, cb, 1 << 20, 128, 1 << 16, 0.1, 0, 1 << 20, None)
+    st = _lib.tq_fattn_decode_noalloc(gk.c, gv.c, cb, cb, 1 << 20, 512, 1 << 16, 0.1, 0, 1 << 20, None)
     assert st == _lib.TQ_ERR_WORKSPACE
