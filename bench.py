@@ -124,6 +124,31 @@ def barrier(world):
         dist.barrier()
 
 
+DECODE_SOURCES = ("tq_decode_mma.cuh", "tq_decode_mma_t3.cu", "tq_decode_mma.cu", "tq_decode_common.cuh",
+                  "tq_common.cuh", "tq_tc.cuh", "tq_internal.h", "tq_host.cu")
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_mma_32k_turbo3_ncu.md")
+
+
+def decode_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, or None when the
+    decode sources changed since that capture (hash of the sources recorded there)."""
+    import hashlib
+    import re
+    try:
+        text = open(DECODE_PROFILE).read()
+        h = hashlib.sha256()
+        for f in DECODE_SOURCES:
+            with open(os.path.join(ROOT, "quantized_kv_cache_tq_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    m_hash = re.search(r"decode_sources_sha256_16:\s*([0-9a-f]{16})", text)
+    if not (m_bytes and m_hash) or m_hash.group(1) != h.hexdigest()[:16]:
+        return None
+    return int(m_bytes.group(1))
+
+
 def per_cache_bytes(tq_type=3):
     per_block = {2: 34, 3: 50, 4: 66}[tq_type]
     return 2 * N_KV * KV_LEN * per_block
@@ -388,7 +413,7 @@ def run_tq(args):
                        "algo": args.algo, "l2": f"working set {B} caches x {cache_bytes / 1e6:.1f} MB > 4x L2 "
                                                  f"({l2 / 1e6:.0f} MB); no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None, "kernel": "decode",
+                         "frac": achieved / hbm_peak, "traffic": decode_traffic(), "kernel": "decode",
                          "kernel_us": dec_us, "bytes_per_launch": dec_bytes, "peak_source": peak_src},
             "e2e": {"value": calls * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
