@@ -5,7 +5,8 @@ Workload (decode at 32K context): 8 KV heads x 32 query heads (GQA 4), head_dim
 128, 32768 cells, turbo3 K and V.  One step = T new tokens (default 64) through
 B independent layers (B caches sized so the working set exceeds 4x L2); each
 token-layer quantises the token's K and V rows into its cache (SET_ROWS) and
-runs the single-query decode attention over the 32768 cells.  The metric is
+runs the single-query decode attention over the 32768 cells, both in one
+tq_fattn_decode_append launch.  The metric is
 decode-attention tokens per second for one layer (token-layer calls / s).
 
 Prints one JSON line.  --impl reference times the CPU oracle instead.
@@ -286,10 +287,11 @@ def run_tq(args):
 
     def token(decode_only=False):
         for b in range(B):
-            if not decode_only:
-                tq.set_rows(ks[b], cbk, newk[b], cell)
-                tq.set_rows(vs[b], cbv, newv[b], cell)
-            tq.fattn_decode(ks[b], vs[b], cbk, cbv, q_all[b], KV_LEN, scale, algo=algo, out=out[b], ws=ws)
+            if decode_only:
+                tq.fattn_decode(ks[b], vs[b], cbk, cbv, q_all[b], KV_LEN, scale, algo=algo, out=out[b], ws=ws)
+            else:   # SET_ROWS of the token's K and V rows + decode, one call
+                tq.fattn_decode_append(ks[b], vs[b], cbk, cbv, newk[b][0], newv[b][0], cell, q_all[b], KV_LEN,
+                                       scale, algo=algo, out=out[b], ws=ws)
 
     def capture(fn):
         s = torch.cuda.Stream(dev)
@@ -417,7 +419,7 @@ def run_tq(args):
                          "kernel_us": dec_us, "bytes_per_launch": dec_bytes, "peak_source": peak_src},
             "e2e": {"value": calls * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": 3 * calls,
+            "gpu_launches": calls * (1 if args.algo != "lut" else 3),
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

@@ -161,6 +161,31 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
                           float scale, int algo, float *out, void *workspace,
                           size_t workspace_bytes, tq_stream stream);
 
+/* SET_ROWS of one new token followed by decode, in one launch:
+ *   tq_set_rows(k, cbk, k_row, src_type, cell_id, 1, <workspace status>);
+ *   tq_set_rows(v, cbv, v_row, src_type, cell_id, 1, <workspace status>);
+ *   tq_fattn_decode(k, v, cbk, cbv, q, n_q_heads, kv_len, scale, algo, out, ...);
+ * with the same cache bytes and the same output as those three calls.  The
+ * pages run the two SET_ROWS ops and FLASH_ATTN_EXT as separate graph nodes
+ * ([TQ#36] "shuffle WHT", [HIP#28] "1. Graph-safe decode"); the tensor-core
+ * decode kernel quantises the token's rows itself (in the CTA whose key range
+ * holds the cell), writes them to the cache and attends the fresh codes, so
+ * a decode step costs one launch instead of three.  With the LUT kernel (or
+ * kv_len = 0) the three launches are issued in order instead.
+ * k_row    device, src_type [k->n_kv_heads][k->head_dim], 16-byte aligned
+ * v_row    device, src_type [v->n_kv_heads][v->head_dim], 16-byte aligned
+ * cell_id  device int64 [1], 8-byte aligned: the cell the token is written to;
+ *          it is attended when cell < kv_len.  A cell outside [0, n_cells)
+ *          writes nothing and stores TQ_ERR_DEVICE_CHECK in the workspace
+ *          status word (tq_workspace_status).
+ * Other arguments, results and errors as tq_fattn_decode; the workspace is the
+ * one tq_fattn_decode_workspace sizes. */
+tq_status tq_fattn_decode_append(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                                 const tq_codebook *cbv, const void *k_row, const void *v_row, int src_type,
+                                 const int64_t *cell_id, const float *q, int n_q_heads, int64_t kv_len,
+                                 float scale, int algo, float *out, void *workspace, size_t workspace_bytes,
+                                 tq_stream stream);
+
 /* tq_fattn_decode without a caller workspace, for callers that cannot
  * allocate device memory (code inside an allocator or memory-pool callback, a
  * runtime that has reserved all device memory up front, a plugin host that only

@@ -80,6 +80,27 @@ def fattn_decode(kc: TqCache, vc: TqCache, cbk, cbv, q, kv_len: int, scale: floa
     return out
 
 
+def fattn_decode_append(kc: TqCache, vc: TqCache, cbk, cbv, k_row, v_row, cell_id, q, kv_len: int,
+                        scale: float | None = None, algo: int = TQ_DECODE_AUTO, out=None, ws=None, stream=None):
+    """SET_ROWS of one token's K/V rows ([n_kv_heads][head_dim]) into cell ``cell_id``
+    (a device int64 tensor of one element), then decode over cells 0..kv_len-1."""
+    torch = _torch()
+    n_q = q.shape[0]
+    src_type = {torch.float32: TQ_F32, torch.float16: TQ_F16, torch.bfloat16: TQ_BF16}[k_row.dtype]
+    assert v_row.dtype == k_row.dtype and k_row.is_contiguous() and v_row.is_contiguous()
+    assert cell_id.dtype == torch.int64 and cell_id.numel() == 1
+    scale = 1.0 / math.sqrt(kc.head_dim) if scale is None else scale
+    if out is None:
+        out = torch.empty((n_q, vc.head_dim), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(_lib.tq_fattn_decode_workspace(kc.c, vc.c, n_q, kv_len), q.device)
+    st = _lib.tq_fattn_decode_append(kc.c, vc.c, cbk, cbv, k_row.data_ptr(), v_row.data_ptr(), src_type,
+                                     cell_id.data_ptr(), q.data_ptr(), n_q, kv_len, scale, algo,
+                                     out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
+    _lib.check("tq_fattn_decode_append", st)
+    return out
+
+
 def fattn_prefill(kc: TqCache, vc: TqCache, cbk, cbv, q, kv_len: int, scale: float | None = None,
                   causal: bool = True, out=None, ws=None, stream=None):
     torch = _torch()

@@ -31,6 +31,7 @@
 #pragma once
 
 #include "tq_decode_common.cuh"
+#include "tq_quant.cuh"
 #include "tq_tc.cuh"
 
 namespace tq {
@@ -289,6 +290,34 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   static_assert(NW >= G * NBK, "one query block per warp");
   float qv[4] = {0.f, 0.f, 0.f, 0.f};
   if (warp < G * NBK) load_query_block(a, hk, warp, lane, qv);
+
+  // ---- append ([TQ#36] SET_ROWS of the new token, fused): the CTA whose key
+  // range holds the cell (split 0 when the cell lies beyond kv_len) quantises the
+  // token's K and V row blocks of head hk with its last warp (4 lanes per block:
+  // K blocks first, then V), writes them to the cache and keeps a copy in
+  // `patch`; the warp that attends the cell copies it over its staged bytes.
+  constexpr int PQ = 0, PS = PQ + (NBK + NBV) * QSB, PN = PS + (NBK + NBV) * (SGB ? SGB : 4);
+  __shared__ __align__(16) uint8_t patch[PN + 2 * (NBK + NBV)];
+  // The row loads go out with the query loads in every CTA (the cell is not
+  // known yet); only the owner quantises, after the query rotation.
+  const bool append = a.cell_id != nullptr;
+  const int64_t cell = append ? __ldg(a.cell_id) : -1;
+  const int gq = lane >> 2, l4 = lane & 3;                  // block of the quantising warp's lane group
+  const bool qblk = gq < NBK + NBV;
+  float nv[8][4];
+  if (append && warp == NW - 1) {
+    const bool isk = gq < NBK;
+    const int b = isk ? gq : gq - NBK;
+    const int dim = isk ? a.dk : a.dv;
+    const void *src = isk ? a.k_src : a.v_src;
+    const int64_t base = static_cast<int64_t>(hk) * dim + b * QK;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e0 = 4 * l4 + 16 * i;
+      if (qblk) quant_load4_rt(a.src_type, src, base + e0, dim - b * QK - e0, nv[i]);
+      else nv[i][0] = nv[i][1] = nv[i][2] = nv[i][3] = 0.f;
+    }
+  }
   __syncthreads();
   if (lane == 0) {
 #pragma unroll
@@ -301,6 +330,24 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   // rotated queries (scale and log2(e) folded in) while the first tiles land, then
   // the score mma's B columns as binary16: n < G q'_hi, G <= n < 2G q'_lo, else 0
   if (warp < G * NBK) rotate_query_block(a, warp, lane, qv, qrot);
+  const bool cell_ok = cell >= 0 && cell < a.n_cells;
+  const bool owner = append && cell_ok && ((cell >= t0 && cell < t1) || (cell >= a.kv_len && split == 0));
+  if (append && !cell_ok && split == 0 && tid == 0) set_status(a.status, TQ_ERR_DEVICE_CHECK);
+  if (owner && warp == NW - 1) {
+    const bool isk = gq < NBK;
+    const int b = isk ? gq : gq - NBK, nb = isk ? NBK : NBV;
+    PackedShare<T> pb;
+    quantise_block4<T>(isk ? a.cbk : a.cbv, l4, nv, pb);
+    if (qblk) {
+      const int64_t blk = (static_cast<int64_t>(hk) * a.n_cells + cell) * nb + b;
+      uint16_t *gn = const_cast<uint16_t *>(isk ? a.kn : a.vn) + blk;
+      uint8_t *gqs = const_cast<uint8_t *>(isk ? a.kqs : a.vqs) + blk * QSB;
+      uint8_t *gsg = SGB ? const_cast<uint8_t *>(isk ? a.ksg : a.vsg) + blk * SGB : nullptr;
+      store_block4<T>(pb, l4, gn, gqs, gsg);
+      store_block4<T>(pb, l4, reinterpret_cast<uint16_t *>(patch + PN) + gq, patch + PQ + gq * QSB,
+                      SGB ? patch + PS + gq * SGB : nullptr);
+    }
+  }
   for (int i = lane; i < NBV * 8 * WK; i += 32) pw[i] = 0;
   __syncthreads();
   uint16_t *qcol = reinterpret_cast<uint16_t *>(smem + WQ::QC);              // [8][128*NBK]
@@ -353,6 +400,30 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     }
     const unsigned char *st = ring + (si % STAGES) * WS::BYTES;
     const int64_t key0 = w0 + static_cast<int64_t>(it) * WK;
+    if (j == 0 && owner && cell < w1 && cell >= w0 + static_cast<int64_t>(si) * WS::SK &&
+        cell < w0 + static_cast<int64_t>(si + 1) * WS::SK) {
+      // the appended cell is in this stage: its freshly quantised bytes replace
+      // whatever the bulk copy read
+      const int row = static_cast<int>(cell - (w0 + static_cast<int64_t>(si) * WS::SK));
+      unsigned char *sw = ring + (si % STAGES) * WS::BYTES;
+      constexpr int QW = QSB / 4, SW = SGB / 4;
+      for (int i = lane; i < (NBK + NBV) * (QW + SW + 1); i += 32) {
+        const int blk = i / (QW + SW + 1), e = i % (QW + SW + 1);
+        const bool isk = blk < NBK;
+        const int b = isk ? blk : blk - NBK, nb = isk ? NBK : NBV;
+        const uint32_t qso = isk ? WS::KQS : WS::VQS, sgo = isk ? WS::KSG : WS::VSG, no = isk ? WS::KN : WS::VN;
+        if (e < QW) {
+          reinterpret_cast<uint32_t *>(sw + qso + (row * nb + b) * QSB)[e] =
+              reinterpret_cast<const uint32_t *>(patch + PQ + blk * QSB)[e];
+        } else if (e < QW + SW) {
+          reinterpret_cast<uint32_t *>(sw + sgo + (row * nb + b) * SGB)[e - QW] =
+              reinterpret_cast<const uint32_t *>(patch + PS + blk * SGB)[e - QW];
+        } else {
+          reinterpret_cast<uint16_t *>(sw + no)[row * nb + b] = reinterpret_cast<const uint16_t *>(patch + PN)[blk];
+        }
+      }
+      __syncwarp();
+    }
     const unsigned char *skq = st + WS::KQS + j * WK * NBK * QSB, *sks = st + WS::KSG + j * WK * NBK * SGB;
     const unsigned char *svq = st + WS::VQS + j * WK * NBV * QSB, *svs = st + WS::VSG + j * WK * NBV * SGB;
     const uint16_t *knr = reinterpret_cast<const uint16_t *>(st + WS::KN) + j * WK * NBK;

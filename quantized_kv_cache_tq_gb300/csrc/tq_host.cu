@@ -341,29 +341,51 @@ size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_h
   return decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, TQ_DECODE_AUTO).total;
 }
 
-tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
-                          const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
-                          float scale, int algo, float *out, void *workspace,
-                          size_t workspace_bytes, tq_stream stream) {
+// Decode, optionally with the new token's rows appended first (k_row != null):
+// fused into the tensor-core kernel, else as two SET_ROWS launches before it.
+static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk, const tq_codebook *cbv,
+                             const void *k_row, const void *v_row, int src_type, const int64_t *cell_id,
+                             const float *q, int n_q_heads, int64_t kv_len, float scale, int algo, float *out,
+                             void *workspace, size_t workspace_bytes, tq_stream stream) {
   tq_status st = check_kv_pair(k, v, n_q_heads, kv_len);
   if (st != TQ_OK) return st;
   if (!codebook_ok(cbk, k->type) || !codebook_ok(cbv, v->type)) return TQ_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out) || !isfinite(scale)) return TQ_ERR_INVALID_ARG;
   if (algo != TQ_DECODE_AUTO && algo != TQ_DECODE_LUT && algo != TQ_DECODE_MMA)
     return TQ_ERR_INVALID_ARG;
+  const bool append = k_row != nullptr;
+  if (append) {
+    if (src_type != TQ_F32 && src_type != TQ_F16 && src_type != TQ_BF16) return TQ_ERR_INVALID_ARG;
+    if (!v_row || !aligned16(k_row) || !aligned16(v_row) || !cell_id ||
+        (reinterpret_cast<uintptr_t>(cell_id) & 7u))
+      return TQ_ERR_INVALID_ARG;
+  }
   const int group = n_q_heads / k->n_kv_heads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (kv_len == 0)
+  const bool ws_ok = workspace && !(reinterpret_cast<uintptr_t>(workspace) & 255u);
+  int32_t *status = ws_ok ? static_cast<int32_t *>(workspace) : nullptr;
+  if (kv_len == 0) {             // nothing to attend: append only, zero output
+    if (append) {
+      st = tq_set_rows(k, cbk, k_row, src_type, cell_id, 1, status, stream);
+      if (st != TQ_OK) return st;
+      st = tq_set_rows(v, cbv, v_row, src_type, cell_id, 1, status, stream);
+      if (st != TQ_OK) return st;
+    }
     return map_cuda(cudaMemsetAsync(out, 0, sizeof(float) * n_q_heads * v->head_dim, s));
+  }
   const bool mma_ok = decode_mma_supported(k->type, v->type, group, k->n_blocks, v->n_blocks);
   const bool lut_ok = group <= 8 && k->n_blocks <= 2 && v->n_blocks <= 2;
   int use = algo;
   if (use == TQ_DECODE_AUTO) use = mma_ok ? TQ_DECODE_MMA : TQ_DECODE_LUT;
-  if ((use == TQ_DECODE_MMA && !mma_ok) || (use == TQ_DECODE_LUT && !lut_ok))
-    return TQ_ERR_UNSUPPORTED;
+  if ((use == TQ_DECODE_MMA && !mma_ok) || (use == TQ_DECODE_LUT && !lut_ok)) return TQ_ERR_UNSUPPORTED;
   const DecodeWorkspaceLayout L = decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, use);
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TQ_ERR_WORKSPACE;
-  if (workspace_bytes < L.total) return TQ_ERR_WORKSPACE;
+  if (!ws_ok || workspace_bytes < L.total) return TQ_ERR_WORKSPACE;
+  if (append && use != TQ_DECODE_MMA) {      // the LUT kernel: SET_ROWS launches first
+    st = tq_set_rows(k, cbk, k_row, src_type, cell_id, 1, status, stream);
+    if (st != TQ_OK) return st;
+    st = tq_set_rows(v, cbv, v_row, src_type, cell_id, 1, status, stream);
+    if (st != TQ_OK) return st;
+  }
 
   DecodeArgs a;
   memset(&a, 0, sizeof(a));
@@ -377,7 +399,7 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
   a.out = out;
   a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.part_off);
   a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.counters_off);
-  a.status = static_cast<int32_t *>(workspace);
+  a.status = status;
   a.n_cells = k->n_cells;
   a.kv_len = kv_len;
   a.chunk = L.chunk;
@@ -394,9 +416,33 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
   a.cbv = to_dev(cbv);
   code_byte_tables(cbk, k->type, a.tabk);
   code_byte_tables(cbv, v->type, a.tabv);
+  if (append && use == TQ_DECODE_MMA) {
+    a.k_src = k_row;
+    a.v_src = v_row;
+    a.cell_id = cell_id;
+    a.src_type = src_type;
+  }
   cudaError_t e = (use == TQ_DECODE_MMA) ? launch_decode_mma(k->type, v->type, a, s)
                                          : launch_decode_lut(k->type, v->type, a, s);
   return map_cuda(e);
+}
+
+tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                          const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
+                          float scale, int algo, float *out, void *workspace,
+                          size_t workspace_bytes, tq_stream stream) {
+  return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, q, n_q_heads, kv_len, scale, algo, out,
+                     workspace, workspace_bytes, stream);
+}
+
+tq_status tq_fattn_decode_append(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                                 const tq_codebook *cbv, const void *k_row, const void *v_row, int src_type,
+                                 const int64_t *cell_id, const float *q, int n_q_heads, int64_t kv_len,
+                                 float scale, int algo, float *out, void *workspace, size_t workspace_bytes,
+                                 tq_stream stream) {
+  if (!k_row) return TQ_ERR_INVALID_ARG;
+  return decode_call(k, v, cbk, cbv, k_row, v_row, src_type, cell_id, q, n_q_heads, kv_len, scale, algo, out,
+                     workspace, workspace_bytes, stream);
 }
 
 size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads,

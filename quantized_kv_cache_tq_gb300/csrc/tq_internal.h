@@ -58,6 +58,12 @@ struct DecodeArgs {
   float scale_log2;       // softmax scale * log2(e)
   DevCodebook cbk, cbv;
   uint32_t tabk[4], tabv[4];   // binary16 byte tables of the code values (see code_byte_tables)
+  // append: the new token's K / V rows ([n_kv_heads][dk], [n_kv_heads][dv] of
+  // src_type) are quantised into cell *cell_id before it is attended; null = none
+  const void *k_src;
+  const void *v_src;
+  const int64_t *cell_id;
+  int32_t src_type;
 };
 
 struct PrefillArgs {

@@ -1,0 +1,216 @@
+// Quantisation of one 128-element block by four lanes: the SET_ROWS arithmetic
+// ([TQ#36] "shuffle WHT": block norm, sign-randomised Walsh-Hadamard rotation
+// with butterfly stages h = 1..64, nearest-centroid codes), shared by the
+// SET_ROWS kernel and the decode kernel's append path so both write identical
+// bytes.
+//
+// Four lanes own a block, 32 elements each: lane l4 holds elements
+// 4*l4 + 16*i + r (i = 0..7, r = 0..3), read as eight coalesced 16-byte loads,
+// so five of the seven butterfly stages (h = 1, 2, 16, 32, 64) stay inside a lane
+// and only h = 4, 8 are lane shuffles: no shared memory and no barrier.
+//
+// The normalisation by the block norm is folded into the decision thresholds:
+// with y = v / (|x| sqrt(128)) (v the unnormalised transform), y >= t becomes
+// v >= t |x| sqrt(128), one multiply per threshold and block instead of one per
+// element.  Codes are sign-magnitude: s = (y >= 0), j = #{positive thresholds
+// <= |y|}.  An exact tie goes to the higher centroid.
+#pragma once
+
+#include "tq_common.cuh"
+
+namespace tq {
+
+// Four source elements at `off` (fewer when `valid` < 4; the rest read as 0).
+template <int SRC>
+__device__ __forceinline__ void quant_load4(const void *base, int64_t off, int valid, float v[4]) {
+  if (SRC == TQ_F32) {
+    const float *p = static_cast<const float *>(base) + off;
+    if (valid >= 4) {
+      const float4 x = __ldcs(reinterpret_cast<const float4 *>(p));
+      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) v[r] = (r < valid) ? p[r] : 0.f;
+    }
+  } else {
+    const uint16_t *p = static_cast<const uint16_t *>(base) + off;
+    uint16_t h[4] = {0, 0, 0, 0};
+    if (valid >= 4) {
+      const uint2 x = __ldcs(reinterpret_cast<const uint2 *>(p));
+      h[0] = x.x & 0xffff; h[1] = x.x >> 16; h[2] = x.y & 0xffff; h[3] = x.y >> 16;
+    } else {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) h[r] = (r < valid) ? p[r] : 0;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      if (SRC == TQ_F16) v[r] = __half2float(__ushort_as_half(h[r]));
+      else v[r] = __bfloat162float(__ushort_as_bfloat16(h[r]));
+    }
+  }
+}
+
+// The same with the source type chosen at run time.
+__device__ __forceinline__ void quant_load4_rt(int src_type, const void *base, int64_t off, int valid, float v[4]) {
+  if (src_type == TQ_F32) quant_load4<TQ_F32>(base, off, valid, v);
+  else if (src_type == TQ_F16) quant_load4<TQ_F16>(base, off, valid, v);
+  else quant_load4<TQ_BF16>(base, off, valid, v);
+}
+
+__device__ __forceinline__ uint32_t pick4(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, int i) {
+  return i == 0 ? x0 : i == 1 ? x1 : i == 2 ? x2 : x3;
+}
+
+// bit position of element 16w + ip inside qs word w (turbo2/3)
+__device__ __forceinline__ int qs2_bit(int ip) { return ip < 8 ? 4 * ip : 4 * (ip - 8) + 2; }
+// bit position of element 32u + rr inside signs word u (turbo3)
+__device__ __forceinline__ int sg_bit(int rr) {
+  return rr < 16 ? 4 * (rr & 7) + 2 + (rr >> 3) : 4 * ((rr - 16) & 7) + ((rr - 16) >> 3);
+}
+
+// One lane's share of a packed block: the norm (binary16 bits), qs words
+// (turbo2/3: words 2 l4 and 2 l4 + 1 in w[0], w[1]; turbo4: words 2 i + l4/2 in
+// w[i], stored by the even lanes) and, for turbo3, signs word l4.
+template <int TYPE>
+struct PackedShare {
+  uint32_t norm;
+  uint32_t w[8];
+  uint32_t sg;
+};
+
+// Quantise the block whose 32 elements per lane are in v (modified).  All 32
+// lanes of the warp must call it (it shuffles within groups of four lanes).
+template <int TYPE>
+__device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, float v[8][4], PackedShare<TYPE> &out) {
+  constexpr int NC = TypeTraits<TYPE>::NC;
+  constexpr int HALF = NC / 2;
+
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t w = cb.sign_bits[i >> 1];
+      const float sgn = ((w >> (16 * (i & 1) + 4 * l4 + r)) & 1u) ? -1.f : 1.f;
+      ss = fmaf(v[i][r], v[i][r], ss);
+      v[i][r] *= sgn;
+    }
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+
+  // butterflies inside the lane: h = 1, 2 (r bits) and h = 16, 32, 64 (i bits)
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a0 = v[i][0] + v[i][1], a1 = v[i][0] - v[i][1];
+    const float a2 = v[i][2] + v[i][3], a3 = v[i][2] - v[i][3];
+    v[i][0] = a0 + a2; v[i][2] = a0 - a2; v[i][1] = a1 + a3; v[i][3] = a1 - a3;
+  }
+#pragma unroll
+  for (int hb = 1; hb < 8; hb <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (!(i & hb))
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float x = v[i][r], y = v[i | hb][r];
+          v[i][r] = x + y;
+          v[i | hb][r] = x - y;
+        }
+  // across the 4 lanes: h = 4 (lane ^ 1), h = 8 (lane ^ 2); element j takes
+  // o = x[j ^ h] and becomes (j & h) ? o - x[j] : x[j] + o
+#pragma unroll
+  for (int m = 1; m < 4; m <<= 1) {
+    const float sg = (l4 & m) ? -1.f : 1.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[i][r], m);
+        v[i][r] = fmaf(sg, v[i][r], o);
+      }
+  }
+
+  // thresholds between positive centroids, scaled to the unnormalised domain
+  const float nrm_scale = sqrtf(ss * 128.f);
+  float thr[HALF - 1];
+#pragma unroll
+  for (int k = 0; k < HALF - 1; ++k)
+    thr[k] = ss > 0.f ? 0.5f * (cb.c[HALF + k] + cb.c[HALF + k + 1]) * nrm_scale : INFINITY;
+
+  uint32_t code[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float y = v[i][r], ay = fabsf(y);
+      uint32_t j = 0;
+#pragma unroll
+      for (int k = 0; k < HALF - 1; ++k) j += (ay >= thr[k]) ? 1u : 0u;
+      code[i][r] = (y >= 0.f) ? (HALF + j) : j;
+    }
+
+  out.norm = __half_as_ushort(__float2half_rn(sqrtf(ss)));
+  out.sg = 0;
+  if (TYPE == 4) {
+    // word w = 2i + l4/2, element nibble 4*(l4 & 1) + r; lanes l4 and l4^1 share a word
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) x |= code[i][r] << (4 * (4 * (l4 & 1) + r));
+      out.w[i] = x | __shfl_xor_sync(0xffffffffu, x, 1);
+    }
+  } else {
+    // qs word i holds elements 16i .. 16i+15; this lane's are 16i + 4*l4 + r
+    uint32_t wq[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t f = (TYPE == 3) ? (code[i][r] & 3u) : code[i][r];
+        x |= f << qs2_bit(4 * l4 + r);
+      }
+      x |= __shfl_xor_sync(0xffffffffu, x, 1);
+      x |= __shfl_xor_sync(0xffffffffu, x, 2);
+      wq[i] = x;
+    }
+    out.w[0] = pick4(wq[0], wq[2], wq[4], wq[6], l4);
+    out.w[1] = pick4(wq[1], wq[3], wq[5], wq[7], l4);
+    if (TYPE == 3) {
+      uint32_t ws[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        uint32_t x = 0;
+#pragma unroll
+        for (int ih = 0; ih < 2; ++ih)
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            x |= (code[2 * u + ih][r] >> 2) << sg_bit(16 * ih + 4 * l4 + r);
+        x |= __shfl_xor_sync(0xffffffffu, x, 1);
+        x |= __shfl_xor_sync(0xffffffffu, x, 2);
+        ws[u] = x;
+      }
+      out.sg = pick4(ws[0], ws[1], ws[2], ws[3], l4);
+    }
+  }
+}
+
+// Store a lane's share of a packed block (global or shared memory; qs 16-byte
+// aligned, signs 4-byte aligned).
+template <int TYPE>
+__device__ __forceinline__ void store_block4(const PackedShare<TYPE> &pb, int l4, uint16_t *norm, uint8_t *qs,
+                                             uint8_t *signs) {
+  if (l4 == 0) *norm = static_cast<uint16_t>(pb.norm);
+  if (TYPE == 4) {
+    if ((l4 & 1) == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t *>(qs)[2 * i + (l4 >> 1)] = pb.w[i];
+    }
+  } else {
+    reinterpret_cast<uint2 *>(qs)[l4] = make_uint2(pb.w[0], pb.w[1]);
+    if (TYPE == 3) reinterpret_cast<uint32_t *>(signs)[l4] = pb.sg;
+  }
+}
+
+}  // namespace tq
