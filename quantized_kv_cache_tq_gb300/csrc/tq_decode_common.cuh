@@ -25,9 +25,9 @@ __host__ __device__ inline int merge_smem_floats(int group, int nbv, int n_split
 //   o = S H o' / sqrt(128)   (R^T for R = H S / sqrt(128)),
 // writes out[h][0 .. dv) and resets the counter so the next launch (or graph
 // replay) finds it at zero.  No CTA ever waits for another one.
-// Each warp merges 32 consecutive outputs of one head, 16 splits at a time:
-// lane s < 16 holds split s's maximum and sum, every lane loads its output's
-// values of the 16 splits at once (one L2 round trip per 16 splits).
+// Each warp merges 32 consecutive outputs of one head, 24 splits at a time:
+// lane s < 24 holds split s's maximum and sum, every lane loads its output's
+// values of the 24 splits at once (one L2 round trip per 24 splits).
 // `smem` must hold merge_smem_floats(group, nbv, n_splits) floats.
 template <int NT>
 __device__ void decode_merge(const DecodeArgs &a, int hk, float *smem) {
@@ -49,26 +49,29 @@ __device__ void decode_merge(const DecodeArgs &a, int hk, float *smem) {
   const int stride = a.part_stride;
   float *orot = smem;                     // [G][dvp]
   const float *base = a.part + static_cast<size_t>(hk) * G * ns * stride;
+  const float *base_ml = a.part_ml + static_cast<size_t>(hk) * G * ns * 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i0 = warp * 32; i0 < G * dvp; i0 += NT) {     // dvp is a multiple of 32: one head per warp pass
     const int i = i0 + lane, g = i / dvp, d = i % dvp;
     const float *p = base + static_cast<size_t>(g) * ns * stride;
+    const float *pml = base_ml + static_cast<size_t>(g) * ns * 2;
     float M = -INFINITY, L = 0.f, o = 0.f;
-    for (int s0 = 0; s0 < ns; s0 += 16) {
-      const int n = min(16, ns - s0);
+    for (int s0 = 0; s0 < ns; s0 += 24) {
+      const int n = min(24, ns - s0);
       const float *ps = p + static_cast<size_t>(s0) * stride;
-      const float ms = (lane < n) ? __ldcg(ps + static_cast<size_t>(lane) * stride) : -INFINITY;
-      const float ls = (lane < n) ? __ldcg(ps + static_cast<size_t>(lane) * stride + 1) : 0.f;
-      float ov[16];
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (lane < n) ml = __ldcg(reinterpret_cast<const float2 *>(pml) + s0 + lane);
+      const float ms = ml.x, ls = ml.y;
+      float ov[24];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) ov[j] = (j < n) ? __ldcg(ps + static_cast<size_t>(j) * stride + 2 + d) : 0.f;
+      for (int j = 0; j < 24; ++j) ov[j] = (j < n) ? __ldcg(ps + static_cast<size_t>(j) * stride + d) : 0.f;
       const float Mn = fmaxf(M, warp_max(ms));
       const float f = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
       const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - Mn);
       L = L * f + warp_sum(w * ls);
       o *= f;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) o = fmaf(__shfl_sync(0xffffffffu, w, j), ov[j], o);
+      for (int j = 0; j < 24; ++j) o = fmaf(__shfl_sync(0xffffffffu, w, j), ov[j], o);
       M = Mn;
     }
     orot[i] = (L > 0.f) ? o / L : 0.f;

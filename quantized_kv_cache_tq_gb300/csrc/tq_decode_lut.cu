@@ -210,9 +210,9 @@ __global__ void __launch_bounds__(kThreads) decode_lut_kernel(const DecodeArgs a
   }
   if (kr == 0) {
     for (int g = 0; g < G; ++g) {
-      float *p = a.part + (static_cast<size_t>(hk * G + g) * a.n_splits + split) * a.part_stride;
-      p[2 + d] = acc[g];
-      if (d == 0) { p[0] = m_run[g]; p[1] = l_run[g]; }
+      const size_t ps = static_cast<size_t>(hk * G + g) * a.n_splits + split;
+      a.part[ps * a.part_stride + d] = acc[g];
+      if (d == 0) { a.part_ml[2 * ps] = m_run[g]; a.part_ml[2 * ps + 1] = l_run[g]; }
     }
   }
   decode_merge<kThreads>(a, hk, lut);

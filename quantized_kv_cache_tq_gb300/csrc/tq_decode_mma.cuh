@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   constexpr int DVP = 128 * NBV;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[NW][STAGES];
+  __shared__ __align__(8) uint64_t first_b[NW];      // group 1 of stage 0 (64-key stages)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -267,21 +268,25 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   const uint8_t *vsg = SGB ? a.vsg + static_cast<size_t>(hk) * a.n_cells * NBV * SGB : nullptr;
   const uint16_t *vn = a.vn + static_cast<size_t>(hk) * a.n_cells * NBV;
 
-  // lane 0 of the warp: bring stage si (groups SUB si .. of this warp, keys
-  // w0 + SK si ..) into ring slot si % STAGES; a last stage may hold fewer groups
+  // lane 0 of the warp: bring groups [jg, jg + ng) of stage si (groups SUB si .. of
+  // this warp, keys w0 + SK si + 32 jg ..) into ring slot si % STAGES, completing
+  // on `bar`; a last stage may hold fewer groups
   const int n_st = (n_it + WS::SUB - 1) / WS::SUB;
-  auto issue = [&](int si) {
-    const int64_t key0 = w0 + static_cast<int64_t>(si) * WS::SK;      // multiple of 32
-    const int nk = min(WS::SUB, n_it - si * WS::SUB) * WK;              // key0 + nk <= n_cells
+  auto issue_part = [&](int si, int jg, int ng, uint64_t *bar) {
+    const int64_t key0 = w0 + static_cast<int64_t>(si) * WS::SK + jg * WK;   // multiple of 32
+    const int nk = ng * WK;                                                   // key0 + nk <= n_cells
     unsigned char *st = ring + (si % STAGES) * WS::BYTES;
-    uint64_t *bar = &full[warp][si % STAGES];
+    const int r0 = jg * WK;
     tc::mbar_expect_tx(bar, nk * WS::KEYB);
-    tc::bulk_g2s(st + WS::KQS, kqs + key0 * NBK * QSB, nk * NBK * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + WS::KSG, ksg + key0 * NBK * SGB, nk * NBK * SGB, bar);
-    tc::bulk_g2s(st + WS::KN, kn + key0 * NBK, nk * NBK * 2, bar);
-    tc::bulk_g2s(st + WS::VQS, vqs + key0 * NBV * QSB, nk * NBV * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + WS::VSG, vsg + key0 * NBV * SGB, nk * NBV * SGB, bar);
-    tc::bulk_g2s(st + WS::VN, vn + key0 * NBV, nk * NBV * 2, bar);
+    tc::bulk_g2s(st + WS::KQS + r0 * NBK * QSB, kqs + key0 * NBK * QSB, nk * NBK * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + WS::KSG + r0 * NBK * SGB, ksg + key0 * NBK * SGB, nk * NBK * SGB, bar);
+    tc::bulk_g2s(st + WS::KN + r0 * NBK * 2, kn + key0 * NBK, nk * NBK * 2, bar);
+    tc::bulk_g2s(st + WS::VQS + r0 * NBV * QSB, vqs + key0 * NBV * QSB, nk * NBV * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + WS::VSG + r0 * NBV * SGB, vsg + key0 * NBV * SGB, nk * NBV * SGB, bar);
+    tc::bulk_g2s(st + WS::VN + r0 * NBV * 2, vn + key0 * NBV, nk * NBV * 2, bar);
+  };
+  auto issue = [&](int si) {
+    issue_part(si, 0, min(WS::SUB, n_it - si * WS::SUB), &full[warp][si % STAGES]);
   };
 
   // The query loads go out before any bulk copy: issued after them they would
@@ -322,9 +327,17 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) tc::mbar_init(&full[warp][s], 1);
+    tc::mbar_init(&first_b[warp], 1);
     tc::mbar_init_fence();
     tc::fence_async_smem();
-    if (n_st > 0) issue(0);          // the other stages once the prologue is done
+    // The first group alone goes first: every CTA's first 32 keys are in the
+    // first wave of HBM traffic, so the compute starts as early as it can.
+    // With 64-key stages the second group follows after the prologue on its own
+    // barrier; the other stages once the first has landed.
+    if (n_st > 0) {
+      if (WS::SUB == 2) issue_part(0, 0, 1, &full[warp][0]);
+      else issue(0);
+    }
   }
 
   // rotated queries (scale and log2(e) folded in) while the first tiles land, then
@@ -362,8 +375,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     qcol[i] = __half_as_ushort(__float2half_rn(x));
   }
   __syncthreads();
-  if (lane == 0)
-    for (int i = 1; i < STAGES && i < n_st; ++i) issue(i);
+  if (WS::SUB == 2 && lane == 0 && n_it > 1) issue_part(0, 1, 1, &first_b[warp]);
 
   const Tab tab_k{a.tabk[0], a.tabk[1], a.tabk[2], a.tabk[3]};
   const Tab tab_v{a.tabv[0], a.tabv[1], a.tabv[2], a.tabv[3]};
@@ -394,17 +406,21 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
 
   for (int it = 0; it < n_it; ++it) {
     const int si = it / WS::SUB, j = it % WS::SUB;             // stage, 32-key group inside it
-    if (j == 0) {
-      const bool ok = tc::mbar_wait(&full[warp][si % STAGES], (si / STAGES) & 1);
+    if (j == 0 || (WS::SUB == 2 && it == 1)) {
+      const bool ok = (it == 1 && WS::SUB == 2) ? tc::mbar_wait(&first_b[warp], 0)
+                                                : tc::mbar_wait(&full[warp][si % STAGES], (si / STAGES) & 1);
       if (!__all_sync(0xffffffffu, ok)) { timed_out = true; break; }
+      // the other stages only once the first has landed: issued earlier, every
+      // CTA's later stages compete with the other CTAs' first stages for HBM
+      if (it == 0 && lane == 0)
+        for (int i = 1; i < STAGES && i < n_st; ++i) issue(i);
     }
     const unsigned char *st = ring + (si % STAGES) * WS::BYTES;
     const int64_t key0 = w0 + static_cast<int64_t>(it) * WK;
-    if (j == 0 && owner && cell < w1 && cell >= w0 + static_cast<int64_t>(si) * WS::SK &&
-        cell < w0 + static_cast<int64_t>(si + 1) * WS::SK) {
-      // the appended cell is in this stage: its freshly quantised bytes replace
-      // whatever the bulk copy read
-      const int row = static_cast<int>(cell - (w0 + static_cast<int64_t>(si) * WS::SK));
+    if (owner && cell >= key0 && cell < key0 + WK && cell < w1) {
+      // the appended cell is in this group (landed): its freshly quantised bytes
+      // replace whatever the bulk copy read
+      const int row = static_cast<int>(cell - key0) + j * WK;                 // row inside the stage
       unsigned char *sw = ring + (si % STAGES) * WS::BYTES;
       constexpr int QW = QSB / 4, SW = SGB / 4;
       for (int i = lane; i < (NBK + NBV) * (QW + SW + 1); i += 32) {
@@ -635,12 +651,9 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
         cpart[G + h] = l;
       }
     } else {
-      float *part = a.part + (static_cast<size_t>(hk * G + h) * a.n_splits + split) * a.part_stride;
-      part[2 + d] = o;
-      if (d == 0) {
-        part[0] = M;
-        part[1] = l;
-      }
+      const size_t ps = static_cast<size_t>(hk * G + h) * a.n_splits + split;
+      a.part[ps * a.part_stride + d] = o;
+      if (d == 0) *reinterpret_cast<float2 *>(a.part_ml + 2 * ps) = make_float2(M, l);
     }
   }
   if (in_cluster) cluster_merge<G, NBV, NT>(a, hk, cpart, qrot);

@@ -93,9 +93,9 @@ DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int6
   L.chunk = chunk;
   L.n_splits = kv_len > 0 ? static_cast<int>((kv_len + chunk - 1) / chunk) : 1;
   L.counters_off = kWsHeader;
-  L.part_off = L.counters_off + round_up(sizeof(int32_t) * n_kv_heads, 256);
-  const size_t stride = 2 + 128 * static_cast<size_t>(nbv);
-  L.total = L.part_off + round_up(sizeof(float) * n_q_heads * L.n_splits * stride, 256);
+  L.ml_off = L.counters_off + round_up(sizeof(int32_t) * n_kv_heads, 256);
+  L.part_off = L.ml_off + round_up(sizeof(float) * 2 * n_q_heads * L.n_splits, 256);
+  L.total = L.part_off + round_up(sizeof(float) * n_q_heads * L.n_splits * 128 * static_cast<size_t>(nbv), 256);
   return L;
 }
 
@@ -398,6 +398,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.q = q;
   a.out = out;
   a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.part_off);
+  a.part_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.ml_off);
   a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.counters_off);
   a.status = status;
   a.n_cells = k->n_cells;
@@ -410,7 +411,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.dv = v->head_dim;
   a.nbk = k->n_blocks;
   a.nbv = v->n_blocks;
-  a.part_stride = 2 + 128 * v->n_blocks;
+  a.part_stride = 128 * v->n_blocks;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.cbk = to_dev(cbk);
   a.cbv = to_dev(cbv);

@@ -32,8 +32,8 @@ struct SetRowsArgs {
 };
 
 // Everything a decode kernel needs; the partial results of split s of query
-// head h live at part + (h * n_splits + s) * part_stride as
-// [m (log2 domain), l, o'[0 .. 128*nbv)] (o' unnormalised, rotated domain).
+// head h are m (log2 domain), l at part_ml + 2 (h * n_splits + s) and
+// o'[0 .. 128 nbv) (unnormalised, rotated domain) at part + (h * n_splits + s) * part_stride.
 struct DecodeArgs {
   const uint16_t *kn;
   const uint8_t *kqs;
@@ -43,7 +43,8 @@ struct DecodeArgs {
   const uint8_t *vsg;
   const float *q;
   float *out;
-  float *part;
+  float *part;            // split outputs o'[h][split][part_stride]
+  float *part_ml;         // split maxima and sums [h][split][2]
   int32_t *counters;
   int32_t *status;        // workspace status word (device-side errors)
   int64_t n_cells;
@@ -54,7 +55,7 @@ struct DecodeArgs {
   int32_t group;          // query heads per KV head
   int32_t dk, dv;         // logical head dims
   int32_t nbk, nbv;       // 128-blocks of K / V rows
-  int32_t part_stride;    // floats per (head, split) partial
+  int32_t part_stride;    // floats per (head, split) partial output (128 nbv)
   float scale_log2;       // softmax scale * log2(e)
   DevCodebook cbk, cbv;
   uint32_t tabk[4], tabv[4];   // binary16 byte tables of the code values (see code_byte_tables)
@@ -95,7 +96,7 @@ struct PrefillArgs {
 };
 
 struct DecodeWorkspaceLayout {
-  size_t counters_off, part_off, total;
+  size_t counters_off, ml_off, part_off, total;
   int n_splits;
   int64_t chunk;
 };

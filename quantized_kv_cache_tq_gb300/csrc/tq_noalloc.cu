@@ -66,7 +66,7 @@ extern "C" tq_status tq_fattn_decode_noalloc(const tq_cache *k, const tq_cache *
   }
   // counters and status word must start at zero (the array keeps the last call's contents)
   const DecodeWorkspaceLayout L = decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, algo);
-  if (cudaMemsetAsync(ws, 0, L.part_off, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+  if (cudaMemsetAsync(ws, 0, L.ml_off, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
