@@ -98,18 +98,28 @@ __device__ __forceinline__ void dq_pair16(uint32_t a0, uint32_t a1, uint32_t b0,
   }
 }
 
-// selector words (elements 0..7, 8..15 of the 16-dim group g) of one V key block
+// selector words (elements 0..7, 8..15 of the 16-dim group g) of one V key block.
+// turbo3: the group's sign bits sit in signs word g/2 at the positions sel_words
+// expects for an even (odd) qs word rotated left by rl0 = 0 (2) and right by
+// rr1 = 1 (31) -- rotations rather than shifts, so that g's parity is two
+// per-thread constants instead of selects (the wrapped bits fall outside the
+// 0x44444444 mask).
 template <int T>
-__device__ __forceinline__ void v_sel(const uint8_t *qs_row, const uint8_t *sg_row, int g, uint32_t &s0,
-                                      uint32_t &s1) {
+__device__ __forceinline__ void v_sel(const uint8_t *qs_row, const uint8_t *sg_row, int g, int rl0, int rr1,
+                                      uint32_t &s0, uint32_t &s1) {
   if (T == 4) {
     const uint2 w = *reinterpret_cast<const uint2 *>(qs_row + 8 * g);
     s0 = w.x;
     s1 = w.y;
   } else {
     const uint32_t w = reinterpret_cast<const uint32_t *>(qs_row)[g];
-    const uint32_t sg = (T == 3) ? reinterpret_cast<const uint32_t *>(sg_row)[g >> 1] : 0u;
-    sel_words<T>(w, sg, (g & 1) != 0, s0, s1);
+    s0 = w & 0x33333333u;
+    s1 = (w >> 2) & 0x33333333u;
+    if (T == 3) {
+      const uint32_t sg = reinterpret_cast<const uint32_t *>(sg_row)[g >> 1];
+      s0 |= __funnelshift_l(sg, sg, rl0) & 0x44444444u;
+      s1 |= __funnelshift_r(sg, sg, rr1) & 0x44444444u;
+    }
   }
 }
 
@@ -125,7 +135,11 @@ struct WarpStage {
   static constexpr int NW = (16 * 3 * BYTES0 <= 200 * 1024) ? 16 : 8;
   static constexpr int NT = NW * 32;
   // P tiles, rotated q and the B columns (sized for a group of 4) beside the rings
-  static constexpr uint32_t EXTRA = NW * NBV * 8 * WK * 2 + 4 * 128 * NBK * 4 + 8 * 128 * NBK * 2;
+  // P' tile per warp and V block: 8 columns x PSTR words (16 key pairs, padded so
+  // that neither the pair stores nor the fragment loads conflict on a bank)
+  static constexpr int PSTR = 20;
+  static constexpr uint32_t PTW = NBV * 8 * PSTR * 4;                 // bytes per warp
+  static constexpr uint32_t EXTRA = NW * PTW + 4 * 128 * NBK * 4 + 8 * 128 * NBK * 2;
   static constexpr uint32_t BUDGET = 222 * 1024;
   // A stage holds SUB groups of 32 keys (fewer, larger bulk copies: the copy count,
   // not the bytes, limits how fast the copies are issued).  Two 64-key stages per
@@ -144,8 +158,8 @@ struct WarpStage {
                                 : (NW * 4 * BYTES + EXTRA <= BUDGET) ? 4
                                 : (NW * 3 * BYTES + EXTRA <= BUDGET) ? 3 : 2;
   static constexpr uint32_t RING = STAGES * BYTES;                    // per warp
-  static constexpr uint32_t PT = NW * RING;                           // P tiles [NW][NBV][8][WK] fp16
-  static constexpr uint32_t QR = PT + NW * NBV * 8 * WK * 2;          // rotated q (floats)
+  static constexpr uint32_t PT = NW * RING;                           // P' tiles [NW][NBV][8][PSTR] u32
+  static constexpr uint32_t QR = PT + NW * PTW;                       // rotated q (floats)
 };
 
 template <int T, int G, int NBK, int NBV>
@@ -258,7 +272,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   const int n_it = ge - gb;
 
   unsigned char *ring = smem + warp * WS::RING;
-  uint16_t *pw = reinterpret_cast<uint16_t *>(smem + WS::PT) + warp * NBV * 8 * WK;
+  uint32_t *pw32 = reinterpret_cast<uint32_t *>(smem + WS::PT + warp * WS::PTW);   // P' pairs [NBV][8][PSTR]
   float *qrot = reinterpret_cast<float *>(smem + WS::QR);
 
   const uint8_t *kqs = a.kqs + static_cast<size_t>(hk) * a.n_cells * NBK * QSB;
@@ -341,7 +355,8 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   }
 
   // rotated queries (scale and log2(e) folded in) while the first tiles land, then
-  // the score mma's B columns as binary16: n < G q'_hi, G <= n < 2G q'_lo, else 0
+  // the score mma's B columns as binary16: n = 2h q'_hi, n = 2h + 1 q'_lo of head h,
+  // zero for h >= G
   if (warp < G * NBK) rotate_query_block(a, warp, lane, qv, qrot);
   const bool cell_ok = cell >= 0 && cell < a.n_cells;
   const bool owner = append && cell_ok && ((cell >= t0 && cell < t1) || (cell >= a.kv_len && split == 0));
@@ -361,16 +376,16 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
                       SGB ? patch + PS + gq * SGB : nullptr);
     }
   }
-  for (int i = lane; i < NBV * 8 * WK; i += 32) pw[i] = 0;
+  for (int i = lane; i < NBV * 8 * WS::PSTR; i += 32) pw32[i] = 0;
   __syncthreads();
   uint16_t *qcol = reinterpret_cast<uint16_t *>(smem + WQ::QC);              // [8][128*NBK]
   for (int i = tid; i < 8 * 128 * NBK; i += NT) {
     const int n = i / (128 * NBK), d = i % (128 * NBK);
     float x = 0.f;
-    if (n < 2 * G) {
-      const float q = qrot[(n % G) * 128 * NBK + d];
+    if (n < 2 * G) {                      // column 2h: q'_hi of head h, 2h + 1: q'_lo
+      const float q = qrot[(n >> 1) * 128 * NBK + d];
       const __half hi = __float2half_rn(q);
-      x = (n < G) ? __half2float(hi) : (q - __half2float(hi));
+      x = (n & 1) ? (q - __half2float(hi)) : __half2float(hi);
     }
     qcol[i] = __half_as_ushort(__float2half_rn(x));
   }
@@ -398,10 +413,11 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) oacc[b][mt][i] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  const bool writer = (G == 4) ? (c < 2) : (c == 0);
-  const int hA = (G == 4) ? 2 * (c & 1) : 0;
-  const int nh = (G == 1) ? 1 : 2;
+  // Thread (g, c) owns query head c (if c < G): its score columns 2c, 2c + 1
+  // (hi, lo) and output columns 2c, 2c + 1 are in the thread's own fragments.
+  const bool has_head = c < G;
+  const int rl0 = (g & 1) ? 2 : 0, rr1 = (g & 1) ? 31 : 1;   // v_sel's sign-word rotations
+  float m_run = -INFINITY, l_run = 0.f;
   bool timed_out = false;
 
   for (int it = 0; it < n_it; ++it) {
@@ -445,13 +461,16 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     const uint16_t *knr = reinterpret_cast<const uint16_t *>(st + WS::KN) + j * WK * NBK;
     const uint16_t *vnr = reinterpret_cast<const uint16_t *>(st + WS::VN) + j * WK * NBV;
 
-    // ---- scores S^T[key][n] for two groups of 16 keys (rows grp*16 + g, + 8)
-    float s[2][4];
+    // keys of this group that are in the warp's range (rows >= rem are masked)
+    const int rem = static_cast<int>(min(w1 - key0, static_cast<int64_t>(WK)));
+
+    // ---- scores S^T[key][n] for two groups of 16 keys (rows grp*16 + g, + 8):
+    // sc[grp][0] = row grp*16 + g, sc[grp][1] = row grp*16 + g + 8, head c
+    float sc[2][2];
 #pragma unroll
     for (int grp = 0; grp < 2; ++grp) {
       const int r0 = grp * 16 + g, r1 = r0 + 8;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) s[grp][i] = 0.f;
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
       for (int b = 0; b < NBK; ++b) {
         uint32_t ka0[16], ka1[16];
@@ -463,113 +482,81 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
           mma16816(acc, ka0[2 * kk], ka1[2 * kk], ka0[2 * kk + 1], ka1[2 * kk + 1], qb[b][kk][0], qb[b][kk][1]);
         const float n0 = __half2float(__ushort_as_half(knr[r0 * NBK + b]));
         const float n1 = __half2float(__ushort_as_half(knr[r1 * NBK + b]));
-        s[grp][0] = fmaf(n0, acc[0], s[grp][0]);
-        s[grp][1] = fmaf(n0, acc[1], s[grp][1]);
-        s[grp][2] = fmaf(n1, acc[2], s[grp][2]);
-        s[grp][3] = fmaf(n1, acc[3], s[grp][3]);
+        s0 = fmaf(n0, acc[0] + acc[1], s0);         // hi + lo columns of head c
+        s1 = fmaf(n1, acc[2] + acc[3], s1);
       }
-      // hi + lo columns -> full scores; the thread then holds heads hA, hA+1 of rows r0, r1
-      if (G == 4) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s[grp][i] += __shfl_xor_sync(0xffffffffu, s[grp][i], 2);
-      } else if (G == 2) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s[grp][i] += __shfl_xor_sync(0xffffffffu, s[grp][i], 1);
-      } else {
-        s[grp][0] += s[grp][1];
-        s[grp][2] += s[grp][3];
-        s[grp][1] = s[grp][0];
-        s[grp][3] = s[grp][2];
-      }
-      if (key0 + r0 >= w1) s[grp][0] = s[grp][1] = -INFINITY;
-      if (key0 + r1 >= w1) s[grp][2] = s[grp][3] = -INFINITY;
+      sc[grp][0] = (r0 < rem) ? s0 : -INFINITY;
+      sc[grp][1] = (r1 < rem) ? s1 : -INFINITY;
     }
 
-    // ---- online softmax per head (log2 domain); the reference maximum is raised
+    // ---- online softmax of head c (log2 domain); the reference maximum is raised
     // only when the running maximum grows by more than 2^8 (then O and l rescale)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float tm = fmaxf(fmaxf(s[0][j], s[0][2 + j]), fmaxf(s[1][j], s[1][2 + j]));
+    {
+      float tm = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
-      if (tm > m_run[j] + 8.f) {
-        const float fct = (m_run[j] == -INFINITY) ? 0.f : fast_ex2(m_run[j] - tm);
-        l_run[j] *= fct;
+      if (tm > m_run + 8.f) {
+        const float fct = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - tm);
+        l_run *= fct;
 #pragma unroll
         for (int b = 0; b < NBV; ++b)
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            oacc[b][mt][j] *= fct;
-            oacc[b][mt][2 + j] *= fct;
-          }
-        m_run[j] = tm;
+          for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) oacc[b][mt][i] *= fct;
+        m_run = tm;
       }
 #pragma unroll
-      for (int grp = 0; grp < 2; ++grp) {
-        s[grp][j] = fast_ex2(s[grp][j] - m_run[j]);           // -inf -> 0
-        s[grp][2 + j] = fast_ex2(s[grp][2 + j] - m_run[j]);
-        l_run[j] += s[grp][j] + s[grp][2 + j];
-      }
+      for (int grp = 0; grp < 2; ++grp)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          sc[grp][r] = fast_ex2(sc[grp][r] - m_run);             // -inf -> 0
+          l_run += sc[grp][r];
+        }
     }
 
-    // ---- P' = p * |v| (per V block) as fp16 hi / lo columns of the per-warp tile [n][key]
+    // ---- P' = p * |v| (per V block) as binary16 (hi, lo) key pairs: column 2c (hi)
+    // and 2c + 1 (lo), pair g of group grp = keys (grp*16 + g, grp*16 + g + 8)
 #pragma unroll
     for (int b = 0; b < NBV; ++b) {
-      uint16_t *pt = pw + b * 8 * WK;
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
         const int r0 = grp * 16 + g, r1 = r0 + 8;
         const float v0 = __half2float(__ushort_as_half(vnr[r0 * NBV + b]));
         const float v1 = __half2float(__ushort_as_half(vnr[r1 * NBV + b]));
-        if (G == 4) {
-          // lanes c and c^2 hold the same scores: c < 2 writes the hi halves, c >= 2 the lo
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            // masked keys have p = 0 and may carry garbage norms: select the zero
-            const float x0 = s[grp][j] > 0.f ? s[grp][j] * v0 : 0.f;
-            const float x1 = s[grp][2 + j] > 0.f ? s[grp][2 + j] * v1 : 0.f;
-            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-            const int n = (c < 2) ? hA + j : G + hA + j;
-            pt[n * WK + r0] = __half_as_ushort(c < 2 ? h0 : __float2half_rn(x0 - __half2float(h0)));
-            pt[n * WK + r1] = __half_as_ushort(c < 2 ? h1 : __float2half_rn(x1 - __half2float(h1)));
-          }
-        } else if (writer) {
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            if (j < nh) {
-              const float x0 = s[grp][j] > 0.f ? s[grp][j] * v0 : 0.f;
-              const float x1 = s[grp][2 + j] > 0.f ? s[grp][2 + j] * v1 : 0.f;
-              const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-              const int nhi = hA + j, nlo = G + hA + j;
-              pt[nhi * WK + r0] = __half_as_ushort(h0);
-              pt[nhi * WK + r1] = __half_as_ushort(h1);
-              pt[nlo * WK + r0] = __half_as_ushort(__float2half_rn(x0 - __half2float(h0)));
-              pt[nlo * WK + r1] = __half_as_ushort(__float2half_rn(x1 - __half2float(h1)));
-            }
-          }
+        // masked keys have p = 0 and may carry garbage norms: select the zero
+        const float x0 = sc[grp][0] > 0.f ? sc[grp][0] * v0 : 0.f;
+        const float x1 = sc[grp][1] > 0.f ? sc[grp][1] * v1 : 0.f;
+        const __half2 hi = __floats2half2_rn(x0, x1);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+        if (has_head) {
+          pw32[(b * 8 + 2 * c) * WS::PSTR + grp * 8 + g] = *reinterpret_cast<const uint32_t *>(&hi);
+          pw32[(b * 8 + 2 * c + 1) * WS::PSTR + grp * 8 + g] = *reinterpret_cast<const uint32_t *>(&lo);
         }
       }
     }
     __syncwarp();
 
-    // ---- O'^T[d][n] += V'^T[d][key] P'^T[key][n]
+    // ---- O'^T[d][n] += V'^T[d][key] P'^T[key][n], contraction order: k-slots
+    // (2c, 2c + 1) <-> keys (c, c + 8), (2c + 8, 2c + 9) <-> keys (c + 4, c + 12)
 #pragma unroll
     for (int b = 0; b < NBV; ++b) {
-      const uint32_t *pt32 = reinterpret_cast<const uint32_t *>(pw + b * 8 * WK);
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
-        const uint32_t pb0 = pt32[g * (WK / 2) + grp * 8 + c], pb1 = pt32[g * (WK / 2) + grp * 8 + c + 4];
+        const uint32_t pb0 = pw32[(b * 8 + g) * WS::PSTR + grp * 8 + c];
+        const uint32_t pb1 = pw32[(b * 8 + g) * WS::PSTR + grp * 8 + c + 4];
         const int kr = grp * 16;
         uint32_t s00, s01, s10, s11, s20, s21, s30, s31;
         const uint8_t *vq = svq, *vs = svs;
-        v_sel<T>(vq + ((kr + 2 * c) * NBV + b) * QSB, vs + ((kr + 2 * c) * NBV + b) * SGB, g, s00, s01);
-        v_sel<T>(vq + ((kr + 2 * c + 1) * NBV + b) * QSB, vs + ((kr + 2 * c + 1) * NBV + b) * SGB, g, s10, s11);
-        v_sel<T>(vq + ((kr + 2 * c + 8) * NBV + b) * QSB, vs + ((kr + 2 * c + 8) * NBV + b) * SGB, g, s20, s21);
-        v_sel<T>(vq + ((kr + 2 * c + 9) * NBV + b) * QSB, vs + ((kr + 2 * c + 9) * NBV + b) * SGB, g, s30, s31);
+        v_sel<T>(vq + ((kr + c) * NBV + b) * QSB, vs + ((kr + c) * NBV + b) * SGB, g, rl0, rr1, s00, s01);
+        v_sel<T>(vq + ((kr + c + 8) * NBV + b) * QSB, vs + ((kr + c + 8) * NBV + b) * SGB, g, rl0, rr1, s10, s11);
+        v_sel<T>(vq + ((kr + c + 4) * NBV + b) * QSB, vs + ((kr + c + 4) * NBV + b) * SGB, g, rl0, rr1, s20, s21);
+        v_sel<T>(vq + ((kr + c + 12) * NBV + b) * QSB, vs + ((kr + c + 12) * NBV + b) * SGB, g, rl0, rr1, s30, s31);
         uint32_t lo[16], hi[16];
-        dq_pair16<T>(s00, s01, s10, s11, tab_v, lo);     // keys 2c, 2c+1
-        dq_pair16<T>(s20, s21, s30, s31, tab_v, hi);     // keys 2c+8, 2c+9
+        dq_pair16<T>(s00, s01, s10, s11, tab_v, lo);     // keys c, c + 8
+        dq_pair16<T>(s20, s21, s30, s31, tab_v, hi);     // keys c + 4, c + 12
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
           mma16816(oacc[b][mt], lo[2 * mt], lo[2 * mt + 1], hi[2 * mt], hi[2 * mt + 1], pb0, pb1);
@@ -583,47 +570,24 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   // ---- per-warp results -> this warp's ring (all its copies have landed), CTA merge
   if (timed_out && lane == 0) set_status(a.status, TQ_ERR_TIMEOUT);
   float *wbuf = reinterpret_cast<float *>(ring);                 // m[G], l[G], o[G][DVP]
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    float l = l_run[j];
-    l += __shfl_xor_sync(0xffffffffu, l, 4);
-    l += __shfl_xor_sync(0xffffffffu, l, 8);
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
-    l_run[j] = l;
-  }
-#pragma unroll
-  for (int b = 0; b < NBV; ++b)
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float v = oacc[b][mt][i];
-        if (G == 4) v += __shfl_xor_sync(0xffffffffu, v, 2);
-        else if (G == 2) v += __shfl_xor_sync(0xffffffffu, v, 1);
-        oacc[b][mt][i] = v;
-      }
-  if (writer) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int h = hA + j;
-      if (h < G) {
-        if (g == 0) {
-          wbuf[h] = timed_out ? -INFINITY : m_run[j];
-          wbuf[G + h] = timed_out ? 0.f : l_run[j];
-        }
-#pragma unroll
-        for (int b = 0; b < NBV; ++b)
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            // G == 1: columns 0 (hi) and 1 (lo) of head 0
-            const float top = (G == 1) ? oacc[b][mt][0] + oacc[b][mt][1] : oacc[b][mt][j];
-            const float bot = (G == 1) ? oacc[b][mt][2] + oacc[b][mt][3] : oacc[b][mt][2 + j];
-            float *o = wbuf + 2 * G + h * DVP + b * 128 + 16 * g + 2 * mt;
-            o[0] = timed_out ? 0.f : top;
-            o[1] = timed_out ? 0.f : bot;
-          }
-      }
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 4);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 8);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
+  if (has_head) {
+    const int h = c;
+    if (g == 0) {
+      wbuf[h] = timed_out ? -INFINITY : m_run;
+      wbuf[G + h] = timed_out ? 0.f : l_run;
     }
+#pragma unroll
+    for (int b = 0; b < NBV; ++b)
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        // columns 2c (hi part of P') and 2c + 1 (lo part) of dims 16g + 2mt, + 1
+        float *o = wbuf + 2 * G + h * DVP + b * 128 + 16 * g + 2 * mt;
+        o[0] = timed_out ? 0.f : oacc[b][mt][0] + oacc[b][mt][1];
+        o[1] = timed_out ? 0.f : oacc[b][mt][2] + oacc[b][mt][3];
+      }
   }
   __syncthreads();
   // CTA partial over the warps.  Launched as one cluster per KV head (cluster
