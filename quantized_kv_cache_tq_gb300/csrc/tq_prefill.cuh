@@ -254,16 +254,22 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
     if (lane == 0) {
       constexpr uint32_t ID_S = tc::idesc_f16(BM, BN, false, false);
       constexpr uint32_t ID_PV = tc::idesc_f16(BM, 128, false, true);
+      // Descriptors: the start-address field holds addr >> 4 in 14 bits and no
+      // operand crosses 256 KB, so an operand at base + off has the descriptor
+      // desc(base) + (off >> 4) -- one add per mma instead of a rebuild.
+      const uint64_t q_desc = tc::sdesc(sbase + C::Q, 2048, 128);
+      const uint64_t k_desc = tc::sdesc(sbase + C::KV, 128, 2048);
+      const uint64_t v_desc = tc::sdesc(sbase + C::KV + NBK * C::TBLK, 2048, 128);
       auto issue_pv = [&](int j) {
         const uint32_t pbuf = tmem + C::SP0 + (j & 1) * C::SPW;
-        const uint32_t vbuf = sbase + C::KV + (j & 1) * C::KVBUF + NBK * C::TBLK;
+        const uint64_t vb = v_desc + (((j & 1) * C::KVBUF) >> 4);
 #pragma unroll
         for (int b = 0; b < NBV; ++b)
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks) {
-              const uint64_t bd = tc::sdesc(vbuf + b * C::TBLK + ks * 4096, 2048, 128);
+              const uint64_t bd = vb + ((b * C::TBLK + ks * 4096) >> 4);
               mma_f16_ta(tmem + b * 128, pbuf + (2 * b + part) * (BN / 2) + ks * 8, bd, ID_PV,
                          j > 0 || part > 0 || ks > 0);
             }
@@ -276,19 +282,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
         if (!ok) break;
         tc::fence_after_sync();
         const uint32_t sbuf = tmem + C::SP0 + (j & 1) * C::SPW;
-        const uint32_t kbuf = sbase + C::KV + (j & 1) * C::KVBUF;
+        const uint64_t kb = k_desc + (((j & 1) * C::KVBUF) >> 4);
 #pragma unroll
         for (int b = 0; b < NBK; ++b)
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t ad = tc::sdesc(sbase + C::Q + (part * NBK + b) * C::QBLK + ks * 4096, 2048, 128);
-              const uint64_t bd = tc::sdesc(kbuf + b * C::TBLK + ks * 256, 128, 2048);
+              const uint64_t ad = q_desc + (((part * NBK + b) * C::QBLK + ks * 4096) >> 4);
+              const uint64_t bd = kb + ((b * C::TBLK + ks * 256) >> 4);
               tc::mma_f16(sbuf + b * BN, ad, bd, ID_S, part > 0 || ks > 0);
             }
         tc::mma_commit(&bars.sf[j & 1]);
-        if (j + STAGES < n_tiles) issue(j + STAGES);           // the stage of tile j was consumed
         if (j >= 1) {
           ok = tc::mbar_wait(&bars.pf[(j - 1) & 1], ((j - 1) >> 1) & 1);
           if (!ok) break;
@@ -372,6 +377,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
       tc::fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.dq[j & 1]);
+      // the stage of tile j is free once all four dequant warps are done with it:
+      // one of them refills it (the control thread only issues mma)
+      if (warp == 4 && lane == 0 && j + STAGES < n_tiles) {
+        if (tc::mbar_wait(&bars.dq[j & 1], (j >> 1) & 1)) issue(j + STAGES);
+        else s_fail = 1;
+      }
     }
   } else {
     // ===================== softmax: one query row per thread =====================
@@ -439,10 +450,11 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
           // masked keys may carry garbage norms: select, never multiply, a zero
           const float x0 = s[k0] > 0.f ? s[k0] * nr[k0 * (NBK + NBV) + NBK + b] : 0.f;
           const float x1 = s[k0 + 1] > 0.f ? s[k0 + 1] * nr[(k0 + 1) * (NBK + NBV) + NBK + b] : 0.f;
-          const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-          ph[i] = __half_as_ushort(h0) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-          pl[i] = __half_as_ushort(__float2half_rn(x0 - __half2float(h0))) |
-                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x1 - __half2float(h1)))) << 16);
+          const __half2 h = __floats2half2_rn(x0, x1);
+          const float2 hf = __half22float2(h);
+          const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+          ph[i] = *reinterpret_cast<const uint32_t *>(&h);
+          pl[i] = *reinterpret_cast<const uint32_t *>(&l);
         }
         tmem_st<BN / 2>(sbuf + (2 * b) * (BN / 2), ph);
         tmem_st<BN / 2>(sbuf + (2 * b + 1) * (BN / 2), pl);
