@@ -5,17 +5,22 @@
 //
 // The page's sm_75 kernel gathers each 32-cell chunk's rows into registers
 // during the previous chunk and shares one shared buffer between K and V to fit
-// two blocks per SM.  On GB300 the gather is asynchronous instead: warp 0
-// issues one 128-byte cp.async.bulk per scattered K or V row into a 2-deep ring,
-// completion counted on an mbarrier, so the next tile's rows stream in while the
-// tensor cores work on the current one.  The tile math is tcgen05:
-//   S = Q K_int^T (M = 128 rows, N = 64 keys, K = 128), fp16 operands -- int8
-//   values and the fp16 queries are exact in binary16, so S is exact up to fp32
-//   accumulation; the row scales and the softmax scale are applied in fp32;
-//   O += P' V_int with P' = p * scale_v split into fp16 hi + lo parts.
-// int8 -> binary16 in registers: a byte b becomes the half 0x64xx with
-// xx = b ^ 0x80 (value 1024 + b + 128) by one byte permute, then one packed
-// subtraction of 1152 gives b exactly.
+// two blocks per SM.  On GB300 the gather is asynchronous and spread over four
+// warps: every gather thread owns one K or V row of the key tile and streams it
+// with 16-byte cp.async copies into its own slots of a 4-deep ring (its cell id
+// one tile ahead of the copy, its scale one tile ahead of the use), so it only
+// ever waits for its own copies.  The math runs on tcgen05 in the same
+// warp-specialised pipeline as the turbo prefill:
+//   control warp (one thread): S_j = Q K'_j^T into tensor memory, then
+//     O += P'_{j-1} V'_{j-1} while the softmax works on tile j;
+//   4 gather warps: int8 rows -> exact binary16 K' / V' tiles (a byte b becomes
+//     the half 0x64xx, xx = b ^ 0x80, i.e. 1024 + b + 128, by one byte permute;
+//     one packed subtraction of 1152 gives b), row scales as floats;
+//   4 softmax warps (one query row per thread, TMEM lanes 0..127): read S_j,
+//     apply scale_k * scale * log2(e) and the causal mask by logical position,
+//     the online softmax (lazy rescale of O in tensor memory), and write
+//     P' = p * scale_v as binary16 hi + lo over S_j, where the PV mma reads it.
+// Q is binary16 as given, so S is exact up to fp32 accumulation.
 #include <math.h>
 
 #include "tq_common.cuh"
@@ -40,17 +45,20 @@ struct Int8Args {
 
 namespace i8 {
 
-constexpr int BM = 128, BN = 64, D = 128, NT = 256;
-constexpr uint32_t SQ = 0;                      // Q      [d/8][row/8]      32 KB
-constexpr uint32_t SK = SQ + 32768;             // K'     [key/8][d/8]      16 KB
-constexpr uint32_t SV = SK + 16384;             // V'     [key/8][d/8]      16 KB
-constexpr uint32_t SP = SV + 16384;             // P' hi, lo [key/8][row/8] 2 x 16 KB
-constexpr uint32_t SSTG = SP + 32768;           // raw rows: 2 stages x (K 8 KB + V 8 KB)
-constexpr uint32_t STAGE = 2 * BN * D;
-constexpr uint32_t SCELL = SSTG + 2 * STAGE;    // int32 cells [2][BN]
-constexpr uint32_t SSCL = SCELL + 2 * BN * 4;   // float scales [BN][2] (k, v) of the current tile
-constexpr uint32_t TOTAL = SSCL + BN * 2 * 4;
-constexpr int TMEM_COLS = 256;                  // O: 128 columns, S: 64 columns
+constexpr int BM = 128, BN = 64, D = 128;
+constexpr int NWARP = 9;                        // 0-3 softmax, 4-7 gather, 8 control
+constexpr int NT = NWARP * 32;
+constexpr int RING = 4;                         // raw-row ring depth (tiles)
+constexpr int LOOK = RING - 1;                  // copies run this many tiles ahead
+constexpr uint32_t SQ = 0;                      // Q       [d/8][row/8]            32 KB
+constexpr uint32_t SK = SQ + 32768;             // K'      2 x [key/8][d/8]       2 x 16 KB
+constexpr uint32_t SV = SK + 2 * 16384;         // V'      2 x [key/8][d/8]       2 x 16 KB
+constexpr uint32_t SR = SV + 2 * 16384;         // raw     RING x [K|V][key][128 B]
+constexpr uint32_t RSTAGE = 2 * BN * D;
+constexpr uint32_t SSC = SR + RING * RSTAGE;    // scales  2 x [key][k, v] floats
+constexpr uint32_t TOTAL = SSC + 2 * BN * 2 * 4;
+constexpr int TMEM_COLS = 256;                  // O: 128 columns, S / P': 2 x 64 columns
+constexpr uint32_t SP0 = 128;
 
 __device__ __forceinline__ long long i64min(long long x, long long y) { return x < y ? x : y; }
 __device__ __forceinline__ long long i64max(long long x, long long y) { return x > y ? x : y; }
@@ -67,11 +75,49 @@ __device__ __forceinline__ void i8x4_to_h(uint32_t w, uint32_t &h01, uint32_t &h
   h23 = *reinterpret_cast<const uint32_t *>(&hb);
 }
 
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(tc::smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+// tcgen05.mma with the A operand in tensor memory
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc)));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+struct Bars {
+  uint64_t cv[2];          // K'/V' tile and its scales written (4 gather warps)
+  uint64_t sf[2];          // S_j computed (mma commit)
+  uint64_t pf[2];          // P'_j written (4 softmax warps)
+  uint64_t pv[2];          // PV_j computed (mma commit)
+};
+
 __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  __shared__ __align__(8) uint64_t full[2];
-  __shared__ __align__(8) uint64_t bar_s, bar_pv;
+  __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_slot;
+  __shared__ int s_fail;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hk = blockIdx.y, G = a.group;
@@ -80,61 +126,19 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
   const int64_t pos0 = a.ctx - a.nq;
   const int64_t kv_hi = a.causal ? i64min(a.ctx, pos0 + q_last + 1) : a.ctx;
   const int n_tiles = static_cast<int>((kv_hi + BN - 1) / BN);
-  const int64_t row_stride = static_cast<int64_t>(a.n_kv_heads) * D;      // bytes per cell
-  int32_t *cells = reinterpret_cast<int32_t *>(smem + SCELL);
-
-  // warp 0: gather the tile's scattered rows (one bulk copy per row)
-  auto issue = [&](int tile) {
-    const int st = tile & 1;
-    unsigned char *kst = smem + SSTG + st * STAGE, *vst = kst + BN * D;
-    int cl[2];
-    bool ok[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int key = lane + 32 * h;
-      const int64_t t = static_cast<int64_t>(tile) * BN + key;
-      int c = -1;
-      if (t < kv_hi) c = a.cell_of_pos[t];
-      ok[h] = t < kv_hi && c >= 0 && c < a.n_cells;
-      if (t < kv_hi && !ok[h]) set_status(a.status, TQ_ERR_DEVICE_CHECK);
-      cl[h] = ok[h] ? c : -1;
-      cells[st * BN + key] = cl[h];
-      if (!ok[h]) {                       // out-of-range cell: a zero row; beyond kv_hi: unused
-        for (int i = 0; i < D; i += 16) {
-          *reinterpret_cast<uint4 *>(kst + key * D + i) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4 *>(vst + key * D + i) = make_uint4(0, 0, 0, 0);
-        }
-      }
-    }
-    const uint32_t n_ok = __popc(__ballot_sync(0xffffffffu, ok[0])) + __popc(__ballot_sync(0xffffffffu, ok[1]));
-    if (lane == 0) tc::mbar_expect_tx(&full[st], n_ok * 2 * D);
-    __syncwarp();
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (ok[h]) {
-        const int key = lane + 32 * h;
-        const int64_t off = static_cast<int64_t>(cl[h]) * row_stride + hk * D;
-        tc::bulk_g2s(kst + key * D, a.k + off, D, &full[st]);
-        tc::bulk_g2s(vst + key * D, a.v + off, D, &full[st]);
-      }
-    }
-  };
+  float *scl = reinterpret_cast<float *>(smem + SSC);
 
   if (warp == 0) tc::tmem_alloc<TMEM_COLS>(&tmem_slot);
-  if (tid == 0) {
-    tc::mbar_init(&full[0], 1);
-    tc::mbar_init(&full[1], 1);
-    tc::mbar_init(&bar_s, 1);
-    tc::mbar_init(&bar_pv, 1);
+  if (tid == NT - 32) {
+    s_fail = 0;
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&bars.cv[b], 4);
+      tc::mbar_init(&bars.sf[b], 1);
+      tc::mbar_init(&bars.pf[b], 4);
+      tc::mbar_init(&bars.pv[b], 1);
+    }
     tc::mbar_init_fence();
   }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = tmem_slot;
-  if (warp == 0)
-    for (int i = 0; i < 2 && i < n_tiles; ++i) issue(i);
-
   // Q tile (binary16 as given): row r = query q0 + r/G, head hk*G + r%G
   for (int it = tid; it < BM * (D / 8); it += NT) {
     const int r = it / (D / 8), dc = it % (D / 8);
@@ -143,77 +147,161 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
     if (qi < a.nq) val = *reinterpret_cast<const uint4 *>(a.q + (static_cast<size_t>(qi) * a.n_q_heads + h) * D + dc * 8);
     *reinterpret_cast<uint4 *>(smem + SQ + (dc * 16 + (r >> 3)) * 128 + (r & 7) * 16) = val;
   }
-
-  constexpr uint32_t ID_S = tc::idesc_f16(BM, BN, false, false);
-  constexpr uint32_t ID_PV = tc::idesc_f16(BM, D, false, true);
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_slot;
   const uint32_t sbase = tc::smem_u32(smem);
-  float *scl = reinterpret_cast<float *>(smem + SSCL);
 
-  const int row = tid;
+  const int row = tid & (BM - 1);
   const int row_q = q0 + row / G;
-  const bool row_ok = tid < BM && row_q < a.nq;
+  const bool row_ok = warp < 4 && row_q < a.nq;
   const int64_t row_end = a.causal ? (pos0 + row_q + 1) : a.ctx;
   float m_used = -INFINITY, l_sum = 0.f;
-  bool failed = false;
 
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    const int st = tile & 1;
-    bool ok = tc::mbar_wait(&full[st], (tile >> 1) & 1);
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-
-    // ---- int8 rows -> binary16 K' / V' tiles; row scales as floats
-    const unsigned char *kst = smem + SSTG + st * STAGE, *vst = kst + BN * D;
-    for (int it = tid; it < 2 * BN * (D / 8); it += NT) {
-      const bool is_v = it >= BN * (D / 8);
-      const int rem = is_v ? it - BN * (D / 8) : it;
-      const int dc = rem / BN, key = rem % BN;
-      const uint2 w = *reinterpret_cast<const uint2 *>((is_v ? vst : kst) + key * D + dc * 8);
-      uint4 o;
-      i8x4_to_h(w.x, o.x, o.y);
-      i8x4_to_h(w.y, o.z, o.w);
-      *reinterpret_cast<uint4 *>(smem + (is_v ? SV : SK) + ((key >> 3) * 16 + dc) * 128 + (key & 7) * 16) = o;
-    }
-    if (tid < BN) {
-      const int c = cells[st * BN + tid];
-      float ks = 0.f, vs = 0.f;
-      if (c >= 0) {
-        ks = __half2float(__ushort_as_half(a.k_scale[static_cast<int64_t>(c) * a.n_kv_heads + hk]));
-        vs = __half2float(__ushort_as_half(a.v_scale[static_cast<int64_t>(c) * a.n_kv_heads + hk]));
-      }
-      scl[2 * tid] = ks;
-      scl[2 * tid + 1] = vs;
-    }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    if (warp == 0 && tile + 2 < n_tiles) issue(tile + 2);
-    if (tid == 0) {
+  if (warp == 8) {
+    // ===================== control: mma issue =====================
+    if (lane == 0) {
+      constexpr uint32_t ID_S = tc::idesc_f16(BM, BN, false, false);
+      constexpr uint32_t ID_PV = tc::idesc_f16(BM, D, false, true);
+      // descriptor of base + off = descriptor of base + (off >> 4) (14-bit address field, < 256 KB)
+      const uint64_t q_desc = tc::sdesc(sbase + SQ, 2048, 128);
+      const uint64_t k_desc = tc::sdesc(sbase + SK, 128, 2048);
+      const uint64_t v_desc = tc::sdesc(sbase + SV, 2048, 128);
+      auto issue_pv = [&](int j) {
+        const uint32_t pbuf = tmem + SP0 + (j & 1) * BN;
+        const uint64_t vb = v_desc + (((j & 1) * 16384) >> 4);
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint64_t ad = tc::sdesc(sbase + SQ + ks * 4096, 2048, 128);
-        const uint64_t bd = tc::sdesc(sbase + SK + ks * 256, 128, 2048);
-        tc::mma_f16(tmem + 128, ad, bd, ID_S, ks > 0);
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks)
+            mma_f16_ta(tmem, pbuf + part * (BN / 2) + ks * 8, vb + ((ks * 4096) >> 4), ID_PV,
+                       j > 0 || part > 0 || ks > 0);
+        tc::mma_commit(&bars.pv[j & 1]);
+      };
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        ok = tc::mbar_wait(&bars.cv[j & 1], (j >> 1) & 1);
+        if (ok && j >= 2) ok = tc::mbar_wait(&bars.pv[j & 1], ((j - 2) >> 1) & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t sbuf = tmem + SP0 + (j & 1) * BN;
+        const uint64_t kb = k_desc + (((j & 1) * 16384) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc::mma_f16(sbuf, q_desc + ((ks * 4096) >> 4), kb + ((ks * 256) >> 4), ID_S, ks > 0);
+        tc::mma_commit(&bars.sf[j & 1]);
+        if (j >= 1) {
+          ok = tc::mbar_wait(&bars.pf[(j - 1) & 1], ((j - 1) >> 1) & 1);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_pv(j - 1);
+        }
       }
-      tc::mma_commit(&bar_s);
+      if (ok && n_tiles > 0) {
+        const int j = n_tiles - 1;
+        ok = tc::mbar_wait(&bars.pf[j & 1], (j >> 1) & 1);
+        if (ok) {
+          tc::fence_after_sync();
+          issue_pv(j);
+        }
+      }
+      if (!ok) s_fail = 1;
     }
-    ok = tc::mbar_wait(&bar_s, tile & 1);
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-    tc::fence_after_sync();
-
-    if (warp < 4) {
-      const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+  } else if (warp >= 4) {
+    // ===================== gather: one K or V row of the tile per thread =====================
+    const int gt = tid - 128;                     // 0..127
+    const bool is_v = gt >= BN;
+    const int key = gt & (BN - 1);
+    const int8_t *src = (is_v ? a.v : a.k) + static_cast<int64_t>(hk) * D;
+    const uint16_t *ssrc = (is_v ? a.v_scale : a.k_scale) + hk;
+    const int64_t row_stride = static_cast<int64_t>(a.n_kv_heads) * D;
+    // cell of this thread's key in tile j, -1 if beyond kv_hi or out of range (a zero row)
+    auto cell_of = [&](int j) -> int64_t {
+      const int64_t t = static_cast<int64_t>(j) * BN + key;
+      if (j >= n_tiles || t >= kv_hi) return -1;
+      const int64_t c = __ldg(a.cell_of_pos + t);
+      if (c < 0 || c >= a.n_cells) {
+        if (!is_v) set_status(a.status, TQ_ERR_DEVICE_CHECK);
+        return -1;
+      }
+      return c;
+    };
+    auto fetch = [&](int j, int64_t c) {          // this thread's row of tile j -> ring slot j % RING
+      unsigned char *dst = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
+      const int8_t *p = (c >= 0) ? src + c * row_stride : src;
+      const uint32_t nb = (c >= 0) ? 16u : 0u;
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) cp_async16(dst + 16 * i, p + 16 * i, nb);
+    };
+    // cells of tiles 0 .. LOOK (registers cN[k] = cell of tile j + k at iteration j)
+    int64_t cN[LOOK + 1];
+#pragma unroll
+    for (int k = 0; k <= LOOK; ++k) cN[k] = cell_of(k);
+#pragma unroll
+    for (int k = 0; k < LOOK; ++k) {
+      fetch(k, cN[k]);
+      cp_async_commit();
+    }
+    float sc_cur = (cN[0] >= 0) ? __half2float(__ushort_as_half(__ldg(ssrc + cN[0] * a.n_kv_heads))) : 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      // copies LOOK tiles ahead, the next cell id one step further, the next scale
+      const int64_t c_far = cell_of(j + LOOK + 1);
+      if (j + LOOK < n_tiles) fetch(j + LOOK, cN[LOOK]);
+      cp_async_commit();
+      const float sc_next =
+          (cN[1] >= 0) ? __half2float(__ushort_as_half(__ldg(ssrc + cN[1] * a.n_kv_heads))) : 0.f;
+      cp_async_wait<LOOK>();                        // this thread's row of tile j has landed
+      // K'/V' buffer j & 1 is free once PV_{j-2} is done
+      if (j >= 2) ok = tc::mbar_wait(&bars.pv[j & 1], ((j - 2) >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { s_fail = 1; break; }
+      tc::fence_after_sync();
+      const unsigned char *rw = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
+      unsigned char *dst = smem + (is_v ? SV : SK) + (j & 1) * 16384 + (key >> 3) * 2048 + (key & 7) * 16;
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(rw + 16 * i);
+        uint4 o0, o1;
+        i8x4_to_h(w.x, o0.x, o0.y);
+        i8x4_to_h(w.y, o0.z, o0.w);
+        i8x4_to_h(w.z, o1.x, o1.y);
+        i8x4_to_h(w.w, o1.z, o1.w);
+        *reinterpret_cast<uint4 *>(dst + (2 * i) * 128) = o0;          // dims 16 i .. 16 i + 7
+        *reinterpret_cast<uint4 *>(dst + (2 * i + 1) * 128) = o1;      // dims 16 i + 8 .. 16 i + 15
+      }
+      scl[((j & 1) * BN + key) * 2 + (is_v ? 1 : 0)] = sc_cur;
+      tc::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.cv[j & 1]);
+      sc_cur = sc_next;
+#pragma unroll
+      for (int k = 0; k < LOOK; ++k) cN[k] = cN[k + 1];
+      cN[LOOK] = c_far;
+    }
+    cp_async_wait<0>();
+  } else {
+    // ===================== softmax: one query row per thread =====================
+    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = tc::mbar_wait(&bars.sf[j & 1], (j >> 1) & 1);
+      if (ok) ok = tc::mbar_wait(&bars.cv[j & 1], (j >> 1) & 1);      // scales of tile j are written
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc::fence_after_sync();
+      const uint32_t sbuf = tmem + lane_off + SP0 + (j & 1) * BN;
+      const float *sc = scl + (j & 1) * BN * 2;
       float s[BN];
-#pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r0[32];
-        tc::tmem_ld32(tmem + lane_off + 128 + c0, r0);
+      {
+        uint32_t r0[BN];
+        tc::tmem_ld32(sbuf, r0);
+        tc::tmem_ld32(sbuf + 32, r0 + 32);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(r0[i]) * scl[2 * (c0 + i)] * a.scale_log2;
+        for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r0[i]) * (sc[2 * i] * a.scale_log2);
       }
-      const int64_t key0 = static_cast<int64_t>(tile) * BN;
+      const int64_t key0 = static_cast<int64_t>(j) * BN;
       const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(BN, row_end - key0))) : 0;
       float mt = -INFINITY;
 #pragma unroll
@@ -223,6 +311,10 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
       const float fct = (raise && m_used != -INFINITY) ? exp2f(m_used - mt) : 1.f;
       if (raise) m_used = mt;
       if (__any_sync(0xffffffffu, fct != 1.f)) {
+        // O must be stable: wait for the PV mma of the previous tile
+        bool okp = (j == 0) || tc::mbar_wait(&bars.pv[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        if (!__all_sync(0xffffffffu, okp)) { ok = false; break; }
+        tc::fence_after_sync();
         l_sum *= fct;
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
@@ -233,7 +325,6 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * fct);
           tc::tmem_st32(tmem + lane_off + c, r);
         }
-        tc::tmem_wait_st();
       }
       float psum = 0.f;
 #pragma unroll
@@ -242,48 +333,44 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
         psum += s[i];
       }
       l_sum += psum;
+      // P' = p * scale_v as binary16 (hi, lo) key pairs over S_j: row = lane
+      uint32_t ph[BN / 2], pl[BN / 2];
 #pragma unroll
-      for (int kc = 0; kc < BN / 8; ++kc) {
-        uint32_t wh[4], wl[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int k0 = kc * 8 + 2 * j;
-          const float x0 = s[k0] > 0.f ? s[k0] * scl[2 * k0 + 1] : 0.f;
-          const float x1 = s[k0 + 1] > 0.f ? s[k0 + 1] * scl[2 * (k0 + 1) + 1] : 0.f;
-          const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-          wh[j] = __half_as_ushort(h0) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
-          wl[j] = __half_as_ushort(__float2half_rn(x0 - __half2float(h0))) |
-                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(x1 - __half2float(h1)))) << 16);
-        }
-        const uint32_t off = (kc * 16 + (row >> 3)) * 128 + (row & 7) * 16;
-        *reinterpret_cast<uint4 *>(smem + SP + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4 *>(smem + SP + 16384 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      for (int i = 0; i < BN / 2; ++i) {
+        const int k0 = 2 * i;
+        // masked keys may carry garbage scales: select, never multiply, a zero
+        const float x0 = s[k0] > 0.f ? s[k0] * sc[2 * k0 + 1] : 0.f;
+        const float x1 = s[k0 + 1] > 0.f ? s[k0 + 1] * sc[2 * (k0 + 1) + 1] : 0.f;
+        const __half2 h = __floats2half2_rn(x0, x1);
+        const float2 hf = __half22float2(h);
+        const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+        ph[i] = *reinterpret_cast<const uint32_t *>(&h);
+        pl[i] = *reinterpret_cast<const uint32_t *>(&l);
       }
+      tc::tmem_st32(sbuf, ph);
+      tc::tmem_st32(sbuf + BN / 2, pl);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.pf[j & 1]);
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-
-    if (tid == 0) {
-#pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t ad = tc::sdesc(sbase + SP + part * 16384 + ks * 4096, 2048, 128);
-          const uint64_t bd = tc::sdesc(sbase + SV + ks * 4096, 2048, 128);
-          tc::mma_f16(tmem, ad, bd, ID_PV, tile > 0 || part > 0 || ks > 0);
-        }
-      tc::mma_commit(&bar_pv);
+    // the last PV must be complete before O is read
+    if (ok && n_tiles > 0) {
+      const int j = n_tiles - 1;
+      ok = tc::mbar_wait(&bars.pv[j & 1], (j >> 1) & 1);
+      ok = __all_sync(0xffffffffu, ok);
+      tc::fence_after_sync();
     }
-    ok = tc::mbar_wait(&bar_pv, tile & 1);
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-    tc::fence_after_sync();
+    if (!ok) s_fail = 1;
   }
 
-  if (failed) {
-    if (tid == 0) set_status(a.status, TQ_ERR_TIMEOUT);
-  } else if (warp < 4) {
+  // ===================== epilogue =====================
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const bool failed = s_fail != 0;
+  if (failed && tid == 0) set_status(a.status, TQ_ERR_TIMEOUT);
+  if (warp < 4 && !failed) {
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
     const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
     const int h = hk * G + row % G;
@@ -297,8 +384,9 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
           *reinterpret_cast<float4 *>(orow + c + i) =
-              make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
-                          __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
+              n_tiles > 0 ? make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
+                                        __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
   }
