@@ -50,14 +50,15 @@ constexpr int NWARP = 9;                        // 0-3 softmax, 4-7 gather, 8 co
 constexpr int NT = NWARP * 32;
 constexpr int RING = 4;                         // raw-row ring depth (tiles)
 constexpr int LOOK = RING - 1;                  // copies run this many tiles ahead
+constexpr int NB = 3;                           // K'/V' tiles, scales and S / P' buffers in flight
 constexpr uint32_t SQ = 0;                      // Q       [d/8][row/8]            32 KB
-constexpr uint32_t SK = SQ + 32768;             // K'      2 x [key/8][d/8]       2 x 16 KB
-constexpr uint32_t SV = SK + 2 * 16384;         // V'      2 x [key/8][d/8]       2 x 16 KB
-constexpr uint32_t SR = SV + 2 * 16384;         // raw     RING x [K|V][key][128 B]
+constexpr uint32_t SK = SQ + 32768;             // K'      NB x [key/8][d/8]      NB x 16 KB
+constexpr uint32_t SV = SK + NB * 16384;        // V'      NB x [key/8][d/8]      NB x 16 KB
+constexpr uint32_t SR = SV + NB * 16384;        // raw     RING x [K|V][key][128 B]
 constexpr uint32_t RSTAGE = 2 * BN * D;
-constexpr uint32_t SSC = SR + RING * RSTAGE;    // scales  2 x [key][k, v] floats
-constexpr uint32_t TOTAL = SSC + 2 * BN * 2 * 4;
-constexpr int TMEM_COLS = 256;                  // O: 128 columns, S / P': 2 x 64 columns
+constexpr uint32_t SSC = SR + RING * RSTAGE;    // scales  NB x [key][k, v] floats
+constexpr uint32_t TOTAL = SSC + NB * BN * 2 * 4;
+constexpr int TMEM_COLS = 512;                  // O: 128 columns, S / P': NB x 64 columns
 constexpr uint32_t SP0 = 128;
 
 __device__ __forceinline__ long long i64min(long long x, long long y) { return x < y ? x : y; }
@@ -106,11 +107,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
       : "memory");
 }
 
-struct Bars {
-  uint64_t cv[2];          // K'/V' tile and its scales written (4 gather warps)
-  uint64_t sf[2];          // S_j computed (mma commit)
-  uint64_t pf[2];          // P'_j written (4 softmax warps)
-  uint64_t pv[2];          // PV_j computed (mma commit)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+struct Bars {               // buffer j % NB, phase (j / NB) & 1
+  uint64_t cv[NB];         // K'/V' tile and its scales written (4 gather warps)
+  uint64_t sf[NB];         // S_j computed (mma commit)
+  uint64_t pf[NB];         // P'_j written (4 softmax warps)
+  uint64_t pv[NB];         // PV_j computed (mma commit)
 };
 
 __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
@@ -131,7 +140,7 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
   if (warp == 0) tc::tmem_alloc<TMEM_COLS>(&tmem_slot);
   if (tid == NT - 32) {
     s_fail = 0;
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NB; ++b) {
       tc::mbar_init(&bars.cv[b], 4);
       tc::mbar_init(&bars.sf[b], 1);
       tc::mbar_init(&bars.pf[b], 4);
@@ -170,30 +179,30 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
       const uint64_t k_desc = tc::sdesc(sbase + SK, 128, 2048);
       const uint64_t v_desc = tc::sdesc(sbase + SV, 2048, 128);
       auto issue_pv = [&](int j) {
-        const uint32_t pbuf = tmem + SP0 + (j & 1) * BN;
-        const uint64_t vb = v_desc + (((j & 1) * 16384) >> 4);
+        const uint32_t pbuf = tmem + SP0 + (j % NB) * BN;
+        const uint64_t vb = v_desc + (((j % NB) * 16384) >> 4);
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int ks = 0; ks < BN / 16; ++ks)
             mma_f16_ta(tmem, pbuf + part * (BN / 2) + ks * 8, vb + ((ks * 4096) >> 4), ID_PV,
                        j > 0 || part > 0 || ks > 0);
-        tc::mma_commit(&bars.pv[j & 1]);
+        tc::mma_commit(&bars.pv[j % NB]);
       };
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
-        ok = tc::mbar_wait(&bars.cv[j & 1], (j >> 1) & 1);
-        if (ok && j >= 2) ok = tc::mbar_wait(&bars.pv[j & 1], ((j - 2) >> 1) & 1);
+        ok = tc::mbar_wait(&bars.cv[j % NB], (j / NB) & 1);
+        if (ok && j >= NB) ok = tc::mbar_wait(&bars.pv[j % NB], ((j - NB) / NB) & 1);
         if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t sbuf = tmem + SP0 + (j & 1) * BN;
-        const uint64_t kb = k_desc + (((j & 1) * 16384) >> 4);
+        const uint32_t sbuf = tmem + SP0 + (j % NB) * BN;
+        const uint64_t kb = k_desc + (((j % NB) * 16384) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           tc::mma_f16(sbuf, q_desc + ((ks * 4096) >> 4), kb + ((ks * 256) >> 4), ID_S, ks > 0);
-        tc::mma_commit(&bars.sf[j & 1]);
+        tc::mma_commit(&bars.sf[j % NB]);
         if (j >= 1) {
-          ok = tc::mbar_wait(&bars.pf[(j - 1) & 1], ((j - 1) >> 1) & 1);
+          ok = tc::mbar_wait(&bars.pf[(j - 1) % NB], ((j - 1) / NB) & 1);
           if (!ok) break;
           tc::fence_after_sync();
           issue_pv(j - 1);
@@ -201,7 +210,7 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
       }
       if (ok && n_tiles > 0) {
         const int j = n_tiles - 1;
-        ok = tc::mbar_wait(&bars.pf[j & 1], (j >> 1) & 1);
+        ok = tc::mbar_wait(&bars.pf[j % NB], (j / NB) & 1);
         if (ok) {
           tc::fence_after_sync();
           issue_pv(j);
@@ -217,68 +226,75 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
     const int8_t *src = (is_v ? a.v : a.k) + static_cast<int64_t>(hk) * D;
     const uint16_t *ssrc = (is_v ? a.v_scale : a.k_scale) + hk;
     const int64_t row_stride = static_cast<int64_t>(a.n_kv_heads) * D;
-    // cell of this thread's key in tile j, -1 if beyond kv_hi or out of range (a zero row)
-    auto cell_of = [&](int j) -> int64_t {
+    // Loaded values are only read one or more tiles after their load (the loop is
+    // unrolled by RING, so the per-tile registers rotate by renaming, not by moves
+    // that would wait for the load): a thread never stalls on a global load.
+    static_assert(RING == 4 && LOOK == 3, "register rotation below assumes a 4-deep ring");
+    auto cell_load = [&](int j) -> int64_t {       // raw cell id of this thread's key in tile j, or -1
       const int64_t t = static_cast<int64_t>(j) * BN + key;
-      if (j >= n_tiles || t >= kv_hi) return -1;
-      const int64_t c = __ldg(a.cell_of_pos + t);
-      if (c < 0 || c >= a.n_cells) {
-        if (!is_v) set_status(a.status, TQ_ERR_DEVICE_CHECK);
-        return -1;
-      }
-      return c;
+      return (j < n_tiles && t < kv_hi) ? static_cast<int64_t>(__ldg(a.cell_of_pos + t)) : -1;
     };
+    auto cell_ok = [&](int64_t c) { return c >= 0 && c < a.n_cells; };
     auto fetch = [&](int j, int64_t c) {          // this thread's row of tile j -> ring slot j % RING
+      const int64_t t = static_cast<int64_t>(j) * BN + key;
+      const bool ok = cell_ok(c);
+      if (!ok && t < kv_hi && !is_v) set_status(a.status, TQ_ERR_DEVICE_CHECK);   // a zero row
       unsigned char *dst = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
-      const int8_t *p = (c >= 0) ? src + c * row_stride : src;
-      const uint32_t nb = (c >= 0) ? 16u : 0u;
+      const int8_t *p = ok ? src + c * row_stride : src;
+      const uint32_t nb = ok ? 16u : 0u;
 #pragma unroll
       for (int i = 0; i < D / 16; ++i) cp_async16(dst + 16 * i, p + 16 * i, nb);
     };
-    // cells of tiles 0 .. LOOK (registers cN[k] = cell of tile j + k at iteration j)
-    int64_t cN[LOOK + 1];
+    auto scale_load = [&](int64_t c) -> float {
+      return cell_ok(c) ? __half2float(__ushort_as_half(__ldg(ssrc + c * a.n_kv_heads))) : 0.f;
+    };
+    int64_t cb[RING];                             // cb[t % RING]: cell of tile t (t = j .. j + LOOK)
+    float sb[RING];                               // sb[t % RING]: scale of tile t (t = j, j + 1)
 #pragma unroll
-    for (int k = 0; k <= LOOK; ++k) cN[k] = cell_of(k);
+    for (int k = 0; k < RING; ++k) cb[k] = cell_load(k);
 #pragma unroll
     for (int k = 0; k < LOOK; ++k) {
-      fetch(k, cN[k]);
+      fetch(k, cb[k]);
       cp_async_commit();
     }
-    float sc_cur = (cN[0] >= 0) ? __half2float(__ushort_as_half(__ldg(ssrc + cN[0] * a.n_kv_heads))) : 0.f;
+    sb[0] = scale_load(cb[0]);
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      // copies LOOK tiles ahead, the next cell id one step further, the next scale
-      const int64_t c_far = cell_of(j + LOOK + 1);
-      if (j + LOOK < n_tiles) fetch(j + LOOK, cN[LOOK]);
-      cp_async_commit();
-      const float sc_next =
-          (cN[1] >= 0) ? __half2float(__ushort_as_half(__ldg(ssrc + cN[1] * a.n_kv_heads))) : 0.f;
-      cp_async_wait<LOOK>();                        // this thread's row of tile j has landed
-      // K'/V' buffer j & 1 is free once PV_{j-2} is done
-      if (j >= 2) ok = tc::mbar_wait(&bars.pv[j & 1], ((j - 2) >> 1) & 1);
-      if (!__all_sync(0xffffffffu, ok)) { s_fail = 1; break; }
-      tc::fence_after_sync();
-      const unsigned char *rw = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
-      unsigned char *dst = smem + (is_v ? SV : SK) + (j & 1) * 16384 + (key >> 3) * 2048 + (key & 7) * 16;
+    for (int j0 = 0; j0 < n_tiles && ok; j0 += RING) {
 #pragma unroll
-      for (int i = 0; i < D / 16; ++i) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(rw + 16 * i);
-        uint4 o0, o1;
-        i8x4_to_h(w.x, o0.x, o0.y);
-        i8x4_to_h(w.y, o0.z, o0.w);
-        i8x4_to_h(w.z, o1.x, o1.y);
-        i8x4_to_h(w.w, o1.z, o1.w);
-        *reinterpret_cast<uint4 *>(dst + (2 * i) * 128) = o0;          // dims 16 i .. 16 i + 7
-        *reinterpret_cast<uint4 *>(dst + (2 * i + 1) * 128) = o1;      // dims 16 i + 8 .. 16 i + 15
+      for (int u = 0; u < RING; ++u) {
+        const int j = j0 + u;
+        if (j >= n_tiles) break;
+        // tile j + LOOK's copies (its cell was loaded a tile ago), tile j + 1's scale,
+        // then tile j + RING's cell into the slot tile j no longer needs
+        if (j + LOOK < n_tiles) fetch(j + LOOK, cb[(u + LOOK) % RING]);
+        cp_async_commit();
+        sb[(u + 1) % RING] = scale_load(cb[(u + 1) % RING]);
+        const float sc_j = sb[u];
+        cb[u] = cell_load(j + RING);
+        cp_async_wait<LOOK>();                      // this thread's row of tile j has landed
+        // K'/V' buffer j % NB is free once PV_{j-NB} is done
+        if (j >= NB) ok = tc::mbar_wait(&bars.pv[j % NB], ((j - NB) / NB) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; s_fail = 1; break; }
+        tc::fence_after_sync();
+        const unsigned char *rw = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
+        unsigned char *dst = smem + (is_v ? SV : SK) + (j % NB) * 16384 + (key >> 3) * 2048 + (key & 7) * 16;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          const uint4 w = *reinterpret_cast<const uint4 *>(rw + 16 * i);
+          uint4 o0, o1;
+          i8x4_to_h(w.x, o0.x, o0.y);
+          i8x4_to_h(w.y, o0.z, o0.w);
+          i8x4_to_h(w.z, o1.x, o1.y);
+          i8x4_to_h(w.w, o1.z, o1.w);
+          *reinterpret_cast<uint4 *>(dst + (2 * i) * 128) = o0;          // dims 16 i .. 16 i + 7
+          *reinterpret_cast<uint4 *>(dst + (2 * i + 1) * 128) = o1;      // dims 16 i + 8 .. 16 i + 15
+        }
+        // k scales pre-multiplied by scale * log2(e): the softmax does one multiply per score
+        scl[((j % NB) * BN + key) * 2 + (is_v ? 1 : 0)] = is_v ? sc_j : sc_j * a.scale_log2;
+        tc::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.cv[j % NB]);
       }
-      scl[((j & 1) * BN + key) * 2 + (is_v ? 1 : 0)] = sc_cur;
-      tc::fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.cv[j & 1]);
-      sc_cur = sc_next;
-#pragma unroll
-      for (int k = 0; k < LOOK; ++k) cN[k] = cN[k + 1];
-      cN[LOOK] = c_far;
     }
     cp_async_wait<0>();
   } else {
@@ -286,12 +302,12 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
     const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      ok = tc::mbar_wait(&bars.sf[j & 1], (j >> 1) & 1);
-      if (ok) ok = tc::mbar_wait(&bars.cv[j & 1], (j >> 1) & 1);      // scales of tile j are written
+      ok = tc::mbar_wait(&bars.sf[j % NB], (j / NB) & 1);
+      if (ok) ok = tc::mbar_wait(&bars.cv[j % NB], (j / NB) & 1);      // scales of tile j are written
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc::fence_after_sync();
-      const uint32_t sbuf = tmem + lane_off + SP0 + (j & 1) * BN;
-      const float *sc = scl + (j & 1) * BN * 2;
+      const uint32_t sbuf = tmem + lane_off + SP0 + (j % NB) * BN;
+      const float *sc = scl + (j % NB) * BN * 2;
       float s[BN];
       {
         uint32_t r0[BN];
@@ -299,65 +315,74 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
         tc::tmem_ld32(sbuf + 32, r0 + 32);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r0[i]) * (sc[2 * i] * a.scale_log2);
+        for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r0[i]) * sc[2 * i];
       }
       const int64_t key0 = static_cast<int64_t>(j) * BN;
       const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(BN, row_end - key0))) : 0;
-      float mt = -INFINITY;
+      const bool full_tile = __all_sync(0xffffffffu, nvis == BN);     // no mask in this warp
+      if (!full_tile) {
 #pragma unroll
-      for (int i = 0; i < BN; ++i)
-        if (i < nvis) mt = fmaxf(mt, s[i]);
+        for (int i = 0; i < BN; ++i)
+          if (i >= nvis) s[i] = -INFINITY;
+      }
+      // four independent chains for the maximum (and the sum below)
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const bool raise = mt > m_used + 8.f || (m_used == -INFINITY && mt > -INFINITY);
       const float fct = (raise && m_used != -INFINITY) ? exp2f(m_used - mt) : 1.f;
       if (raise) m_used = mt;
       if (__any_sync(0xffffffffu, fct != 1.f)) {
         // O must be stable: wait for the PV mma of the previous tile
-        bool okp = (j == 0) || tc::mbar_wait(&bars.pv[(j - 1) & 1], ((j - 1) >> 1) & 1);
+        bool okp = (j == 0) || tc::mbar_wait(&bars.pv[(j - 1) % NB], ((j - 1) / NB) & 1);
         if (!__all_sync(0xffffffffu, okp)) { ok = false; break; }
         tc::fence_after_sync();
         l_sum *= fct;
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t r[32];
-          tc::tmem_ld32(tmem + lane_off + c, r);
+#pragma unroll 1
+        for (int c = 0; c < D; c += 16) {          // 16 columns at a time: s[] is live here
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_off + c, r);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * fct);
-          tc::tmem_st32(tmem + lane_off + c, r);
+          for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * fct);
+          tmem_st16(tmem + lane_off + c, r);
         }
       }
-      float psum = 0.f;
+      // P' = p * scale_v as binary16 (hi, lo) key pairs over S_j (row = lane), 32 keys
+      // at a time.  Every scale of the tile is finite (0 beyond kv_hi and for
+      // rejected cells); a row with nothing visible yet has m_used = -inf and p = 0.
+      const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < BN; ++i) {
-        s[i] = (i < nvis) ? tc::ex2(s[i] - m_used) : 0.f;
-        psum += s[i];
-      }
-      l_sum += psum;
-      // P' = p * scale_v as binary16 (hi, lo) key pairs over S_j: row = lane
-      uint32_t ph[BN / 2], pl[BN / 2];
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t ph[16], pl[16];
 #pragma unroll
-      for (int i = 0; i < BN / 2; ++i) {
-        const int k0 = 2 * i;
-        // masked keys may carry garbage scales: select, never multiply, a zero
-        const float x0 = s[k0] > 0.f ? s[k0] * sc[2 * k0 + 1] : 0.f;
-        const float x1 = s[k0 + 1] > 0.f ? s[k0 + 1] * sc[2 * (k0 + 1) + 1] : 0.f;
-        const __half2 h = __floats2half2_rn(x0, x1);
-        const float2 hf = __half22float2(h);
-        const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-        ph[i] = *reinterpret_cast<const uint32_t *>(&h);
-        pl[i] = *reinterpret_cast<const uint32_t *>(&l);
+        for (int i = 0; i < 16; ++i) {
+          const int k0 = 32 * ch + 2 * i;
+          const float p0 = tc::ex2(s[k0] - m_ref), p1 = tc::ex2(s[k0 + 1] - m_ref);     // masked: 0
+          ps[i & 3] += p0 + p1;
+          const float x0 = p0 * sc[2 * k0 + 1];
+          const float x1 = p1 * sc[2 * (k0 + 1) + 1];
+          const __half2 h = __floats2half2_rn(x0, x1);
+          const float2 hf = __half22float2(h);
+          const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+          ph[i] = *reinterpret_cast<const uint32_t *>(&h);
+          pl[i] = *reinterpret_cast<const uint32_t *>(&l);
+        }
+        tmem_st16(sbuf + 16 * ch, ph);
+        tmem_st16(sbuf + BN / 2 + 16 * ch, pl);
       }
-      tc::tmem_st32(sbuf, ph);
-      tc::tmem_st32(sbuf + BN / 2, pl);
+      l_sum += (ps[0] + ps[1]) + (ps[2] + ps[3]);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.pf[j & 1]);
+      if (lane == 0) mbar_arrive(&bars.pf[j % NB]);
     }
     // the last PV must be complete before O is read
     if (ok && n_tiles > 0) {
       const int j = n_tiles - 1;
-      ok = tc::mbar_wait(&bars.pv[j & 1], (j >> 1) & 1);
+      ok = tc::mbar_wait(&bars.pv[j % NB], (j / NB) & 1);
       ok = __all_sync(0xffffffffu, ok);
       tc::fence_after_sync();
     }
