@@ -242,8 +242,10 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
       unsigned char *dst = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
       const int8_t *p = ok ? src + c * row_stride : src;
       const uint32_t nb = ok ? 16u : 0u;
+      // 16-byte chunk i of the row sits in slot i ^ (key & 7): the lanes of a warp
+      // (consecutive keys, rows 128 bytes apart) then hit different banks
 #pragma unroll
-      for (int i = 0; i < D / 16; ++i) cp_async16(dst + 16 * i, p + 16 * i, nb);
+      for (int i = 0; i < D / 16; ++i) cp_async16(dst + 16 * (i ^ (key & 7)), p + 16 * i, nb);
     };
     auto scale_load = [&](int64_t c) -> float {
       return cell_ok(c) ? __half2float(__ushort_as_half(__ldg(ssrc + c * a.n_kv_heads))) : 0.f;
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
         unsigned char *dst = smem + (is_v ? SV : SK) + (j % NB) * 16384 + (key >> 3) * 2048 + (key & 7) * 16;
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) {
-          const uint4 w = *reinterpret_cast<const uint4 *>(rw + 16 * i);
+          const uint4 w = *reinterpret_cast<const uint4 *>(rw + 16 * (i ^ (key & 7)));
           uint4 o0, o1;
           i8x4_to_h(w.x, o0.x, o0.y);
           i8x4_to_h(w.y, o0.z, o0.w);
