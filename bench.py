@@ -510,6 +510,25 @@ def run_int8_extra(tq, torch, dev, tflops_peak, ctx=140000, nq=2048):
             "algorithmic_GFLOP": flop / 1e9}
 
 
+def run_f16_prompt_extra(tq, torch, dev, tflops_peak, ctx=40000, nq=2048):
+    """Prompt attention over binary16 rows (the int8 path's other cache mode)."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20265)
+    HK, HQ, DD = 8, 32, 128
+    k = _device_gaussian(torch, gen, (ctx, HK, DD), dev).to(torch.float16)
+    v = _device_gaussian(torch, gen, (ctx, HK, DD), dev).to(torch.float16)
+    perm = torch.randperm(ctx, generator=gen, device=dev).to(torch.int32)
+    q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.float16)
+    out = torch.empty((nq, HQ, DD), device=dev)
+    ws = tq.workspace(tq._lib.tq_int8_prompt_attn_workspace(nq, HQ, HK, DD, ctx), dev)
+    t = time_graph(torch, lambda: tq.f16_prompt_attn(k, v, perm, ctx, q, out=out, ws=ws), reps=3)
+    pairs = sum(min(ctx, ctx - nq + i + 1) for i in range(nq))
+    flop = 4.0 * DD * pairs * HQ
+    return {"workload": f"f16_prompt: 8 KV x 32 Q heads, D=128, {nq} queries, ctx {ctx} scattered binary16 rows",
+            "ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
+            "algorithmic_GFLOP": flop / 1e9}
+
+
 def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak, tflops_peak):
     """Other rows of the hot path, measured on their own workloads."""
     ex = {}
@@ -523,6 +542,7 @@ def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv
                            "ms": t * 1e3, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak}
     ex["prefill"] = run_prefill_extra(tq, torch, dev, tflops_peak)
     ex["int8_prompt"] = run_int8_extra(tq, torch, dev, tflops_peak)
+    ex["f16_prompt"] = run_f16_prompt_extra(tq, torch, dev, tflops_peak)
     return ex
 
 

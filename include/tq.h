@@ -248,6 +248,17 @@ tq_status tq_int8_prompt_attn(const int8_t *k, const uint16_t *k_scale, const in
                               int n_kv_heads, int head_dim, float scale, int causal, float *out,
                               void *workspace, size_t workspace_bytes, tq_stream stream);
 
+/* The same prompt attention over a binary16 KV cache (the other cache mode of
+ * [QSA#1821], whose output checksums the page compares alongside int8): rows
+ *   k_t = k[cell_of_pos[t]][hk][:],  v_t = v[cell_of_pos[t]][hk][:]   (no scales)
+ * k, v   device binary16 [n_cells][n_kv_heads][head_dim], 16-byte aligned
+ * Other arguments, the workspace (tq_int8_prompt_attn_workspace), results and
+ * errors as tq_int8_prompt_attn. */
+tq_status tq_f16_prompt_attn(const uint16_t *k, const uint16_t *v, int64_t n_cells,
+                             const int32_t *cell_of_pos, int64_t ctx, const uint16_t *q, int nq,
+                             int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
+                             float *out, void *workspace, size_t workspace_bytes, tq_stream stream);
+
 /* Reads (and clears) the device status word kept in a workspace of the
  * calls above: waits for `stream`, so it must not be called while the stream
  * is being captured.  *status_out receives TQ_OK or the first device-side

@@ -428,6 +428,28 @@ def int8_prompt_attn(k_i8, k_scale, v_i8, v_scale, cell_of_pos, ctx: int,
     return out
 
 
+def f16_prompt_attn(k_bits, v_bits, cell_of_pos, ctx: int, q: np.ndarray, scale: float, causal: bool = True,
+                    rows: np.ndarray | None = None) -> np.ndarray:
+    """The other cache mode of [QSA#1821] ("Measured": output checksums for int8
+    and fp16): the same attention with rows k, v read as binary16 values
+    [n_cells][Hkv][D] (uint16 bit patterns), no scales."""
+    nq, n_q, _ = q.shape
+    kv = np.asarray(k_bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+    vv = np.asarray(v_bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+    hkv = kv.shape[1]
+    g = n_q // hkv
+    rows = np.arange(nq) if rows is None else np.asarray(rows)
+    pos = (ctx - nq + rows) if causal else None
+    cells = np.asarray(cell_of_pos[:ctx], dtype=np.int64)
+    out = np.zeros((nq, n_q, vv.shape[2]))
+    for hk in range(hkv):
+        k = kv[cells, hk]
+        v = vv[cells, hk]
+        for h in range(hk * g, (hk + 1) * g):
+            out[rows, h] = softmax_attention(q[rows, h], k, v, scale, pos)
+    return out
+
+
 def nmse(a: np.ndarray, b: np.ndarray) -> float:
     """sum (a - b)^2 / sum b^2, b the reference ([HIP#28 "Correctness"])."""
     a = np.asarray(a, np.float64)

@@ -133,3 +133,23 @@ def int8_prompt_attn(k, k_scale, v, v_scale, cell_of_pos, ctx: int, q, scale: fl
                                   _stream(stream))
     _lib.check("tq_int8_prompt_attn", st)
     return out
+
+
+def f16_prompt_attn(k, v, cell_of_pos, ctx: int, q, scale: float | None = None, causal: bool = True, out=None,
+                    ws=None, stream=None):
+    """Prompt attention over binary16 K/V rows [n_cells][n_kv_heads][128] gathered
+    through cell_of_pos (the int8 path's other cache mode, no scales)."""
+    torch = _torch()
+    assert k.dtype == torch.float16 and v.dtype == torch.float16
+    n_cells, n_kv, d = k.shape
+    nq, n_q, _ = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if out is None:
+        out = torch.empty((nq, n_q, d), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(_lib.tq_int8_prompt_attn_workspace(nq, n_q, n_kv, d, ctx), q.device)
+    st = _lib.tq_f16_prompt_attn(k.data_ptr(), v.data_ptr(), n_cells, cell_of_pos.data_ptr(), ctx, q.data_ptr(),
+                                 nq, n_q, n_kv, d, scale, int(causal), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                 _stream(stream))
+    _lib.check("tq_f16_prompt_attn", st)
+    return out

@@ -79,6 +79,8 @@ _SIGS = {
     "tq_int8_prompt_attn_workspace": (C.c_size_t, [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int64]),
     "tq_int8_prompt_attn": (C.c_int, [_P, _P, _P, _P, C.c_int64, _P, C.c_int64, _P, C.c_int, C.c_int,
                                       C.c_int, C.c_int, C.c_float, C.c_int, _P, _P, C.c_size_t, _P]),
+    "tq_f16_prompt_attn": (C.c_int, [_P, _P, C.c_int64, _P, C.c_int64, _P, C.c_int, C.c_int, C.c_int, C.c_int,
+                                     C.c_float, C.c_int, _P, _P, C.c_size_t, _P]),
     "tq_workspace_status": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_int32), _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -176,6 +178,13 @@ def tq_int8_prompt_attn(k: int, k_scale: int, v: int, v_scale: int, n_cells: int
     return lib.tq_int8_prompt_attn(k, k_scale, v, v_scale, n_cells, cell_of_pos, ctx, q, nq,
                                    n_q_heads, n_kv_heads, head_dim, scale, causal, out, ws, ws_bytes,
                                    stream)
+
+
+def tq_f16_prompt_attn(k: int, v: int, n_cells: int, cell_of_pos: int, ctx: int, q: int, nq: int,
+                       n_q_heads: int, n_kv_heads: int, head_dim: int, scale: float, causal: int, out: int,
+                       ws: int, ws_bytes: int, stream: int | None) -> int:
+    return lib.tq_f16_prompt_attn(k, v, n_cells, cell_of_pos, ctx, q, nq, n_q_heads, n_kv_heads, head_dim,
+                                  scale, causal, out, ws, ws_bytes, stream)
 
 
 def tq_workspace_status(ws: int, ws_bytes: int, stream: int | None) -> int:

@@ -40,6 +40,7 @@ struct Int8Args {
   int64_t n_cells;
   int64_t ctx;
   int32_t nq, n_q_heads, n_kv_heads, group, causal;
+  int32_t f16;            // rows are binary16 (k, v hold uint16), no scales
   float scale_log2;
 };
 
@@ -122,7 +123,10 @@ struct Bars {               // buffer j % NB, phase (j / NB) & 1
   uint64_t pv[NB];         // PV_j computed (mma commit)
 };
 
-__global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
+// F16 = false: int8 rows with binary16 scales; true: binary16 rows, no scales
+// (the second cache mode of the same prompt attention).
+template <bool F16>
+__global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_slot;
@@ -223,79 +227,138 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
     const int gt = tid - 128;                     // 0..127
     const bool is_v = gt >= BN;
     const int key = gt & (BN - 1);
-    const int8_t *src = (is_v ? a.v : a.k) + static_cast<int64_t>(hk) * D;
-    const uint16_t *ssrc = (is_v ? a.v_scale : a.k_scale) + hk;
-    const int64_t row_stride = static_cast<int64_t>(a.n_kv_heads) * D;
-    // Loaded values are only read one or more tiles after their load (the loop is
-    // unrolled by RING, so the per-tile registers rotate by renaming, not by moves
-    // that would wait for the load): a thread never stalls on a global load.
-    static_assert(RING == 4 && LOOK == 3, "register rotation below assumes a 4-deep ring");
-    auto cell_load = [&](int j) -> int64_t {       // raw cell id of this thread's key in tile j, or -1
-      const int64_t t = static_cast<int64_t>(j) * BN + key;
-      return (j < n_tiles && t < kv_hi) ? static_cast<int64_t>(__ldg(a.cell_of_pos + t)) : -1;
-    };
-    auto cell_ok = [&](int64_t c) { return c >= 0 && c < a.n_cells; };
-    auto fetch = [&](int j, int64_t c) {          // this thread's row of tile j -> ring slot j % RING
-      const int64_t t = static_cast<int64_t>(j) * BN + key;
-      const bool ok = cell_ok(c);
-      if (!ok && t < kv_hi && !is_v) set_status(a.status, TQ_ERR_DEVICE_CHECK);   // a zero row
-      unsigned char *dst = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
-      const int8_t *p = ok ? src + c * row_stride : src;
-      const uint32_t nb = ok ? 16u : 0u;
-      // 16-byte chunk i of the row sits in slot i ^ (key & 7): the lanes of a warp
-      // (consecutive keys, rows 128 bytes apart) then hit different banks
-#pragma unroll
-      for (int i = 0; i < D / 16; ++i) cp_async16(dst + 16 * (i ^ (key & 7)), p + 16 * i, nb);
-    };
-    auto scale_load = [&](int64_t c) -> float {
-      return cell_ok(c) ? __half2float(__ushort_as_half(__ldg(ssrc + c * a.n_kv_heads))) : 0.f;
-    };
-    int64_t cb[RING];                             // cb[t % RING]: cell of tile t (t = j .. j + LOOK)
-    float sb[RING];                               // sb[t % RING]: scale of tile t (t = j, j + 1)
-#pragma unroll
-    for (int k = 0; k < RING; ++k) cb[k] = cell_load(k);
-#pragma unroll
-    for (int k = 0; k < LOOK; ++k) {
-      fetch(k, cb[k]);
-      cp_async_commit();
-    }
-    sb[0] = scale_load(cb[0]);
-    bool ok = true;
-    for (int j0 = 0; j0 < n_tiles && ok; j0 += RING) {
-#pragma unroll
-      for (int u = 0; u < RING; ++u) {
-        const int j = j0 + u;
-        if (j >= n_tiles) break;
-        // tile j + LOOK's copies (its cell was loaded a tile ago), tile j + 1's scale,
-        // then tile j + RING's cell into the slot tile j no longer needs
-        if (j + LOOK < n_tiles) fetch(j + LOOK, cb[(u + LOOK) % RING]);
-        cp_async_commit();
-        sb[(u + 1) % RING] = scale_load(cb[(u + 1) % RING]);
-        const float sc_j = sb[u];
-        cb[u] = cell_load(j + RING);
-        cp_async_wait<LOOK>();                      // this thread's row of tile j has landed
-        // K'/V' buffer j % NB is free once PV_{j-NB} is done
-        if (j >= NB) ok = tc::mbar_wait(&bars.pv[j % NB], ((j - NB) / NB) & 1);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; s_fail = 1; break; }
-        tc::fence_after_sync();
-        const unsigned char *rw = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
+    if constexpr (F16) {
+      // binary16 rows are operand-ready: each 16-byte chunk (8 dims) is copied
+      // straight to its core-matrix slot of the K'/V' tile, LOOK16 tiles ahead,
+      // once that tile's buffer is free (PV of the tile NB before it is done)
+      constexpr int LOOK16 = NB - 1;
+      const uint8_t *src = reinterpret_cast<const uint8_t *>(is_v ? a.v : a.k) + static_cast<int64_t>(hk) * D * 2;
+      const int64_t row_stride = static_cast<int64_t>(a.n_kv_heads) * D * 2;
+      auto cell_load = [&](int j) -> int64_t {
+        const int64_t t = static_cast<int64_t>(j) * BN + key;
+        return (j < n_tiles && t < kv_hi) ? static_cast<int64_t>(__ldg(a.cell_of_pos + t)) : -1;
+      };
+      auto fetch = [&](int j, int64_t c) {
+        const int64_t t = static_cast<int64_t>(j) * BN + key;
+        const bool okc = c >= 0 && c < a.n_cells;
+        if (!okc && t < kv_hi && !is_v) set_status(a.status, TQ_ERR_DEVICE_CHECK);   // a zero row
         unsigned char *dst = smem + (is_v ? SV : SK) + (j % NB) * 16384 + (key >> 3) * 2048 + (key & 7) * 16;
+        const uint8_t *p = okc ? src + c * row_stride : src;
+        const uint32_t nb = okc ? 16u : 0u;
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-          const uint4 w = *reinterpret_cast<const uint4 *>(rw + 16 * (i ^ (key & 7)));
-          uint4 o0, o1;
-          i8x4_to_h(w.x, o0.x, o0.y);
-          i8x4_to_h(w.y, o0.z, o0.w);
-          i8x4_to_h(w.z, o1.x, o1.y);
-          i8x4_to_h(w.w, o1.z, o1.w);
-          *reinterpret_cast<uint4 *>(dst + (2 * i) * 128) = o0;          // dims 16 i .. 16 i + 7
-          *reinterpret_cast<uint4 *>(dst + (2 * i + 1) * 128) = o1;      // dims 16 i + 8 .. 16 i + 15
+        for (int i = 0; i < D / 8; ++i) cp_async16(dst + i * 128, p + 16 * i, nb);
+      };
+      // constant scales: k * scale * log2(e), v * 1, for every buffer
+      for (int i = gt; i < NB * BN; i += 128) {
+        scl[2 * i] = a.scale_log2;
+        scl[2 * i + 1] = 1.f;
+      }
+      int64_t cb[RING];                           // cb[t % RING]: cell of tile t
+#pragma unroll
+      for (int k = 0; k < RING; ++k) cb[k] = cell_load(k);
+#pragma unroll
+      for (int k = 0; k < LOOK16; ++k) {
+        if (k < n_tiles) fetch(k, cb[k]);
+        cp_async_commit();
+      }
+      bool ok = true;
+      for (int j0 = 0; j0 < n_tiles && ok; j0 += RING) {
+#pragma unroll
+        for (int u = 0; u < RING; ++u) {
+          const int j = j0 + u;
+          if (j >= n_tiles) break;
+          // tile j first: the control thread issues PV_{j-1} only after S_j, so
+          // tile j must be published before this thread waits for PV_{j-1}
+          cp_async_wait<LOOK16 - 1>();              // this thread's row of tile j has landed
+          tc::fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.cv[j % NB]);
+          const int jn = j + LOOK16;                // its buffer was used by tile jn - NB = j - 1
+          if (jn < n_tiles) {
+            if (jn >= NB) ok = tc::mbar_wait(&bars.pv[(jn - NB) % NB], ((jn - NB) / NB) & 1);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; s_fail = 1; break; }
+            tc::fence_after_sync();
+            fetch(jn, cb[(u + LOOK16) % RING]);
+          }
+          cp_async_commit();
+          cb[u] = cell_load(j + RING);
         }
-        // k scales pre-multiplied by scale * log2(e): the softmax does one multiply per score
-        scl[((j % NB) * BN + key) * 2 + (is_v ? 1 : 0)] = is_v ? sc_j : sc_j * a.scale_log2;
-        tc::fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.cv[j % NB]);
+      }
+    } else {
+      const int8_t *src = (is_v ? a.v : a.k) + static_cast<int64_t>(hk) * D;
+      const uint16_t *ssrc = (is_v ? a.v_scale : a.k_scale) + hk;
+      const int64_t row_stride = static_cast<int64_t>(a.n_kv_heads) * D;
+      // Loaded values are only read one or more tiles after their load (the loop is
+      // unrolled by RING, so the per-tile registers rotate by renaming, not by moves
+      // that would wait for the load): a thread never stalls on a global load.
+      static_assert(RING == 4 && LOOK == 3, "register rotation below assumes a 4-deep ring");
+      auto cell_load = [&](int j) -> int64_t {       // raw cell id of this thread's key in tile j, or -1
+        const int64_t t = static_cast<int64_t>(j) * BN + key;
+        return (j < n_tiles && t < kv_hi) ? static_cast<int64_t>(__ldg(a.cell_of_pos + t)) : -1;
+      };
+      auto cell_ok = [&](int64_t c) { return c >= 0 && c < a.n_cells; };
+      auto fetch = [&](int j, int64_t c) {          // this thread's row of tile j -> ring slot j % RING
+        const int64_t t = static_cast<int64_t>(j) * BN + key;
+        const bool ok = cell_ok(c);
+        if (!ok && t < kv_hi && !is_v) set_status(a.status, TQ_ERR_DEVICE_CHECK);   // a zero row
+        unsigned char *dst = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
+        const int8_t *p = ok ? src + c * row_stride : src;
+        const uint32_t nb = ok ? 16u : 0u;
+        // 16-byte chunk i of the row sits in slot i ^ (key & 7): the lanes of a warp
+        // (consecutive keys, rows 128 bytes apart) then hit different banks
+  #pragma unroll
+        for (int i = 0; i < D / 16; ++i) cp_async16(dst + 16 * (i ^ (key & 7)), p + 16 * i, nb);
+      };
+      auto scale_load = [&](int64_t c) -> float {
+        return cell_ok(c) ? __half2float(__ushort_as_half(__ldg(ssrc + c * a.n_kv_heads))) : 0.f;
+      };
+      int64_t cb[RING];                             // cb[t % RING]: cell of tile t (t = j .. j + LOOK)
+      float sb[RING];                               // sb[t % RING]: scale of tile t (t = j, j + 1)
+  #pragma unroll
+      for (int k = 0; k < RING; ++k) cb[k] = cell_load(k);
+  #pragma unroll
+      for (int k = 0; k < LOOK; ++k) {
+        fetch(k, cb[k]);
+        cp_async_commit();
+      }
+      sb[0] = scale_load(cb[0]);
+      bool ok = true;
+      for (int j0 = 0; j0 < n_tiles && ok; j0 += RING) {
+  #pragma unroll
+        for (int u = 0; u < RING; ++u) {
+          const int j = j0 + u;
+          if (j >= n_tiles) break;
+          // tile j + LOOK's copies (its cell was loaded a tile ago), tile j + 1's scale,
+          // then tile j + RING's cell into the slot tile j no longer needs
+          if (j + LOOK < n_tiles) fetch(j + LOOK, cb[(u + LOOK) % RING]);
+          cp_async_commit();
+          sb[(u + 1) % RING] = scale_load(cb[(u + 1) % RING]);
+          const float sc_j = sb[u];
+          cb[u] = cell_load(j + RING);
+          cp_async_wait<LOOK>();                      // this thread's row of tile j has landed
+          // K'/V' buffer j % NB is free once PV_{j-NB} is done
+          if (j >= NB) ok = tc::mbar_wait(&bars.pv[j % NB], ((j - NB) / NB) & 1);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; s_fail = 1; break; }
+          tc::fence_after_sync();
+          const unsigned char *rw = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
+          unsigned char *dst = smem + (is_v ? SV : SK) + (j % NB) * 16384 + (key >> 3) * 2048 + (key & 7) * 16;
+  #pragma unroll
+          for (int i = 0; i < D / 16; ++i) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(rw + 16 * (i ^ (key & 7)));
+            uint4 o0, o1;
+            i8x4_to_h(w.x, o0.x, o0.y);
+            i8x4_to_h(w.y, o0.z, o0.w);
+            i8x4_to_h(w.z, o1.x, o1.y);
+            i8x4_to_h(w.w, o1.z, o1.w);
+            *reinterpret_cast<uint4 *>(dst + (2 * i) * 128) = o0;          // dims 16 i .. 16 i + 7
+            *reinterpret_cast<uint4 *>(dst + (2 * i + 1) * 128) = o1;      // dims 16 i + 8 .. 16 i + 15
+          }
+          // k scales pre-multiplied by scale * log2(e): the softmax does one multiply per score
+          scl[((j % NB) * BN + key) * 2 + (is_v ? 1 : 0)] = is_v ? sc_j : sc_j * a.scale_log2;
+          tc::fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.cv[j % NB]);
+        }
       }
     }
     cp_async_wait<0>();
@@ -426,12 +489,13 @@ __global__ void __launch_bounds__(NT, 1) int8_attn_kernel(const Int8Args a) {
 
 cudaError_t launch_int8_attn(const Int8Args &a, cudaStream_t s) {
   static_assert(i8::TOTAL <= 227 * 1024, "shared memory");
-  cudaError_t e = cudaFuncSetAttribute(i8::int8_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = a.f16 ? i8::prompt_attn_kernel<true> : i8::prompt_attn_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)i8::TOTAL);
   if (e != cudaSuccess) return e;
   const int rows = a.nq * a.group;
   dim3 grid((rows + i8::BM - 1) / i8::BM, a.n_kv_heads);
-  i8::int8_attn_kernel<<<grid, i8::NT, i8::TOTAL, s>>>(a);
+  kern<<<grid, i8::NT, i8::TOTAL, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -444,11 +508,10 @@ extern "C" size_t tq_int8_prompt_attn_workspace(int nq, int n_q_heads, int n_kv_
   return 256;    // the status word
 }
 
-extern "C" tq_status tq_int8_prompt_attn(const int8_t *k, const uint16_t *k_scale, const int8_t *v,
-                                         const uint16_t *v_scale, int64_t n_cells, const int32_t *cell_of_pos,
-                                         int64_t ctx, const uint16_t *q, int nq, int n_q_heads, int n_kv_heads,
-                                         int head_dim, float scale, int causal, float *out, void *workspace,
-                                         size_t workspace_bytes, tq_stream stream) {
+static tq_status prompt_attn_call(const void *k, const uint16_t *k_scale, const void *v, const uint16_t *v_scale,
+                                  bool f16, int64_t n_cells, const int32_t *cell_of_pos, int64_t ctx,
+                                  const uint16_t *q, int nq, int n_q_heads, int n_kv_heads, int head_dim, float scale,
+                                  int causal, float *out, void *workspace, size_t workspace_bytes, tq_stream stream) {
   auto al = [](const void *p, uintptr_t m) { return (reinterpret_cast<uintptr_t>(p) & (m - 1)) == 0; };
   if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
   const int group = n_q_heads / n_kv_heads;
@@ -461,14 +524,13 @@ extern "C" tq_status tq_int8_prompt_attn(const int8_t *k, const uint16_t *k_scal
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (ctx == 0) return cudaMemsetAsync(out, 0, sizeof(float) * nq * n_q_heads * head_dim, s) == cudaSuccess
                            ? TQ_OK : TQ_ERR_CUDA;
-  if (!k || !v || !al(k, 16) || !al(v, 16) || !k_scale || !v_scale || !al(k_scale, 2) || !al(v_scale, 2) ||
-      !cell_of_pos || !al(cell_of_pos, 4))
-    return TQ_ERR_INVALID_ARG;
+  if (!k || !v || !al(k, 16) || !al(v, 16) || !cell_of_pos || !al(cell_of_pos, 4)) return TQ_ERR_INVALID_ARG;
+  if (!f16 && (!k_scale || !v_scale || !al(k_scale, 2) || !al(v_scale, 2))) return TQ_ERR_INVALID_ARG;
   if (static_cast<int64_t>(nq) * group > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;
   Int8Args a;
-  a.k = k;
+  a.k = static_cast<const int8_t *>(k);
   a.k_scale = k_scale;
-  a.v = v;
+  a.v = static_cast<const int8_t *>(v);
   a.v_scale = v_scale;
   a.cell_of_pos = cell_of_pos;
   a.q = q;
@@ -481,6 +543,24 @@ extern "C" tq_status tq_int8_prompt_attn(const int8_t *k, const uint16_t *k_scal
   a.n_kv_heads = n_kv_heads;
   a.group = group;
   a.causal = causal ? 1 : 0;
+  a.f16 = f16 ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_int8_attn(a, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+}
+
+extern "C" tq_status tq_int8_prompt_attn(const int8_t *k, const uint16_t *k_scale, const int8_t *v,
+                                         const uint16_t *v_scale, int64_t n_cells, const int32_t *cell_of_pos,
+                                         int64_t ctx, const uint16_t *q, int nq, int n_q_heads, int n_kv_heads,
+                                         int head_dim, float scale, int causal, float *out, void *workspace,
+                                         size_t workspace_bytes, tq_stream stream) {
+  return prompt_attn_call(k, k_scale, v, v_scale, false, n_cells, cell_of_pos, ctx, q, nq, n_q_heads, n_kv_heads,
+                          head_dim, scale, causal, out, workspace, workspace_bytes, stream);
+}
+
+extern "C" tq_status tq_f16_prompt_attn(const uint16_t *k, const uint16_t *v, int64_t n_cells,
+                                        const int32_t *cell_of_pos, int64_t ctx, const uint16_t *q, int nq,
+                                        int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
+                                        float *out, void *workspace, size_t workspace_bytes, tq_stream stream) {
+  return prompt_attn_call(k, nullptr, v, nullptr, true, n_cells, cell_of_pos, ctx, q, nq, n_q_heads, n_kv_heads,
+                          head_dim, scale, causal, out, workspace, workspace_bytes, stream);
 }

@@ -340,6 +340,48 @@ def test_int8_dequantised_attention_and_permutation():
     assert np.all(np.abs(recon - raw) <= 0.5 * step[..., None] * (1 + 1e-3) + 1e-3 * np.abs(raw))
 
 
+def test_f16_prompt_attention_loops_and_causality():
+    # binary16 rows through a permutation: plain-loop attention over the gathered
+    # rows, the causal horizon of each query, and the non-causal case
+    n_cells, hkv, d, nq, hq = 24, 2, 128, 4, 4
+    kb = W.to_f16_bits(W.gaussian_with_outliers(9, W.S_K, W.S_K_OUT, n_cells, hkv, d))
+    vb = W.to_f16_bits(W.gaussian_with_outliers(9, W.S_V, W.S_V_OUT, n_cells, hkv, d))
+    perm = W.permutation(9, W.S_PERM, n_cells)
+    ctx = 20
+    q = W.normal(9, W.S_Q, nq * hq * d).reshape(nq, hq, d)
+    out = O.f16_prompt_attn(kb, vb, perm, ctx, q, 0.05, causal=True)
+    kf = kb.view(np.float16).astype(np.float64)
+    vf = vb.view(np.float16).astype(np.float64)
+    for i in range(nq):
+        p_i = ctx - nq + i                                  # keys 0..p_i are visible
+        for h in range(hq):
+            hk = h // (hq // hkv)
+            kk = [[kf[perm[t], hk, j] for j in range(d)] for t in range(p_i + 1)]
+            vv = [[vf[perm[t], hk, j] for j in range(d)] for t in range(p_i + 1)]
+            ref = _loop_attention(q[i:i + 1, h], kk, vv, 0.05)
+            assert np.allclose(out[i, h], ref[0], atol=1e-12)
+    full = O.f16_prompt_attn(kb, vb, perm, ctx, q, 0.05, causal=False)
+    kk = [[kf[perm[t], 0, j] for j in range(d)] for t in range(ctx)]
+    vv = [[vf[perm[t], 0, j] for j in range(d)] for t in range(ctx)]
+    assert np.allclose(full[0, 1], _loop_attention(q[0:1, 1], kk, vv, 0.05)[0], atol=1e-12)
+
+
+def test_f16_rows_of_integers_match_int8_rows_with_unit_scales():
+    # the two cache modes agree when the binary16 rows hold the int8 values and
+    # every scale is 1
+    n_cells, hkv, d = 16, 1, 128
+    raw = W.gaussian_with_outliers(10, W.S_K, W.S_K_OUT, n_cells, hkv, d)
+    ki, _ = W.int8_rows(raw)
+    vi, _ = W.int8_rows(W.gaussian_with_outliers(10, W.S_V, W.S_V_OUT, n_cells, hkv, d))
+    ones = W.to_f16_bits(np.ones((n_cells, hkv)))
+    q = W.normal(10, W.S_Q, 3 * 2 * d).reshape(3, 2, d) * 0.01
+    perm = W.permutation(10, W.S_PERM, n_cells)
+    a = O.int8_prompt_attn(ki, ones, vi, ones, perm, n_cells, q, 0.1)
+    b = O.f16_prompt_attn(W.to_f16_bits(ki.astype(np.float64)), W.to_f16_bits(vi.astype(np.float64)), perm,
+                          n_cells, q, 0.1)
+    assert np.allclose(a, b, atol=1e-12)
+
+
 def test_nmse_definition():
     b = np.array([1.0, 2.0, 2.0])
     a = b + np.array([0.0, 0.3, 0.0])
