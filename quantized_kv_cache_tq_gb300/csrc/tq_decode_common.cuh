@@ -33,14 +33,13 @@ template <int NT>
 __device__ void decode_merge(const DecodeArgs &a, int hk, float *smem) {
   __shared__ int s_last;
   // the CTA's partial stores are ordered before the counter update by the CTA
-  // barrier plus thread 0's release fence; the last CTA's acquire fence orders
-  // its loads of the other partials after it
+  // barrier and the release half of thread 0's acq_rel atomic; its acquire half
+  // orders the last CTA's loads of the other partials after it
   __syncthreads();
   if (threadIdx.x == 0) {
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    const int prev = atomicAdd(&a.counters[hk], 1);
+    int prev;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(a.counters + hk) : "memory");
     s_last = (prev == a.n_splits - 1);
-    if (s_last) asm volatile("fence.acq_rel.gpu;" ::: "memory");
   }
   __syncthreads();
   if (!s_last) return;
