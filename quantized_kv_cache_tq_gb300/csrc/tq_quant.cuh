@@ -68,6 +68,18 @@ __device__ __forceinline__ int sg_bit(int rr) {
   return rr < 16 ? 4 * (rr & 7) + 2 + (rr >> 3) : 4 * ((rr - 16) & 7) + ((rr - 16) >> 3);
 }
 
+// all-ones if a >= b (an unordered compare gives zero), else zero
+__device__ __forceinline__ uint32_t ge_mask(float a, float b) {
+  uint32_t m;
+  asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(a), "f"(b));
+  return m;
+}
+
+// m all-ones ? a : b, for a mask m from ge_mask
+__device__ __forceinline__ float sel_f(uint32_t m, float a, float b) {
+  return __uint_as_float((m & __float_as_uint(a)) | (~m & __float_as_uint(b)));
+}
+
 // One lane's share of a packed block: the norm (binary16 bits), qs words
 // (turbo2/3: words 2 l4 and 2 l4 + 1 in w[0], w[1]; turbo4: words 2 i + l4/2 in
 // w[i], stored by the even lanes) and, for turbo3, signs word l4.
@@ -85,15 +97,19 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
   constexpr int NC = TypeTraits<TYPE>::NC;
   constexpr int HALF = NC / 2;
 
+  // this lane's 32 sign bits: bit 4i + r = sign of element 4 l4 + 16 i + r (bit
+  // 16 (i & 1) + 4 l4 + r of sign word i / 2); a set bit flips the float's sign bit
+  uint32_t smask = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    smask |= ((cb.sign_bits[i >> 1] >> (16 * (i & 1) + 4 * l4)) & 0xFu) << (4 * i);
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const uint32_t w = cb.sign_bits[i >> 1];
-      const float sgn = ((w >> (16 * (i & 1) + 4 * l4 + r)) & 1u) ? -1.f : 1.f;
       ss = fmaf(v[i][r], v[i][r], ss);
-      v[i][r] *= sgn;
+      v[i][r] = __uint_as_float(__float_as_uint(v[i][r]) ^ ((smask << (31 - (4 * i + r))) & 0x80000000u));
     }
   ss += __shfl_xor_sync(0xffffffffu, ss, 1);
   ss += __shfl_xor_sync(0xffffffffu, ss, 2);
@@ -137,39 +153,52 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
   for (int k = 0; k < HALF - 1; ++k)
     thr[k] = ss > 0.f ? 0.5f * (cb.c[HALF + k] + cb.c[HALF + k + 1]) * nrm_scale : INFINITY;
 
-  uint32_t code[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float y = v[i][r], ay = fabsf(y);
-      uint32_t j = 0;
-#pragma unroll
-      for (int k = 0; k < HALF - 1; ++k) j += (ay >= thr[k]) ? 1u : 0u;
-      code[i][r] = (y >= 0.f) ? (HALF + j) : j;
-    }
-
+  // Decisions as all-ones / zero masks (set.ge), folded into the packed words
+  // with masked ORs; |y| >= t_k against the ascending thresholds.
   out.norm = __half_as_ushort(__float2half_rn(sqrtf(ss)));
   out.sg = 0;
-  if (TYPE == 4) {
-    // word w = 2i + l4/2, element nibble 4*(l4 & 1) + r; lanes l4 and l4^1 share a word
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t x = 0;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) x |= code[i][r] << (4 * (4 * (l4 & 1) + r));
-      out.w[i] = x | __shfl_xor_sync(0xffffffffu, x, 1);
-    }
-  } else {
-    // qs word i holds elements 16i .. 16i+15; this lane's are 16i + 4*l4 + r
-    uint32_t wq[8];
+  if constexpr (TYPE == 4) {
+    // word w = 2i + l4/2, element nibble 4*(l4 & 1) + r: code = 8 s + j, j = #{t_k <= |y|}
+    // (3 bits by a three-level search over the 7 thresholds); lanes l4, l4^1 share a word
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       uint32_t x = 0;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const uint32_t f = (TYPE == 3) ? (code[i][r] & 3u) : code[i][r];
-        x |= f << qs2_bit(4 * l4 + r);
+        const float y = v[i][r], ay = fabsf(y);
+        const int sh = 4 * (4 * (l4 & 1) + r);
+        const uint32_t m2 = ge_mask(ay, thr[3]);                       // j >= 4
+        const float ta = sel_f(m2, thr[5], thr[1]);
+        const uint32_t m1 = ge_mask(ay, ta);                           // j & 2
+        const float tb = sel_f(m2, sel_f(m1, thr[6], thr[4]), sel_f(m1, thr[2], thr[0]));
+        const uint32_t m0 = ge_mask(ay, tb);                           // j & 1
+        const uint32_t ms = ge_mask(y, 0.f);                           // positive half
+        x |= (ms & (8u << sh)) | (m2 & (4u << sh)) | (m1 & (2u << sh)) | (m0 & (1u << sh));
+      }
+      out.w[i] = x | __shfl_xor_sync(0xffffffffu, x, 1);
+    }
+  } else {
+    // qs word i holds elements 16i .. 16i+15; this lane's are 16i + 4*l4 + r.
+    // turbo3: 2-bit j in qs, sign in the signs plane; turbo2: 2-bit code 2 s + j in qs.
+    uint32_t wq[8];
+    uint32_t ws[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float y = v[i][r], ay = fabsf(y);
+        const int pos = qs2_bit(4 * l4 + r);
+        const uint32_t ms = ge_mask(y, 0.f);
+        if constexpr (TYPE == 3) {
+          // j = #{t0, t1, t2 <= |y|}: bit 1 = (|y| >= t1), bit 0 = odd count
+          const uint32_t m0 = ge_mask(ay, thr[0]), m1 = ge_mask(ay, thr[1]), m2 = ge_mask(ay, thr[2]);
+          x |= ((m0 ^ m1 ^ m2) & (1u << pos)) | (m1 & (2u << pos));
+          ws[i >> 1] |= ms & (1u << sg_bit(16 * (i & 1) + 4 * l4 + r));
+        } else {
+          const uint32_t m0 = ge_mask(ay, thr[0]);
+          x |= (m0 & (1u << pos)) | (ms & (2u << pos));
+        }
       }
       x |= __shfl_xor_sync(0xffffffffu, x, 1);
       x |= __shfl_xor_sync(0xffffffffu, x, 2);
@@ -177,19 +206,11 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
     }
     out.w[0] = pick4(wq[0], wq[2], wq[4], wq[6], l4);
     out.w[1] = pick4(wq[1], wq[3], wq[5], wq[7], l4);
-    if (TYPE == 3) {
-      uint32_t ws[4];
+    if constexpr (TYPE == 3) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        uint32_t x = 0;
-#pragma unroll
-        for (int ih = 0; ih < 2; ++ih)
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            x |= (code[2 * u + ih][r] >> 2) << sg_bit(16 * ih + 4 * l4 + r);
-        x |= __shfl_xor_sync(0xffffffffu, x, 1);
-        x |= __shfl_xor_sync(0xffffffffu, x, 2);
-        ws[u] = x;
+        ws[u] |= __shfl_xor_sync(0xffffffffu, ws[u], 1);
+        ws[u] |= __shfl_xor_sync(0xffffffffu, ws[u], 2);
       }
       out.sg = pick4(ws[0], ws[1], ws[2], ws[3], l4);
     }

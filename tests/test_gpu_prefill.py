@@ -108,3 +108,13 @@ def test_asym_8k_prefill_512():
     rows = np.arange(0, 512, 7)
     out, ref = _run(sh, 512, 8192, rows=rows)
     compare_outputs(out, ref)
+
+
+@pytest.mark.parametrize("nq", [2, 4, 6])
+def test_verify_batches_at_32k_context(nq):
+    # speculative-decoding verify batches: a few new tokens attend causally over
+    # the 32K decode cache (8 KV x 32 query heads, D = 128, f32 queries)
+    sh = W.decode_32k()
+    out, ref = _run(sh, nq, 32768, dtype="f32")
+    err, nm = compare_outputs(out, ref)
+    print(f"verify nq={nq} at 32K: max-abs {err:.2e} nmse {nm:.2e}")
