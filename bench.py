@@ -126,7 +126,7 @@ def barrier(world):
 
 
 DECODE_SOURCES = ("tq_decode_mma.cuh", "tq_decode_mma_t3.cu", "tq_decode_mma.cu", "tq_decode_common.cuh",
-                  "tq_common.cuh", "tq_tc.cuh", "tq_internal.h", "tq_host.cu")
+                  "tq_common.cuh", "tq_tc.cuh", "tq_quant.cuh", "tq_internal.h", "tq_host.cu")
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_mma_32k_turbo3_ncu.md")
 
 

@@ -264,9 +264,13 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   const int64_t t0 = static_cast<int64_t>(split) * a.chunk;
   const int64_t t1 = min(a.kv_len, t0 + a.chunk);
   // this warp's key range [w0, w1): the CTA's groups of WK keys dealt out evenly
-  // (warps differ by at most one group)
+  // (warps differ by at most one group).  The warps with an extra group are the
+  // first ones, so that they fall on different SM sub-partitions (warp w runs on
+  // sub-partition w % 4): the main loop is bound by each sub-partition's issue
+  // and integer-pipe throughput, so the CTA takes as long as its busiest one.
   const int n_grp = (t1 > t0) ? static_cast<int>((t1 - t0 + WK - 1) / WK) : 0;
-  const int gb = warp * n_grp / NW, ge = (warp + 1) * n_grp / NW;
+  const int gbase = n_grp / NW, gextra = n_grp % NW;
+  const int gb = warp * gbase + min(warp, gextra), ge = gb + gbase + (warp < gextra ? 1 : 0);
   const int64_t w0 = t0 + static_cast<int64_t>(gb) * WK;
   const int64_t w1 = min(t1, t0 + static_cast<int64_t>(ge) * WK);
   const int n_it = ge - gb;
@@ -304,53 +308,87 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   };
 
   // The query loads go out before any bulk copy: issued after them they would
-  // queue behind this CTA's ~200 KB of key/value traffic.  One query block per
-  // warp (NW >= G * NBK).
+  // queue behind the key/value traffic.  One query block per warp (NW >= G * NBK).
   static_assert(NW >= G * NBK, "one query block per warp");
   float qv[4] = {0.f, 0.f, 0.f, 0.f};
   if (warp < G * NBK) load_query_block(a, hk, warp, lane, qv);
 
   // ---- append ([TQ#36] SET_ROWS of the new token, fused): the CTA whose key
   // range holds the cell (split 0 when the cell lies beyond kv_len) quantises the
-  // token's K and V row blocks of head hk with its last warp (4 lanes per block:
-  // K blocks first, then V), writes them to the cache and keeps a copy in
-  // `patch`; the warp that attends the cell copies it over its staged bytes.
+  // token's K and V row blocks of head hk with warp QWARP (4 lanes per block: K
+  // blocks first, then V), writes them to the cache and keeps a copy in `patch`;
+  // the warp that attends the cell copies it over its staged bytes once
+  // `patch_bar` has completed.  Warp QWARP quantises after the prologue, while its
+  // first tiles are in flight, and no other warp waits for it there: the last
+  // warp holds the fewest key groups, on the sub-partition with the fewest.
   constexpr int PQ = 0, PS = PQ + (NBK + NBV) * QSB, PN = PS + (NBK + NBV) * (SGB ? SGB : 4);
   __shared__ __align__(16) uint8_t patch[PN + 2 * (NBK + NBV)];
-  // The row loads go out with the query loads in every CTA (the cell is not
-  // known yet); only the owner quantises, after the query rotation.
+  __shared__ __align__(8) uint64_t patch_bar;
+  constexpr int QWARP = NW - 1;
+  // A CTA barrier waits for every load issued before it: the cell id goes out
+  // with the query loads (one lane per CTA: the same 8 bytes read by every warp
+  // of the grid queue up at one L2 line for about a microsecond); the CTA that
+  // owns the cell stages the token's rows in `rowbuf` with cp.async after the
+  // first barrier (the later barriers do not wait for those copies), or, for
+  // rows that are not 16-byte aligned per head, loads them into registers.
   const bool append = a.cell_id != nullptr;
-  const int64_t cell = append ? __ldg(a.cell_id) : -1;
-  const int gq = lane >> 2, l4 = lane & 3;                  // block of the quantising warp's lane group
-  const bool qblk = gq < NBK + NBV;
-  float nv[8][4];
-  if (append && warp == NW - 1) {
-    const bool isk = gq < NBK;
-    const int b = isk ? gq : gq - NBK;
-    const int dim = isk ? a.dk : a.dv;
-    const void *src = isk ? a.k_src : a.v_src;
-    const int64_t base = static_cast<int64_t>(hk) * dim + b * QK;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e0 = 4 * l4 + 16 * i;
-      if (qblk) quant_load4_rt(a.src_type, src, base + e0, dim - b * QK - e0, nv[i]);
-      else nv[i][0] = nv[i][1] = nv[i][2] = nv[i][3] = 0.f;
-    }
-  }
+  __shared__ int64_t s_cell;
+  __shared__ __align__(16) unsigned char rowbuf[(NBK + NBV) * QK * 4];
+  if (warp == QWARP && lane == 0) s_cell = append ? __ldg(a.cell_id) : -1;
   __syncthreads();
+  const int64_t cell = s_cell;
+  const bool cell_ok = cell >= 0 && cell < a.n_cells;
+  const bool owner = append && cell_ok && ((cell >= t0 && cell < t1) || (cell >= a.kv_len && split == 0));
+  if (append && !cell_ok && split == 0 && tid == 0) set_status(a.status, TQ_ERR_DEVICE_CHECK);
+  // The first group alone goes first: every CTA's first 32 keys are in the
+  // first wave of HBM traffic, so the compute starts as early as it can.  With
+  // 64-key stages the second group follows after the prologue on its own
+  // barrier; the other stages once the first has landed.
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) tc::mbar_init(&full[warp][s], 1);
     tc::mbar_init(&first_b[warp], 1);
+    if (warp == QWARP) tc::mbar_init(&patch_bar, 1);
     tc::mbar_init_fence();
     tc::fence_async_smem();
-    // The first group alone goes first: every CTA's first 32 keys are in the
-    // first wave of HBM traffic, so the compute starts as early as it can.
-    // With 64-key stages the second group follows after the prologue on its own
-    // barrier; the other stages once the first has landed.
     if (n_st > 0) {
       if (WS::SUB == 2) issue_part(0, 0, 1, &full[warp][0]);
       else issue(0);
+    }
+  }
+
+  const int gq = lane >> 2, l4 = lane & 3;                  // block of the quantising warp's lane group
+  const bool qblk = gq < NBK + NBV;
+  float nv[8][4];
+  if (owner && warp == QWARP) {
+    if (a.row_async) {
+      const int es = (a.src_type == TQ_F32) ? 4 : 2;
+#pragma unroll
+      for (int blk = 0; blk < NBK + NBV; ++blk) {
+        const bool isk = blk < NBK;
+        const int b = isk ? blk : blk - NBK;
+        const int dim = isk ? a.dk : a.dv;
+        const int nbytes = max(0, min(QK, dim - b * QK)) * es;
+        const unsigned char *s0 =
+            static_cast<const unsigned char *>(isk ? a.k_src : a.v_src) + (static_cast<int64_t>(hk) * dim + b * QK) * es;
+        for (int off = lane * 16; off < QK * es; off += 32 * 16) {
+          const int n = min(max(nbytes - off, 0), 16);
+          tc::cp_async16(rowbuf + blk * QK * 4 + off, n > 0 ? s0 + off : s0, n);
+        }
+      }
+      tc::cp_async_commit();
+    } else {
+      const bool isk = gq < NBK;
+      const int b = isk ? gq : gq - NBK;
+      const int dim = isk ? a.dk : a.dv;
+      const void *src = isk ? a.k_src : a.v_src;
+      const int64_t base = static_cast<int64_t>(hk) * dim + b * QK;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e0 = 4 * l4 + 16 * i;
+        if (qblk) quant_load4_rt(a.src_type, src, base + e0, dim - b * QK - e0, nv[i]);
+        else nv[i][0] = nv[i][1] = nv[i][2] = nv[i][3] = 0.f;
+      }
     }
   }
 
@@ -358,24 +396,6 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   // the score mma's B columns as binary16: n = 2h q'_hi, n = 2h + 1 q'_lo of head h,
   // zero for h >= G
   if (warp < G * NBK) rotate_query_block(a, warp, lane, qv, qrot);
-  const bool cell_ok = cell >= 0 && cell < a.n_cells;
-  const bool owner = append && cell_ok && ((cell >= t0 && cell < t1) || (cell >= a.kv_len && split == 0));
-  if (append && !cell_ok && split == 0 && tid == 0) set_status(a.status, TQ_ERR_DEVICE_CHECK);
-  if (owner && warp == NW - 1) {
-    const bool isk = gq < NBK;
-    const int b = isk ? gq : gq - NBK, nb = isk ? NBK : NBV;
-    PackedShare<T> pb;
-    quantise_block4<T>(isk ? a.cbk : a.cbv, l4, nv, pb);
-    if (qblk) {
-      const int64_t blk = (static_cast<int64_t>(hk) * a.n_cells + cell) * nb + b;
-      uint16_t *gn = const_cast<uint16_t *>(isk ? a.kn : a.vn) + blk;
-      uint8_t *gqs = const_cast<uint8_t *>(isk ? a.kqs : a.vqs) + blk * QSB;
-      uint8_t *gsg = SGB ? const_cast<uint8_t *>(isk ? a.ksg : a.vsg) + blk * SGB : nullptr;
-      store_block4<T>(pb, l4, gn, gqs, gsg);
-      store_block4<T>(pb, l4, reinterpret_cast<uint16_t *>(patch + PN) + gq, patch + PQ + gq * QSB,
-                      SGB ? patch + PS + gq * SGB : nullptr);
-    }
-  }
   for (int i = lane; i < NBV * 8 * WS::PSTR; i += 32) pw32[i] = 0;
   __syncthreads();
   uint16_t *qcol = reinterpret_cast<uint16_t *>(smem + WQ::QC);              // [8][128*NBK]
@@ -391,6 +411,33 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   }
   __syncthreads();
   if (WS::SUB == 2 && lane == 0 && n_it > 1) issue_part(0, 1, 1, &first_b[warp]);
+  if (owner && warp == QWARP) {
+    const bool isk = gq < NBK;
+    const int b = isk ? gq : gq - NBK, nb = isk ? NBK : NBV;
+    if (a.row_async) {
+      tc::cp_async_wait_all();
+      __syncwarp();
+      const int es = (a.src_type == TQ_F32) ? 4 : 2;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (qblk) quant_unpack4_rt(a.src_type, rowbuf + gq * QK * 4 + (4 * l4 + 16 * i) * es, nv[i]);
+        else nv[i][0] = nv[i][1] = nv[i][2] = nv[i][3] = 0.f;
+      }
+    }
+    PackedShare<T> pb;
+    quantise_block4<T>(isk ? a.cbk : a.cbv, l4, nv, pb);
+    if (qblk) {
+      const int64_t blk = (static_cast<int64_t>(hk) * a.n_cells + cell) * nb + b;
+      uint16_t *gn = const_cast<uint16_t *>(isk ? a.kn : a.vn) + blk;
+      uint8_t *gqs = const_cast<uint8_t *>(isk ? a.kqs : a.vqs) + blk * QSB;
+      uint8_t *gsg = SGB ? const_cast<uint8_t *>(isk ? a.ksg : a.vsg) + blk * SGB : nullptr;
+      store_block4<T>(pb, l4, gn, gqs, gsg);
+      store_block4<T>(pb, l4, reinterpret_cast<uint16_t *>(patch + PN) + gq, patch + PQ + gq * QSB,
+                      SGB ? patch + PS + gq * SGB : nullptr);
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&patch_bar);
+  }
 
   const Tab tab_k{a.tabk[0], a.tabk[1], a.tabk[2], a.tabk[3]};
   const Tab tab_v{a.tabv[0], a.tabv[1], a.tabv[2], a.tabv[3]};
@@ -436,6 +483,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     if (owner && cell >= key0 && cell < key0 + WK && cell < w1) {
       // the appended cell is in this group (landed): its freshly quantised bytes
       // replace whatever the bulk copy read
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&patch_bar, 0))) { timed_out = true; break; }
       const int row = static_cast<int>(cell - key0) + j * WK;                 // row inside the stage
       unsigned char *sw = ring + (si % STAGES) * WS::BYTES;
       constexpr int QW = QSB / 4, SW = SGB / 4;

@@ -422,6 +422,8 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
     a.v_src = v_row;
     a.cell_id = cell_id;
     a.src_type = src_type;
+    const int es = (src_type == TQ_F32) ? 4 : 2;
+    a.row_async = (k->head_dim * es) % 16 == 0 && (v->head_dim * es) % 16 == 0;
   }
   cudaError_t e = (use == TQ_DECODE_MMA) ? launch_decode_mma(k->type, v->type, a, s)
                                          : launch_decode_lut(k->type, v->type, a, s);

@@ -65,6 +65,7 @@ struct DecodeArgs {
   const void *v_src;
   const int64_t *cell_id;
   int32_t src_type;
+  int32_t row_async;      // every head's source rows start 16-byte aligned: staged by cp.async
 };
 
 struct PrefillArgs {

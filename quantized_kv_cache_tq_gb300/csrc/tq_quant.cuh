@@ -57,6 +57,22 @@ __device__ __forceinline__ void quant_load4_rt(int src_type, const void *base, i
   else quant_load4<TQ_BF16>(base, off, valid, v);
 }
 
+// Four source elements staged in shared memory (16-byte aligned for f32, 8 for
+// f16 / bf16), source type chosen at run time.
+__device__ __forceinline__ void quant_unpack4_rt(int src_type, const unsigned char *p, float v[4]) {
+  if (src_type == TQ_F32) {
+    const float4 x = *reinterpret_cast<const float4 *>(p);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  } else {
+    const uint2 x = *reinterpret_cast<const uint2 *>(p);
+    const uint16_t h[4] = {static_cast<uint16_t>(x.x & 0xffff), static_cast<uint16_t>(x.x >> 16),
+                           static_cast<uint16_t>(x.y & 0xffff), static_cast<uint16_t>(x.y >> 16)};
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      v[r] = (src_type == TQ_F16) ? __half2float(__ushort_as_half(h[r])) : __bfloat162float(__ushort_as_bfloat16(h[r]));
+  }
+}
+
 __device__ __forceinline__ uint32_t pick4(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3, int i) {
   return i == 0 ? x0 : i == 1 ? x1 : i == 2 ? x2 : x3;
 }

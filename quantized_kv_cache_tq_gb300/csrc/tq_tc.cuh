@@ -119,6 +119,16 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 }
 
 // Bounded wait for phase `parity` of `bar` without a suspend-time hint: each
+// 16-byte asynchronous copy global -> shared reading `src_bytes` (0..16) bytes and
+// zero-filling the rest; both addresses 16-byte aligned.  CTA barriers do not wait
+// for it: cp_async_wait_all does.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // try_wait returns after a short system-defined time when the phase is not
 // complete, and the loop tries again.  false if the limit was reached (well
 // under a minute).
