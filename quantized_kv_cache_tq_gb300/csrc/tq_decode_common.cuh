@@ -1,5 +1,5 @@
-// Split-KV bookkeeping shared by the decode kernels: the log-sum-exp merge of
-// the per-split partials and the inverse rotation of the merged output.
+// Split-KV bookkeeping shared by the decode kernels: tagged per-split partials,
+// their log-sum-exp merge and the inverse rotation of the merged output.
 #pragma once
 
 #include "tq_common.cuh"
@@ -18,63 +18,121 @@ __host__ __device__ inline int merge_smem_floats(int group, int nbv, int n_split
   return group * QK * nbv + 2 * group * n_splits;
 }
 
-// Called by every CTA of a decode grid after it stored its partials.  The last
-// CTA to arrive for KV head `hk` (counter in the workspace) merges the splits:
+// ---- split partials.  Each 32-bit value of a partial (m, l, o') is stored with
+// a 32-bit tag in one 64-bit word, which a single access reads or writes whole.
+// The tag is the KV head's launch epoch + 1 (never 0, so a zero-filled workspace
+// holds no valid word): the merging CTA loads every partial of its head in one
+// round trip and knows from the tags alone which ones are this launch's, so a
+// CTA that stored its partial needs no fence and no second counter, and the
+// arrival counter can be bumped before the partial is even computed.  A stale
+// word of this head carries an older epoch; the epoch of head hk changes only
+// after all CTAs of head hk have arrived, i.e. after all of them have read it.
+__device__ __forceinline__ uint32_t split_tag(uint32_t epoch) {
+  const uint32_t t = epoch + 1u;
+  return t ? t : 1u;
+}
+
+__device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t tag) {
+  const uint64_t w = (static_cast<uint64_t>(tag) << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t *p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+
+__device__ __forceinline__ float tagged_value(uint64_t w) { return __uint_as_float(static_cast<uint32_t>(w)); }
+__device__ __forceinline__ bool tagged_ok(uint64_t w, uint32_t tag) { return static_cast<uint32_t>(w >> 32) == tag; }
+
+// Epoch of KV head hk for this launch (one thread; the value goes to every
+// thread of the CTA through shared memory).
+__device__ __forceinline__ uint32_t load_epoch(const DecodeArgs &a, int hk) {
+  uint32_t e;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(e) : "l"(a.epochs + hk) : "memory");
+  return e;
+}
+
+// Arrival of this CTA at its KV head's counter (one thread, before the CTA's
+// partial is stored); the returned count says whether it is the last one.
+__device__ __forceinline__ int split_arrive(const DecodeArgs &a, int hk) {
+  int prev;
+  asm volatile("atom.add.relaxed.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(a.counters + hk) : "memory");
+  return prev;
+}
+
+// Partial of query head h = hk * group + g, split s: (m, l) and o'[d].
+__device__ __forceinline__ void store_partial_ml(const DecodeArgs &a, int h, int s, float m, float l, uint32_t tag) {
+  uint64_t *p = a.part_ml + (static_cast<size_t>(h) * a.n_splits + s) * 2;
+  st_tagged(p, m, tag);
+  st_tagged(p + 1, l, tag);
+}
+__device__ __forceinline__ void store_partial_o(const DecodeArgs &a, int h, int s, int d, float o, uint32_t tag) {
+  st_tagged(a.part + (static_cast<size_t>(h) * a.n_splits + s) * a.part_stride + d, o, tag);
+}
+
+// Run by every thread of the last CTA of KV head hk to arrive (its own partial
+// stored and a CTA barrier passed).  Merges the splits
 //   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  o' = sum_s o'_s 2^(m_s - M) / L
 // (scores are kept in the log2 domain), rotates back with the V codebook,
 //   o = S H o' / sqrt(128)   (R^T for R = H S / sqrt(128)),
-// writes out[h][0 .. dv) and resets the counter so the next launch (or graph
-// replay) finds it at zero.  No CTA ever waits for another one.
-// Each warp merges 32 consecutive outputs of one head, 24 splits at a time:
-// lane s < 24 holds split s's maximum and sum, every lane loads its output's
-// values of the 24 splits at once (one L2 round trip per 24 splits).
+// writes out[h][0 .. dv), resets the counter and advances the epoch, so the next
+// launch (or graph replay) finds the workspace ready.  Each warp merges 32
+// consecutive outputs of one head, 24 splits at a time: lane s < 24 holds split
+// s's maximum and sum, every lane loads its output's words of the 24 splits at
+// once (one L2 round trip per 24 splits) and the batch is loaded again, a
+// bounded number of times, while a word of it still carries another tag.
 // `smem` must hold merge_smem_floats(group, nbv, n_splits) floats.
 template <int NT>
-__device__ void decode_merge(const DecodeArgs &a, int hk, float *smem) {
-  __shared__ int s_last;
-  // the CTA's partial stores are ordered before the counter update by the CTA
-  // barrier and the release half of thread 0's acq_rel atomic; its acquire half
-  // orders the last CTA's loads of the other partials after it
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int prev;
-    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(a.counters + hk) : "memory");
-    s_last = (prev == a.n_splits - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-
+__device__ void decode_merge(const DecodeArgs &a, int hk, uint32_t epoch, float *smem) {
+  const uint32_t tag = split_tag(epoch);
   const int G = a.group, ns = a.n_splits, dvp = QK * a.nbv;
   const int stride = a.part_stride;
   float *orot = smem;                     // [G][dvp]
-  const float *base = a.part + static_cast<size_t>(hk) * G * ns * stride;
-  const float *base_ml = a.part_ml + static_cast<size_t>(hk) * G * ns * 2;
+  const uint64_t *base = a.part + static_cast<size_t>(hk) * G * ns * stride;
+  const uint64_t *base_ml = a.part_ml + static_cast<size_t>(hk) * G * ns * 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool late = false;
   for (int i0 = warp * 32; i0 < G * dvp; i0 += NT) {     // dvp is a multiple of 32: one head per warp pass
     const int i = i0 + lane, g = i / dvp, d = i % dvp;
-    const float *p = base + static_cast<size_t>(g) * ns * stride;
-    const float *pml = base_ml + static_cast<size_t>(g) * ns * 2;
+    const uint64_t *p = base + static_cast<size_t>(g) * ns * stride;
+    const uint64_t *pml = base_ml + static_cast<size_t>(g) * ns * 2;
     float M = -INFINITY, L = 0.f, o = 0.f;
     for (int s0 = 0; s0 < ns; s0 += 24) {
       const int n = min(24, ns - s0);
-      const float *ps = p + static_cast<size_t>(s0) * stride;
-      float2 ml = make_float2(-INFINITY, 0.f);
-      if (lane < n) ml = __ldcg(reinterpret_cast<const float2 *>(pml) + s0 + lane);
-      const float ms = ml.x, ls = ml.y;
-      float ov[24];
+      const uint64_t *ps = p + static_cast<size_t>(s0) * stride + d;
+      uint64_t wm = 0, wl = 0, wo[24];
+      for (int tries = 0;; ++tries) {
+        if (lane < n) {
+          wm = ld_tagged(pml + 2 * (s0 + lane));
+          wl = ld_tagged(pml + 2 * (s0 + lane) + 1);
+        }
 #pragma unroll
-      for (int j = 0; j < 24; ++j) ov[j] = (j < n) ? __ldcg(ps + static_cast<size_t>(j) * stride + d) : 0.f;
+        for (int j = 0; j < 24; ++j) wo[j] = (j < n) ? ld_tagged(ps + static_cast<size_t>(j) * stride) : 0;
+        bool ok = lane >= n || (tagged_ok(wm, tag) && tagged_ok(wl, tag));
+#pragma unroll
+        for (int j = 0; j < 24; ++j) ok = ok && (j >= n || tagged_ok(wo[j], tag));
+        if (__all_sync(0xffffffffu, ok)) break;
+        if (tries >= (1 << 16)) {          // a split never stored its partial: report, merge what is there
+          late = true;
+          break;
+        }
+        __nanosleep(100);
+      }
+      const float ms = (lane < n) ? tagged_value(wm) : -INFINITY, ls = (lane < n) ? tagged_value(wl) : 0.f;
       const float Mn = fmaxf(M, warp_max(ms));
       const float f = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
       const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - Mn);
       L = L * f + warp_sum(w * ls);
       o *= f;
 #pragma unroll
-      for (int j = 0; j < 24; ++j) o = fmaf(__shfl_sync(0xffffffffu, w, j), ov[j], o);
+      for (int j = 0; j < 24; ++j) o = fmaf(__shfl_sync(0xffffffffu, w, j), tagged_value(wo[j]), o);
       M = Mn;
     }
     orot[i] = (L > 0.f) ? o / L : 0.f;
   }
+  if (late && lane == 0) set_status(a.status, TQ_ERR_TIMEOUT);
   __syncthreads();
 
   for (int wb = warp; wb < G * a.nbv; wb += NT / 32) {
@@ -94,7 +152,10 @@ __device__ void decode_merge(const DecodeArgs &a, int hk, float *smem) {
       if (d < a.dv) o[d] = v[r];
     }
   }
-  if (threadIdx.x == 0) a.counters[hk] = 0;
+  if (threadIdx.x == 0) {
+    a.counters[hk] = 0;
+    a.epochs[hk] = epoch + 1u;
+  }
 }
 
 // Query block wb = g * nbk + b (head hk * group + g, dims 128 b ..): lane i

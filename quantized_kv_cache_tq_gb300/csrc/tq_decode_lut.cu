@@ -69,6 +69,9 @@ __global__ void __launch_bounds__(kThreads) decode_lut_kernel(const DecodeArgs a
   const int64_t t1 = min(a.kv_len, t0 + a.chunk);
 
   // 1. rotated, pre-scaled queries and the Q x centroid table
+  __shared__ uint32_t s_epoch;
+  __shared__ int s_last;
+  if (tid == 0) s_epoch = load_epoch(a, hk);
   rotate_queries<kThreads>(a, hk, qrot);
   if (tid < 16) vtab[tid] = (tid < a.cbv.n) ? code_value(a.cbv.c, a.cbv.n, tid) : 0.f;
   __syncthreads();
@@ -208,14 +211,18 @@ __global__ void __launch_bounds__(kThreads) decode_lut_kernel(const DecodeArgs a
     if (kr == 0)
       for (int g = 0; g < G; ++g) acc[g] += accbuf[g * dvp + d];
   }
+  int prev = 0;
+  if (tid == 0) prev = split_arrive(a, hk);
+  const uint32_t epoch = s_epoch, tag = split_tag(epoch);
   if (kr == 0) {
     for (int g = 0; g < G; ++g) {
-      const size_t ps = static_cast<size_t>(hk * G + g) * a.n_splits + split;
-      a.part[ps * a.part_stride + d] = acc[g];
-      if (d == 0) { a.part_ml[2 * ps] = m_run[g]; a.part_ml[2 * ps + 1] = l_run[g]; }
+      store_partial_o(a, hk * G + g, split, d, acc[g], tag);
+      if (d == 0) store_partial_ml(a, hk * G + g, split, m_run[g], l_run[g], tag);
     }
   }
-  decode_merge<kThreads>(a, hk, lut);
+  if (tid == 0) s_last = (prev == a.n_splits - 1);
+  __syncthreads();
+  if (s_last) decode_merge<kThreads>(a, hk, epoch, lut);
 }
 
 template <int KT, int VT>

@@ -333,8 +333,13 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   // rows that are not 16-byte aligned per head, loads them into registers.
   const bool append = a.cell_id != nullptr;
   __shared__ int64_t s_cell;
+  __shared__ uint32_t s_epoch;
   __shared__ __align__(16) unsigned char rowbuf[(NBK + NBV) * QK * 4];
-  if (warp == QWARP && lane == 0) s_cell = append ? __ldg(a.cell_id) : -1;
+  if (warp == QWARP && lane == 0) {
+    const uint32_t e = load_epoch(a, hk);
+    s_cell = append ? __ldg(a.cell_id) : -1;
+    s_epoch = e;
+  }
   __syncthreads();
   const int64_t cell = s_cell;
   const bool cell_ok = cell >= 0 && cell < a.n_cells;
@@ -640,8 +645,13 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   __syncthreads();
   // CTA partial over the warps.  Launched as one cluster per KV head (cluster
   // size == n_splits) the partial stays in this CTA's shared memory for the
-  // cluster merge; otherwise it goes to the workspace for the last-CTA merge.
+  // cluster merge; otherwise it goes to the workspace, tagged, for the last-CTA
+  // merge.  The CTA arrives at its head's counter first, so that the atomic's
+  // round trip overlaps the CTA merge and the stores.
   const bool in_cluster = tc::cluster_size() == static_cast<uint32_t>(a.n_splits);
+  int prev = 0;
+  if (!in_cluster && tid == 0) prev = split_arrive(a, hk);
+  const uint32_t epoch = s_epoch, tag = split_tag(epoch);
   float *cpart = reinterpret_cast<float *>(smem + WS::PT);      // m[G], l[G], o'[G][DVP]
   for (int i = tid; i < G * DVP; i += NT) {
     const int h = i / DVP, d = i % DVP;
@@ -663,13 +673,18 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
         cpart[G + h] = l;
       }
     } else {
-      const size_t ps = static_cast<size_t>(hk * G + h) * a.n_splits + split;
-      a.part[ps * a.part_stride + d] = o;
-      if (d == 0) *reinterpret_cast<float2 *>(a.part_ml + 2 * ps) = make_float2(M, l);
+      store_partial_o(a, hk * G + h, split, d, o, tag);
+      if (d == 0) store_partial_ml(a, hk * G + h, split, M, l, tag);
     }
   }
-  if (in_cluster) cluster_merge<G, NBV, NT>(a, hk, cpart, qrot);
-  else decode_merge<NT>(a, hk, reinterpret_cast<float *>(smem));
+  if (in_cluster) {
+    cluster_merge<G, NBV, NT>(a, hk, cpart, qrot);
+  } else {
+    __shared__ int s_last;
+    if (tid == 0) s_last = (prev == a.n_splits - 1);
+    __syncthreads();
+    if (s_last) decode_merge<NT>(a, hk, epoch, reinterpret_cast<float *>(smem));
+  }
 }
 
 template <int T, int G, int NBK, int NBV>

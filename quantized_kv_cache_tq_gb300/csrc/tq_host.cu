@@ -92,10 +92,11 @@ DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int6
   if (chunk < 128) chunk = 128;
   L.chunk = chunk;
   L.n_splits = kv_len > 0 ? static_cast<int>((kv_len + chunk - 1) / chunk) : 1;
-  L.counters_off = kWsHeader;
+  L.epochs_off = kWsHeader;
+  L.counters_off = L.epochs_off + kWsEpochBytes;
   L.ml_off = L.counters_off + round_up(sizeof(int32_t) * n_kv_heads, 256);
-  L.part_off = L.ml_off + round_up(sizeof(float) * 2 * n_q_heads * L.n_splits, 256);
-  L.total = L.part_off + round_up(sizeof(float) * n_q_heads * L.n_splits * 128 * static_cast<size_t>(nbv), 256);
+  L.part_off = L.ml_off + round_up(sizeof(uint64_t) * 2 * n_q_heads * L.n_splits, 256);
+  L.total = L.part_off + round_up(sizeof(uint64_t) * n_q_heads * L.n_splits * 128 * static_cast<size_t>(nbv), 256);
   return L;
 }
 
@@ -113,7 +114,7 @@ PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t
   if (sp > tiles / 2) sp = tiles / 2;
   if (sp < 1) sp = 1;
   L.n_split = static_cast<int>(sp);
-  L.counters_off = kWsHeader;
+  L.counters_off = kWsHeader + kWsEpochBytes;      // the decode epochs stay untouched
   L.part_off = L.counters_off + round_up(sizeof(int32_t) * qt * n_kv_heads, 256);
   L.total = L.part_off;
   if (L.n_split > 1)
@@ -335,9 +336,16 @@ static tq_status check_kv_pair(const tq_cache *k, const tq_cache *v, int n_q_hea
   return TQ_OK;
 }
 
+// Decode also keeps one epoch word per KV head in the workspace header.
+static tq_status check_decode_pair(const tq_cache *k, const tq_cache *v, int n_q_heads, int64_t kv_len) {
+  const tq_status st = check_kv_pair(k, v, n_q_heads, kv_len);
+  if (st != TQ_OK) return st;
+  return k->n_kv_heads <= kMaxDecodeKvHeads ? TQ_OK : TQ_ERR_INVALID_ARG;
+}
+
 size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_heads,
                                  int64_t kv_len) {
-  if (check_kv_pair(k, v, n_q_heads, kv_len) != TQ_OK) return 0;
+  if (check_decode_pair(k, v, n_q_heads, kv_len) != TQ_OK) return 0;
   return decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, TQ_DECODE_AUTO).total;
 }
 
@@ -347,7 +355,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
                              const void *k_row, const void *v_row, int src_type, const int64_t *cell_id,
                              const float *q, int n_q_heads, int64_t kv_len, float scale, int algo, float *out,
                              void *workspace, size_t workspace_bytes, tq_stream stream) {
-  tq_status st = check_kv_pair(k, v, n_q_heads, kv_len);
+  tq_status st = check_decode_pair(k, v, n_q_heads, kv_len);
   if (st != TQ_OK) return st;
   if (!codebook_ok(cbk, k->type) || !codebook_ok(cbv, v->type)) return TQ_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out) || !isfinite(scale)) return TQ_ERR_INVALID_ARG;
@@ -397,9 +405,10 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.vsg = static_cast<const uint8_t *>(v->signs);
   a.q = q;
   a.out = out;
-  a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.part_off);
-  a.part_ml = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.ml_off);
+  a.part = reinterpret_cast<uint64_t *>(static_cast<char *>(workspace) + L.part_off);
+  a.part_ml = reinterpret_cast<uint64_t *>(static_cast<char *>(workspace) + L.ml_off);
   a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.counters_off);
+  a.epochs = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + L.epochs_off);
   a.status = status;
   a.n_cells = k->n_cells;
   a.kv_len = kv_len;

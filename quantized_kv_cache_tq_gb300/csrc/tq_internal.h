@@ -33,7 +33,8 @@ struct SetRowsArgs {
 
 // Everything a decode kernel needs; the partial results of split s of query
 // head h are m (log2 domain), l at part_ml + 2 (h * n_splits + s) and
-// o'[0 .. 128 nbv) (unnormalised, rotated domain) at part + (h * n_splits + s) * part_stride.
+// o'[0 .. 128 nbv) (unnormalised, rotated domain) at part + (h * n_splits + s) * part_stride,
+// each value in a 64-bit word with its launch tag (tq_decode_common.cuh).
 struct DecodeArgs {
   const uint16_t *kn;
   const uint8_t *kqs;
@@ -43,9 +44,10 @@ struct DecodeArgs {
   const uint8_t *vsg;
   const float *q;
   float *out;
-  float *part;            // split outputs o'[h][split][part_stride]
-  float *part_ml;         // split maxima and sums [h][split][2]
-  int32_t *counters;
+  uint64_t *part;         // split outputs o'[h][split][part_stride], tagged words
+  uint64_t *part_ml;      // split maxima and sums [h][split][2], tagged words
+  int32_t *counters;      // [kv head] arrivals, self-resetting
+  uint32_t *epochs;       // [kv head] launch epochs (tags of the partials)
   int32_t *status;        // workspace status word (device-side errors)
   int64_t n_cells;
   int64_t kv_len;
@@ -55,7 +57,7 @@ struct DecodeArgs {
   int32_t group;          // query heads per KV head
   int32_t dk, dv;         // logical head dims
   int32_t nbk, nbv;       // 128-blocks of K / V rows
-  int32_t part_stride;    // floats per (head, split) partial output (128 nbv)
+  int32_t part_stride;    // words per (head, split) partial output (128 nbv)
   float scale_log2;       // softmax scale * log2(e)
   DevCodebook cbk, cbv;
   uint32_t tabk[4], tabv[4];   // binary16 byte tables of the code values (see code_byte_tables)
@@ -97,12 +99,17 @@ struct PrefillArgs {
 };
 
 struct DecodeWorkspaceLayout {
-  size_t counters_off, ml_off, part_off, total;
+  size_t epochs_off, counters_off, ml_off, part_off, total;
   int n_splits;
   int64_t chunk;
 };
 
 constexpr size_t kWsHeader = 256;   // status word lives at offset 0
+// Decode epochs of KV heads 0 .. 255 sit at a fixed place after the header in
+// every workspace layout, so no other use of a shared workspace overwrites them
+// and a change of decode shape keeps each head's epoch word.
+constexpr size_t kWsEpochBytes = 1024;
+constexpr int kMaxDecodeKvHeads = 256;
 
 int sm_count();
 bool cluster_merge_ok(const void *kern, int csize, int threads, size_t smem, int want);

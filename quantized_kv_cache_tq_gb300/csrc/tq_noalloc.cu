@@ -64,9 +64,12 @@ extern "C" tq_status tq_fattn_decode_noalloc(const tq_cache *k, const tq_cache *
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
-  // counters and status word must start at zero (the array keeps the last call's contents)
+  // the status word and the counters start at zero (the array keeps the last
+  // call's contents); the epochs carry on from call to call
   const DecodeWorkspaceLayout L = decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, algo);
-  if (cudaMemsetAsync(ws, 0, L.ml_off, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, L.epochs_off, s) != cudaSuccess ||
+      cudaMemsetAsync(static_cast<char *>(ws) + L.counters_off, 0, L.ml_off - L.counters_off, s) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
