@@ -13,7 +13,8 @@ Sources (the pages this restates; no code was taken from them):
             o = x[j^h]; x[j] = (j&h) ? o - x[j] : x[j] + o),
             "asymmetric D" (K head dim 192, V head dim 128, padding),
             "Q x centroid LUT" (4/8/16 centroids; 2 qs bytes + 1 signs byte
-            per 8 elements), "VEC tuning" (results table; turbo2 = 7.5x).
+            per 8 elements), "VEC tuning" (results table; turbo2 = 7.5x;
+            item 3: sparse V thresholds 5e-3 for turbo3/4, 1e-2 for turbo2).
   [HIP#28]  atomic-llama-cpp-turboquant pull request #28, "HIP/turbo3:
             graph-safe decode + inline-dequant TILE prefill" -- sections
             "Two coupled changes" and "Correctness" (NMSE vs a CPU reference).
@@ -40,6 +41,14 @@ Readings where the pages are silent (each is a rule both sides follow):
     scale given by the caller; causal query i of nq sits at position
     kv_len - nq + i; query head h reads KV head h // (Hq / Hkv).
   * kv_len = 0 gives a zero output.
+  * sparse V ([TQ#36 "VEC tuning"] item 3 names only the thresholds): a key whose
+    softmax weight relative to the maximum score, exp(s - max), is below the
+    threshold adds nothing to the weighted sum of V rows; the normaliser still
+    sums every key.  A kernel sees only a running maximum, which is at most the
+    final one, so the keys it leaves out are a subset of those this rule names
+    with the final maximum: ``sparse_v_attention`` returns the result without
+    them, the exact result and the bound on the distance of any such subset's
+    result from both.
 """
 from __future__ import annotations
 
@@ -349,6 +358,31 @@ def softmax_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
     return (e @ v) / np.sum(e, axis=1, keepdims=True)
 
 
+def sparse_v_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
+                       threshold: float, slack: float = 1.0):
+    """Sparse-V decode attention of queries q [nq][Dk] over k [L][Dk], v [L][Dv]
+    (f64).  With p_t = exp(s_t - max_t s_t), s = scale q.k, the keys with
+    p_t < threshold * slack are left out of the V sum (the normaliser keeps them):
+        o_skip  = sum_{kept t} p_t v_t / sum_t p_t
+        o_exact = sum_t p_t v_t / sum_t p_t
+        bound_d = sum_{left-out t} p_t |v_t,d| / sum_t p_t.
+    Any result that leaves out a subset of those keys is within bound of both.
+    Returns (o_skip, o_exact, bound), each [nq][Dv]."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    if k.shape[0] == 0:
+        z = np.zeros((q.shape[0], v.shape[1]))
+        return z, z.copy(), z.copy()
+    s = scale * (q @ k.T)
+    p = np.exp(s - np.max(s, axis=1, keepdims=True))
+    total = np.sum(p, axis=1, keepdims=True)
+    out = p < threshold * slack
+    p_kept = np.where(out, 0.0, p)
+    p_out = np.where(out, p, 0.0)
+    return (p_kept @ v) / total, (p @ v) / total, (p_out @ np.abs(v)) / total
+
+
 def lse_partial(q, k, v, scale):
     """(m, l, o) of one key range: m = max score, l = sum exp(s - m),
     o = sum exp(s - m) v / l  (the pieces a split-KV pass keeps)."""
@@ -380,6 +414,22 @@ def decode(kc: Cache, vc: Cache, k_signs, v_signs, k_cents, v_cents,
         for h in range(hk * g, (hk + 1) * g):
             out[h] = softmax_attention(q[h][None, :], k, v, scale)[0]
     return out
+
+
+def decode_sparse_v(kc: Cache, vc: Cache, k_signs, v_signs, k_cents, v_cents,
+                    q: np.ndarray, kv_len: int, scale: float, threshold: float, slack: float = 1.0):
+    """Single-query decode with sparse V (see ``sparse_v_attention``):
+    q [Hq][Dk] -> (o_skip, o_exact, bound), each [Hq][Dv]."""
+    n_q = q.shape[0]
+    g = n_q // kc.n_kv_heads
+    res = [np.zeros((n_q, vc.head_dim)) for _ in range(3)]
+    for hk in range(kc.n_kv_heads):
+        k = dequantize_cache(kc, k_signs, k_cents, kv_len, hk)
+        v = dequantize_cache(vc, v_signs, v_cents, kv_len, hk)
+        for h in range(hk * g, (hk + 1) * g):
+            for r, x in zip(res, sparse_v_attention(q[h][None, :], k, v, scale, threshold, slack)):
+                r[h] = x[0]
+    return tuple(res)
 
 
 def prefill(kc: Cache, vc: Cache, k_signs, v_signs, k_cents, v_cents,

@@ -292,6 +292,66 @@ def test_split_lse_merge_equals_unsplit():
     assert np.allclose(O.lse_merge(parts), full, atol=1e-14)
 
 
+def test_sparse_v_special_cases_and_bound():
+    # [TQ#36 "VEC tuning"] item 3: keys with exp(s - max) < threshold leave the V sum
+    q = W.normal(11, 1, 2 * 16).reshape(2, 16)
+    k = W.normal(11, 2, 40 * 16).reshape(40, 16) * 2
+    v = W.normal(11, 3, 40 * 8).reshape(40, 8)
+    exact = O.softmax_attention(q, k, v, 0.7)
+    # threshold 0 leaves nothing out
+    o_skip, o_exact, bound = O.sparse_v_attention(q, k, v, 0.7, 0.0)
+    assert np.allclose(o_exact, exact, atol=1e-14) and np.array_equal(o_skip, o_exact) and np.all(bound == 0)
+    # a threshold above 1 leaves every key out (the maximum has weight 1): zero output,
+    # and the bound is the whole |V|-weighted mass
+    o_skip, _, bound = O.sparse_v_attention(q, k, v, 0.7, 1.5)
+    assert np.all(o_skip == 0)
+    assert np.allclose(bound, O.softmax_attention(q, k, np.abs(v), 0.7), atol=1e-14)
+    # any threshold: the left-out keys move the result by at most the bound
+    for thr in (1e-3, 5e-3, 1e-2, 0.2):
+        o_skip, o_exact, bound = O.sparse_v_attention(q, k, v, 0.7, thr)
+        assert np.all(np.abs(o_skip - o_exact) <= bound + 1e-15)
+        assert np.all(bound >= 0)
+
+
+def test_sparse_v_by_hand():
+    # scores 0, -10, -1 (natural log units): weights 1, e^-10, e^-1; threshold 1e-3
+    # leaves key 1 out of the V sum only
+    q = np.array([[1.0, 0.0]])
+    k = np.array([[0.0, 0.0], [-10.0, 0.0], [-1.0, 0.0]])
+    v = np.array([[1.0, 2.0], [3.0, -4.0], [5.0, 6.0]])
+    w = np.array([1.0, math.exp(-10.0), math.exp(-1.0)])
+    o_skip, o_exact, bound = O.sparse_v_attention(q, k, v, 1.0, 1e-3)
+    assert np.allclose(o_skip[0], (v[0] + w[2] * v[2]) / w.sum(), atol=1e-15)
+    assert np.allclose(o_exact[0], (w[:, None] * v).sum(0) / w.sum(), atol=1e-15)
+    assert np.allclose(bound[0], w[1] * np.abs(v[1]) / w.sum(), atol=1e-18)
+    # a slack of 50 moves the cut to 0.05, still between e^-10 and e^-1
+    o2, _, _ = O.sparse_v_attention(q, k, v, 1.0, 1e-3, slack=50.0)
+    assert np.array_equal(o2, o_skip)
+
+
+def test_decode_sparse_v_matches_per_head_attention():
+    shape = W.AttnShape("t", 2, 4, 128, 128, 70, seed=5)
+    c = O.centroids(3)
+    sk, sv = W.codebook_signs(shape)
+    kr, vr = W.kv_inputs(shape)
+    kc = O.empty_cache(3, 2, 128, 128)
+    vc = O.empty_cache(3, 2, 128, 128)
+    O.set_rows(kc, kr, np.arange(70), sk, c)
+    O.set_rows(vc, vr, np.arange(70), sv, c)
+    q = W.decode_query(shape) * 4
+    o_skip, o_exact, bound = O.decode_sparse_v(kc, vc, sk, sv, c, c, q, 70, 1 / math.sqrt(128), 5e-3)
+    assert np.allclose(o_exact, O.decode(kc, vc, sk, sv, c, c, q, 70, 1 / math.sqrt(128)), atol=1e-13)
+    kh = O.dequantize_cache(kc, sk, c, 70)
+    vh = O.dequantize_cache(vc, sv, c, 70)
+    for h in range(4):
+        s = (q[h] @ kh[h // 2].T) / math.sqrt(128)
+        p = np.exp(s - s.max())
+        keep = p >= 5e-3
+        ref = (p[keep] @ vh[h // 2][keep]) / p.sum()
+        assert np.allclose(o_skip[h], ref, atol=1e-13)
+    assert np.all(np.abs(o_skip - o_exact) <= bound + 1e-15)
+
+
 def test_decode_gqa_and_dequant_path():
     shape = W.AttnShape("t", 2, 4, 128, 128, 70, seed=3)
     c = O.centroids(3)
