@@ -456,6 +456,46 @@ def _device_gaussian(torch, gen, shape, dev, outliers=True):
     return x
 
 
+def run_sparse_v_extra(tq, torch, dev, n_sets=6, thr=5e-3):
+    """Decode at 32K over caches whose scores have a wide gap: about one key in 64
+    scores near +20, the rest near -20 (K rows +-3 along one direction per KV head
+    plus N(0, 0.1) noise, queries 75 times that direction).  Decode without and
+    with sparse V (threshold 5e-3): the groups of cold keys leave the V work.
+    n_sets cache pairs (26 MB each) are cycled so that the working set exceeds L2."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20263)
+    L, HK, HQ, DD = KV_LEN, N_KV, N_Q, D
+    import workloads as W
+    sk, sv = W.codebook_signs(W.decode_32k())
+    cbk, cbv = tq.codebook(3, sk), tq.codebook(3, sv)
+    cells = torch.arange(L, dtype=torch.int64, device=dev)
+    sets = []
+    for _ in range(n_sets):
+        e = torch.randn((HK, DD), generator=gen, device=dev)
+        e /= e.norm(dim=1, keepdim=True)
+        hot = torch.rand((L, HK), generator=gen, device=dev) < 1.0 / 64
+        krow = 0.1 * torch.randn((L, HK, DD), generator=gen, device=dev) + torch.where(hot, 3.0, -3.0)[..., None] * e
+        kc, vc = tq.TqCache(3, HK, DD, L, dev), tq.TqCache(3, HK, DD, L, dev)
+        tq.set_rows(kc, cbk, krow.contiguous(), cells)
+        tq.set_rows(vc, cbv, torch.randn((L, HK, DD), generator=gen, device=dev), cells)
+        q = 75.0 * e.repeat_interleave(HQ // HK, dim=0) + 0.1 * torch.randn((HQ, DD), generator=gen, device=dev)
+        sets.append((kc, vc, q.contiguous(), torch.empty((HQ, DD), dtype=torch.float32, device=dev)))
+    ws = tq.workspace(tq._lib.tq_fattn_decode_workspace(sets[0][0].c, sets[0][1].c, HQ, L), dev)
+    res = {"workload": f"decode_32k turbo3 over gapped scores (1/64 hot keys), {n_sets} cache sets cycled",
+           "threshold": thr}
+    for name, t_ in (("exact_us", 0.0), ("sparse_v_us", thr)):
+        def once(t_=t_):
+            for kc, vc, q, out in sets:
+                tq.fattn_decode(kc, vc, cbk, cbv, q, L, 1.0 / math.sqrt(DD), out=out, ws=ws, sparse_v=t_)
+        g = torch.cuda.CUDAGraph()
+        once()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            once()
+        res[name] = time_graph(torch, g.replay, reps=50) / n_sets * 1e6
+    return res
+
+
 def run_prefill_extra(tq, torch, dev, tflops_peak, nqs=(4096, 512)):
     """Prefill over the 4K-context turbo3 cache (8 KV x 16 query heads, D = 256, causal)."""
     import workloads as W
@@ -540,6 +580,7 @@ def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv
     nbytes = 2 * (k_src.numel() * 4 + N_KV * KV_LEN * 50) + 2 * KV_LEN * 8
     ex["set_rows_bulk"] = {"workload": "32768 rows x 8 KV heads x 128, K and V, f32 -> turbo3",
                            "ms": t * 1e3, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak}
+    ex["sparse_v"] = run_sparse_v_extra(tq, torch, dev)
     ex["prefill"] = run_prefill_extra(tq, torch, dev, tflops_peak)
     ex["int8_prompt"] = run_int8_extra(tq, torch, dev, tflops_peak)
     ex["f16_prompt"] = run_f16_prompt_extra(tq, torch, dev, tflops_peak)

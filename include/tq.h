@@ -191,6 +191,22 @@ tq_status tq_fattn_decode_append(const tq_cache *k, const tq_cache *v, const tq_
                                  float scale, int algo, float *out, void *workspace, size_t workspace_bytes,
                                  tq_stream stream);
 
+/* tq_fattn_decode with sparse V ([TQ#36] "VEC tuning", item 3: thresholds
+ * 5e-3 for turbo3 / turbo4 and 1e-2 for turbo2).  A key whose softmax weight
+ * relative to the running maximum score, exp(s - m), is below v_threshold for
+ * every query head of its GQA group adds nothing to the weighted sum of V rows;
+ * its weight still counts in the normaliser.  The tensor-core kernel decides per
+ * group of 16 keys, the LUT kernel per key.  The running maximum is at most the
+ * final one, so every key left out has exp(s - max) < v_threshold for each of
+ * those heads; which of those keys are left out depends on the key order and the
+ * launch shape.  v_threshold = 0 gives exactly tq_fattn_decode's result.
+ * Errors: as tq_fattn_decode, and TQ_ERR_INVALID_ARG for a negative or
+ * non-finite v_threshold. */
+tq_status tq_fattn_decode_sparse_v(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                                   const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
+                                   float scale, float v_threshold, int algo, float *out, void *workspace,
+                                   size_t workspace_bytes, tq_stream stream);
+
 /* tq_fattn_decode without a caller workspace, for callers that cannot
  * allocate device memory (code inside an allocator or memory-pool callback, a
  * runtime that has reserved all device memory up front, a plugin host that only

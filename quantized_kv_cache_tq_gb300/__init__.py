@@ -66,7 +66,9 @@ def set_rows(cache: TqCache, cb: tq_codebook, src, cell_ids, dev_status=None, st
 
 
 def fattn_decode(kc: TqCache, vc: TqCache, cbk, cbv, q, kv_len: int, scale: float | None = None,
-                 algo: int = TQ_DECODE_AUTO, out=None, ws=None, stream=None):
+                 algo: int = TQ_DECODE_AUTO, out=None, ws=None, stream=None, sparse_v: float = 0.0):
+    """Decode over cells 0..kv_len-1; ``sparse_v`` > 0 leaves out of the V sum the
+    keys whose weights relative to the running maximum are below it."""
     torch = _torch()
     n_q = q.shape[0]
     scale = 1.0 / math.sqrt(kc.head_dim) if scale is None else scale
@@ -74,9 +76,14 @@ def fattn_decode(kc: TqCache, vc: TqCache, cbk, cbv, q, kv_len: int, scale: floa
         out = torch.empty((n_q, vc.head_dim), dtype=torch.float32, device=q.device)
     if ws is None:
         ws = workspace(_lib.tq_fattn_decode_workspace(kc.c, vc.c, n_q, kv_len), q.device)
-    st = _lib.tq_fattn_decode(kc.c, vc.c, cbk, cbv, q.data_ptr(), n_q, kv_len, scale, algo,
-                              out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
-    _lib.check("tq_fattn_decode", st)
+    if sparse_v:
+        st = _lib.tq_fattn_decode_sparse_v(kc.c, vc.c, cbk, cbv, q.data_ptr(), n_q, kv_len, scale, sparse_v,
+                                           algo, out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
+        _lib.check("tq_fattn_decode_sparse_v", st)
+    else:
+        st = _lib.tq_fattn_decode(kc.c, vc.c, cbk, cbv, q.data_ptr(), n_q, kv_len, scale, algo,
+                                  out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
+        _lib.check("tq_fattn_decode", st)
     return out
 
 

@@ -65,6 +65,9 @@ _SIGS = {
     "tq_fattn_decode": (C.c_int, [C.POINTER(tq_cache), C.POINTER(tq_cache), C.POINTER(tq_codebook),
                                   C.POINTER(tq_codebook), _P, C.c_int, C.c_int64, C.c_float, C.c_int,
                                   _P, _P, C.c_size_t, _P]),
+    "tq_fattn_decode_sparse_v": (C.c_int, [C.POINTER(tq_cache), C.POINTER(tq_cache), C.POINTER(tq_codebook),
+                                           C.POINTER(tq_codebook), _P, C.c_int, C.c_int64, C.c_float, C.c_float,
+                                           C.c_int, _P, _P, C.c_size_t, _P]),
     "tq_fattn_decode_append": (C.c_int, [C.POINTER(tq_cache), C.POINTER(tq_cache), C.POINTER(tq_codebook),
                                          C.POINTER(tq_codebook), _P, _P, C.c_int, _P, _P, C.c_int, C.c_int64,
                                          C.c_float, C.c_int, _P, _P, C.c_size_t, _P]),
@@ -137,6 +140,13 @@ def tq_fattn_decode(k: tq_cache, v: tq_cache, cbk: tq_codebook, cbv: tq_codebook
                     ws_bytes: int, stream: int | None) -> int:
     return lib.tq_fattn_decode(C.byref(k), C.byref(v), C.byref(cbk), C.byref(cbv), q, n_q_heads,
                                kv_len, scale, algo, out, ws, ws_bytes, stream)
+
+
+def tq_fattn_decode_sparse_v(k: tq_cache, v: tq_cache, cbk: tq_codebook, cbv: tq_codebook, q: int,
+                             n_q_heads: int, kv_len: int, scale: float, v_threshold: float, algo: int,
+                             out: int, ws: int, ws_bytes: int, stream: int | None) -> int:
+    return lib.tq_fattn_decode_sparse_v(C.byref(k), C.byref(v), C.byref(cbk), C.byref(cbv), q, n_q_heads,
+                                        kv_len, scale, v_threshold, algo, out, ws, ws_bytes, stream)
 
 
 def tq_fattn_decode_append(k: tq_cache, v: tq_cache, cbk: tq_codebook, cbv: tq_codebook, k_row: int,

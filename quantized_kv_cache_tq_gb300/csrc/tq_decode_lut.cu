@@ -189,8 +189,15 @@ __global__ void __launch_bounds__(kThreads) decode_lut_kernel(const DecodeArgs a
       acc[g] *= alpha[g];
     }
 
-    // 5. o'_g[d] += p_g(t) * n_t * c[code_{t,d}]
+    // 5. o'_g[d] += p_g(t) * n_t * c[code_{t,d}]; with sparse V a key whose
+    // weights (relative to the running maximum) are all below the threshold
+    // adds nothing
     for (int kk = kr; kk < tile_n; kk += n_kr) {
+      if (a.v_thresh > 0.f) {
+        bool keep = false;
+        for (int g = 0; g < G; ++g) keep = keep || sp[g * kTile + kk] >= a.v_thresh;
+        if (!keep) continue;
+      }
       const int blk = kk * a.nbv + vb;
       const float nrm = __half2float(__ushort_as_half(vn_s[blk]));
       const int code = load_code<VT>(vqs_s + static_cast<size_t>(blk) * VQSB,

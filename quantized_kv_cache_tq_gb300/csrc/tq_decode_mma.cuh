@@ -568,6 +568,17 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
           l_run += sc[grp][r];
         }
     }
+    // sparse V ([TQ#36] "VEC tuning"): a group of 16 keys whose weights, relative
+    // to the reference maximum, are below the threshold for every query head of
+    // the warp adds nothing to O' (its weights still count in l).  The reference
+    // maximum trails the running maximum by less than 2^8, so the keys left out
+    // have weights below the threshold relative to the final maximum too.
+    bool vkeep[2] = {true, true};
+    if (a.v_thresh > 0.f) {
+#pragma unroll
+      for (int grp = 0; grp < 2; ++grp)
+        vkeep[grp] = __any_sync(0xffffffffu, has_head && (sc[grp][0] >= a.v_thresh || sc[grp][1] >= a.v_thresh));
+    }
 
     // ---- P' = p * |v| (per V block) as binary16 (hi, lo) key pairs: column 2c (hi)
     // and 2c + 1 (lo), pair g of group grp = keys (grp*16 + g, grp*16 + g + 8)
@@ -575,6 +586,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     for (int b = 0; b < NBV; ++b) {
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
+        if (!vkeep[grp]) continue;
         const int r0 = grp * 16 + g, r1 = r0 + 8;
         const float v0 = __half2float(__ushort_as_half(vnr[r0 * NBV + b]));
         const float v1 = __half2float(__ushort_as_half(vnr[r1 * NBV + b]));
@@ -598,6 +610,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     for (int b = 0; b < NBV; ++b) {
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
+        if (!vkeep[grp]) continue;
         const uint32_t pb0 = pw32[(b * 8 + g) * WS::PSTR + grp * 8 + c];
         const uint32_t pb1 = pw32[(b * 8 + g) * WS::PSTR + grp * 8 + c + 4];
         const int kr = grp * 16;

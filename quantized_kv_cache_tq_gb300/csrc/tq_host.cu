@@ -353,12 +353,13 @@ size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_h
 // fused into the tensor-core kernel, else as two SET_ROWS launches before it.
 static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk, const tq_codebook *cbv,
                              const void *k_row, const void *v_row, int src_type, const int64_t *cell_id,
-                             const float *q, int n_q_heads, int64_t kv_len, float scale, int algo, float *out,
-                             void *workspace, size_t workspace_bytes, tq_stream stream) {
+                             const float *q, int n_q_heads, int64_t kv_len, float scale, float v_thresh,
+                             int algo, float *out, void *workspace, size_t workspace_bytes, tq_stream stream) {
   tq_status st = check_decode_pair(k, v, n_q_heads, kv_len);
   if (st != TQ_OK) return st;
   if (!codebook_ok(cbk, k->type) || !codebook_ok(cbv, v->type)) return TQ_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out) || !isfinite(scale)) return TQ_ERR_INVALID_ARG;
+  if (!(v_thresh >= 0.f) || !isfinite(v_thresh)) return TQ_ERR_INVALID_ARG;
   if (algo != TQ_DECODE_AUTO && algo != TQ_DECODE_LUT && algo != TQ_DECODE_MMA)
     return TQ_ERR_INVALID_ARG;
   const bool append = k_row != nullptr;
@@ -422,6 +423,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.nbv = v->n_blocks;
   a.part_stride = 128 * v->n_blocks;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.v_thresh = v_thresh;
   a.cbk = to_dev(cbk);
   a.cbv = to_dev(cbv);
   code_byte_tables(cbk, k->type, a.tabk);
@@ -443,8 +445,16 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
                           const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
                           float scale, int algo, float *out, void *workspace,
                           size_t workspace_bytes, tq_stream stream) {
-  return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, q, n_q_heads, kv_len, scale, algo, out,
+  return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, q, n_q_heads, kv_len, scale, 0.f, algo, out,
                      workspace, workspace_bytes, stream);
+}
+
+tq_status tq_fattn_decode_sparse_v(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                                   const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
+                                   float scale, float v_threshold, int algo, float *out, void *workspace,
+                                   size_t workspace_bytes, tq_stream stream) {
+  return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, q, n_q_heads, kv_len, scale, v_threshold, algo,
+                     out, workspace, workspace_bytes, stream);
 }
 
 tq_status tq_fattn_decode_append(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
@@ -453,7 +463,7 @@ tq_status tq_fattn_decode_append(const tq_cache *k, const tq_cache *v, const tq_
                                  float scale, int algo, float *out, void *workspace, size_t workspace_bytes,
                                  tq_stream stream) {
   if (!k_row) return TQ_ERR_INVALID_ARG;
-  return decode_call(k, v, cbk, cbv, k_row, v_row, src_type, cell_id, q, n_q_heads, kv_len, scale, algo, out,
+  return decode_call(k, v, cbk, cbv, k_row, v_row, src_type, cell_id, q, n_q_heads, kv_len, scale, 0.f, algo, out,
                      workspace, workspace_bytes, stream);
 }
 
