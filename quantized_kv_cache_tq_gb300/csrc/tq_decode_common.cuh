@@ -13,6 +13,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Order-preserving map of a float to an int (for integer max atomics) and back.
+__device__ __forceinline__ int ordered_int(float x) {
+  const int b = __float_as_int(x);
+  return b >= 0 ? b : b ^ 0x7fffffff;
+}
+__device__ __forceinline__ float ordered_float(int b) { return __int_as_float(b >= 0 ? b : b ^ 0x7fffffff); }
+
 // Floats of shared memory decode_merge needs.
 __host__ __device__ inline int merge_smem_floats(int group, int nbv, int n_splits) {
   return group * QK * nbv + 2 * group * n_splits;

@@ -245,7 +245,7 @@ __device__ void cluster_merge(const DecodeArgs &a, int hk, const float *cpart, f
   tc::cluster_sync();
 }
 
-template <int T, int G, int NBK, int NBV>
+template <int T, int G, int NBK, int NBV, bool SV>
 __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kernel(const DecodeArgs a) {
   static_assert(G == 1 || G == 2 || G == 4, "GQA group must be 1, 2 or 4");
   using WS = WarpStage<T, NBK, NBV>;
@@ -402,6 +402,8 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   // zero for h >= G
   if (warp < G * NBK) rotate_query_block(a, warp, lane, qv, qrot);
   for (int i = lane; i < NBV * 8 * WS::PSTR; i += 32) pw32[i] = 0;
+  __shared__ int s_mref[4];                 // largest score published per query head (sparse V)
+  if (SV && tid < 4) s_mref[tid] = ordered_int(-INFINITY);
   __syncthreads();
   uint16_t *qcol = reinterpret_cast<uint16_t *>(smem + WQ::QC);              // [8][128*NBK]
   for (int i = tid; i < 8 * 128 * NBK; i += NT) {
@@ -544,11 +546,27 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
 
     // ---- online softmax of head c (log2 domain); the reference maximum is raised
     // only when the running maximum grows by more than 2^8 (then O and l rescale)
+    bool vkeep[2] = {true, true};
     {
       float tm = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
       tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+      // sparse V ([TQ#36] "VEC tuning"): a group of 16 keys whose weights,
+      // relative to the largest score known so far, are below the threshold for
+      // every query head of the warp adds nothing to O' (its weights still count
+      // in l).  The largest known score is this group's or one that a warp of
+      // the CTA published (`s_mref`), never above the final maximum, so every
+      // key left out is below the threshold relative to the final maximum too.
+      if (SV) {
+        if (g == 0 && has_head) atomicMax(&s_mref[c], ordered_int(tm));
+        const float mref = has_head ? fmaxf(tm, ordered_float(*reinterpret_cast<volatile int *>(&s_mref[c & 3])))
+                                    : tm;
+        const float cut = mref + a.v_log2_thresh;
+#pragma unroll
+        for (int grp = 0; grp < 2; ++grp)
+          vkeep[grp] = __any_sync(0xffffffffu, has_head && (sc[grp][0] >= cut || sc[grp][1] >= cut));
+      }
       if (tm > m_run + 8.f) {
         const float fct = (m_run == -INFINITY) ? 0.f : fast_ex2(m_run - tm);
         l_run *= fct;
@@ -568,17 +586,6 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
           l_run += sc[grp][r];
         }
     }
-    // sparse V ([TQ#36] "VEC tuning"): a group of 16 keys whose weights, relative
-    // to the reference maximum, are below the threshold for every query head of
-    // the warp adds nothing to O' (its weights still count in l).  The reference
-    // maximum trails the running maximum by less than 2^8, so the keys left out
-    // have weights below the threshold relative to the final maximum too.
-    bool vkeep[2] = {true, true};
-    if (a.v_thresh > 0.f) {
-#pragma unroll
-      for (int grp = 0; grp < 2; ++grp)
-        vkeep[grp] = __any_sync(0xffffffffu, has_head && (sc[grp][0] >= a.v_thresh || sc[grp][1] >= a.v_thresh));
-    }
 
     // ---- P' = p * |v| (per V block) as binary16 (hi, lo) key pairs: column 2c (hi)
     // and 2c + 1 (lo), pair g of group grp = keys (grp*16 + g, grp*16 + g + 8)
@@ -586,7 +593,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     for (int b = 0; b < NBV; ++b) {
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
-        if (!vkeep[grp]) continue;
+        if (SV && !vkeep[grp]) continue;
         const int r0 = grp * 16 + g, r1 = r0 + 8;
         const float v0 = __half2float(__ushort_as_half(vnr[r0 * NBV + b]));
         const float v1 = __half2float(__ushort_as_half(vnr[r1 * NBV + b]));
@@ -610,7 +617,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     for (int b = 0; b < NBV; ++b) {
 #pragma unroll
       for (int grp = 0; grp < 2; ++grp) {
-        if (!vkeep[grp]) continue;
+        if (SV && !vkeep[grp]) continue;
         const uint32_t pb0 = pw32[(b * 8 + g) * WS::PSTR + grp * 8 + c];
         const uint32_t pb1 = pw32[(b * 8 + g) * WS::PSTR + grp * 8 + c + 4];
         const int kr = grp * 16;
@@ -700,7 +707,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   }
 }
 
-template <int T, int G, int NBK, int NBV>
+template <int T, int G, int NBK, int NBV, bool SV>
 cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
   constexpr uint32_t bytes = smem_bytes<T, G, NBK, NBV>();
   static_assert(bytes <= 227 * 1024, "shared memory");
@@ -710,7 +717,7 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
                 "merge region");
   static_assert(WarpStage<T, NBK, NBV>::QR - WarpStage<T, NBK, NBV>::PT >= 4 * (2 * G + G * 128 * NBV),
                 "P-tile region too small for the CTA partial");
-  auto kern = decode_mma_kernel<T, G, NBK, NBV>;
+  auto kern = decode_mma_kernel<T, G, NBK, NBV, SV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -737,7 +744,8 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
 template <int T>
 cudaError_t launch_type(const DecodeArgs &a, cudaStream_t s) {
 #define TQ_DEC_CASE(GG, BK, BV) \
-  if (a.group == GG && a.nbk == BK && a.nbv == BV) return launch_one<T, GG, BK, BV>(a, s);
+  if (a.group == GG && a.nbk == BK && a.nbv == BV)                      \
+    return a.v_thresh > 0.f ? launch_one<T, GG, BK, BV, true>(a, s) : launch_one<T, GG, BK, BV, false>(a, s);
   TQ_DEC_CASE(4, 1, 1)
   TQ_DEC_CASE(2, 1, 1)
   TQ_DEC_CASE(1, 1, 1)

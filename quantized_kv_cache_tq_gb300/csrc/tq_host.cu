@@ -424,6 +424,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.part_stride = 128 * v->n_blocks;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.v_thresh = v_thresh;
+  a.v_log2_thresh = v_thresh > 0.f ? log2f(v_thresh) : -INFINITY;
   a.cbk = to_dev(cbk);
   a.cbv = to_dev(cbv);
   code_byte_tables(cbk, k->type, a.tabk);

@@ -60,6 +60,7 @@ struct DecodeArgs {
   int32_t part_stride;    // words per (head, split) partial output (128 nbv)
   float scale_log2;       // softmax scale * log2(e)
   float v_thresh;         // sparse V: weight relative to the running maximum below which V is skipped (0 = off)
+  float v_log2_thresh;    // log2(v_thresh)
   DevCodebook cbk, cbv;
   uint32_t tabk[4], tabv[4];   // binary16 byte tables of the code values (see code_byte_tables)
   // append: the new token's K / V rows ([n_kv_heads][dk], [n_kv_heads][dv] of
