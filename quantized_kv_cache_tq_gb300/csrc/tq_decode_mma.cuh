@@ -325,30 +325,29 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   __shared__ __align__(16) uint8_t patch[PN + 2 * (NBK + NBV)];
   __shared__ __align__(8) uint64_t patch_bar;
   constexpr int QWARP = NW - 1;
-  // A CTA barrier waits for every load issued before it: the cell id goes out
-  // with the query loads (one lane per CTA: the same 8 bytes read by every warp
-  // of the grid queue up at one L2 line for about a microsecond); the CTA that
-  // owns the cell stages the token's rows in `rowbuf` with cp.async after the
-  // first barrier (the later barriers do not wait for those copies), or, for
-  // rows that are not 16-byte aligned per head, loads them into registers.
+  // A CTA barrier waits for every load issued before it: the cell id and the
+  // epoch go out with the query loads, then each warp's first bulk copy, then
+  // the first barrier (one lane per CTA reads the cell id: the same 8 bytes read
+  // by every warp of the grid queue up at one L2 line for about a microsecond).
+  // The CTA that owns the cell stages the token's rows in `rowbuf` with cp.async
+  // after the first barrier (the later barriers do not wait for those copies),
+  // or, for rows that are not 16-byte aligned per head, loads them into registers.
   const bool append = a.cell_id != nullptr;
   __shared__ int64_t s_cell;
   __shared__ uint32_t s_epoch;
   __shared__ __align__(16) unsigned char rowbuf[(NBK + NBV) * QK * 4];
+  uint32_t e_ld = 0;
+  int64_t c_ld = -1;
   if (warp == QWARP && lane == 0) {
-    const uint32_t e = load_epoch(a, hk);
-    s_cell = append ? __ldg(a.cell_id) : -1;
-    s_epoch = e;
+    e_ld = load_epoch(a, hk);
+    if (append) c_ld = __ldg(a.cell_id);
   }
-  __syncthreads();
-  const int64_t cell = s_cell;
-  const bool cell_ok = cell >= 0 && cell < a.n_cells;
-  const bool owner = append && cell_ok && ((cell >= t0 && cell < t1) || (cell >= a.kv_len && split == 0));
-  if (append && !cell_ok && split == 0 && tid == 0) set_status(a.status, TQ_ERR_DEVICE_CHECK);
-  // The first group alone goes first: every CTA's first 32 keys are in the
-  // first wave of HBM traffic, so the compute starts as early as it can.  With
-  // 64-key stages the second group follows after the prologue on its own
-  // barrier; the other stages once the first has landed.
+  // Each warp's barriers and ring are its own, so lane 0 sets them up and sends
+  // the first copy before the first CTA barrier.  The first group alone goes
+  // first: every CTA's first 32 keys are in the first wave of HBM traffic, so
+  // the compute starts as early as it can.  With 64-key stages the second group
+  // follows after the prologue on its own barrier; the other stages once the
+  // first has landed.
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) tc::mbar_init(&full[warp][s], 1);
@@ -361,7 +360,15 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
       else issue(0);
     }
   }
-
+  if (warp == QWARP && lane == 0) {
+    s_cell = c_ld;
+    s_epoch = e_ld;
+  }
+  __syncthreads();
+  const int64_t cell = s_cell;
+  const bool cell_ok = cell >= 0 && cell < a.n_cells;
+  const bool owner = append && cell_ok && ((cell >= t0 && cell < t1) || (cell >= a.kv_len && split == 0));
+  if (append && !cell_ok && split == 0 && tid == 0) set_status(a.status, TQ_ERR_DEVICE_CHECK);
   const int gq = lane >> 2, l4 = lane & 3;                  // block of the quantising warp's lane group
   const bool qblk = gq < NBK + NBV;
   float nv[8][4];
