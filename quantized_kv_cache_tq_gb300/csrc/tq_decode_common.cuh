@@ -3,6 +3,7 @@
 #pragma once
 
 #include "tq_common.cuh"
+#include "tq_tc.cuh"
 
 namespace tq {
 
@@ -163,6 +164,88 @@ __device__ void decode_merge(const DecodeArgs &a, int hk, uint32_t epoch, float 
     a.counters[hk] = 0;
     a.epochs[hk] = epoch + 1u;
   }
+}
+
+// Merge of one output block (query head h = hk * group + g, V block b) over all
+// splits by 128 threads of one CTA (warps w0 .. w0 + 3, thread t = output d of
+// the block), used when every CTA of the grid is resident (a cooperative launch):
+// the block's partial words of all splits are loaded, 24 splits per round trip,
+// and loaded again (bounded) until every tag is this launch's, i.e. until every
+// split has stored its partial; then the merge, the inverse rotation by warp w0
+// and the store of out[h][128 b ..].  `buf` holds 128 floats of shared memory and
+// named barrier `bar_id` is free for these 128 threads.  Returns false if a
+// split's partial never arrived (the bound ran out).
+__device__ __forceinline__ bool merge_block(const DecodeArgs &a, int hk, int g, int b, uint32_t tag, int t, int bar_id, float *buf) {
+  const int ns = a.n_splits, G = a.group, lane = t & 31;
+  const int h = hk * G + g;
+  const uint64_t *pml = a.part_ml + static_cast<size_t>(h) * ns * 2;
+  const uint64_t *po = a.part + static_cast<size_t>(h) * ns * a.part_stride + b * QK + t;
+  float M = -INFINITY, L = 0.f, o = 0.f;
+  bool arrived = true;
+  for (int s0 = 0; s0 < ns; s0 += 24) {
+    const int n = min(24, ns - s0);
+    const uint64_t *ps = po + static_cast<size_t>(s0) * a.part_stride;
+    uint64_t wm = 0, wl = 0, wo[24];
+    for (int tries = 0;; ++tries) {
+      if (lane < n) {
+        wm = ld_tagged(pml + 2 * (s0 + lane));
+        wl = ld_tagged(pml + 2 * (s0 + lane) + 1);
+      }
+#pragma unroll
+      for (int j = 0; j < 24; ++j) wo[j] = (j < n) ? ld_tagged(ps + static_cast<size_t>(j) * a.part_stride) : 0;
+      bool ok = lane >= n || (tagged_ok(wm, tag) && tagged_ok(wl, tag));
+#pragma unroll
+      for (int j = 0; j < 24; ++j) ok = ok && (j >= n || tagged_ok(wo[j], tag));
+      if (__all_sync(0xffffffffu, ok)) break;
+      if (tries >= (1 << 16)) {
+        arrived = false;
+        break;
+      }
+      __nanosleep(64);
+    }
+    const float ms = (lane < n) ? tagged_value(wm) : -INFINITY, ls = (lane < n) ? tagged_value(wl) : 0.f;
+    const float Mn = fmaxf(M, warp_max(ms));
+    const float f = (M == -INFINITY) ? 0.f : fast_exp2(M - Mn);
+    const float w = (ms == -INFINITY) ? 0.f : fast_exp2(ms - Mn);
+    L = L * f + warp_sum(w * ls);
+    o *= f;
+#pragma unroll
+    for (int j = 0; j < 24; ++j) o = fmaf(__shfl_sync(0xffffffffu, w, j), tagged_value(wo[j]), o);
+    M = Mn;
+  }
+  buf[t] = (L > 0.f) ? o / L : 0.f;
+  tc::named_sync(bar_id, 128);
+  if (t < 32) {
+    float v[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v[r] = buf[4 * lane + r];
+    wht128_warp(v, lane);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v[r] *= kInvSqrtQK;
+    apply_signs(v, a.cbv, lane);
+    float *out = a.out + static_cast<size_t>(h) * a.dv;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int d = b * QK + 4 * lane + r;
+      if (d < a.dv) out[d] = v[r];
+    }
+  }
+  tc::named_sync(bar_id, 128);                  // buf free again
+  return __all_sync(0xffffffffu, arrived);
+}
+
+// The cooperative split merge of KV head hk, run by threads 0..127 of every CTA
+// of the head after it stored its partial: CTA `split` merges output blocks
+// u = split, split + n_splits, ... of the group * nbv blocks; split 0 advances
+// the head's epoch (every CTA of the head has read it by the time its merge
+// found all partials).
+__device__ __forceinline__ void coop_merge(const DecodeArgs &a, int hk, int split, uint32_t epoch, float *buf) {
+  const int t = threadIdx.x;
+  bool arrived = true;
+  for (int u = split; u < a.group * a.nbv; u += a.n_splits)
+    arrived = merge_block(a, hk, u / a.nbv, u % a.nbv, split_tag(epoch), t, 1, buf) && arrived;
+  if (!arrived && (t & 31) == 0) set_status(a.status, TQ_ERR_TIMEOUT);
+  if (split == 0 && t == 0) a.epochs[hk] = epoch + 1u;
 }
 
 // Query block wb = g * nbk + b (head hk * group + g, dims 128 b ..): lane i

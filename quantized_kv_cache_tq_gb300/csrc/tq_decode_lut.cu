@@ -219,13 +219,18 @@ __global__ void __launch_bounds__(kThreads) decode_lut_kernel(const DecodeArgs a
       for (int g = 0; g < G; ++g) acc[g] += accbuf[g * dvp + d];
   }
   int prev = 0;
-  if (tid == 0) prev = split_arrive(a, hk);
+  if (!a.coop && tid == 0) prev = split_arrive(a, hk);
   const uint32_t epoch = s_epoch, tag = split_tag(epoch);
   if (kr == 0) {
     for (int g = 0; g < G; ++g) {
       store_partial_o(a, hk * G + g, split, d, acc[g], tag);
       if (d == 0) store_partial_ml(a, hk * G + g, split, m_run[g], l_run[g], tag);
     }
+  }
+  if (a.coop) {
+    __syncthreads();                      // the table region becomes the merge buffer
+    if (tid < 128) coop_merge(a, hk, split, epoch, lut);
+    return;
   }
   if (tid == 0) s_last = (prev == a.n_splits - 1);
   __syncthreads();
@@ -242,9 +247,20 @@ cudaError_t launch_kt_vt(const DecodeArgs &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(decode_lut_kernel<KT, VT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.n_splits, a.n_kv_heads);
-  decode_lut_kernel<KT, VT><<<grid, kThreads, bytes, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_splits, a.n_kv_heads);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (a.coop) {                           // every CTA resident: each merges a share (coop_merge)
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, decode_lut_kernel<KT, VT>, a);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 template <int KT>

@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   // round trip overlaps the CTA merge and the stores.
   const bool in_cluster = tc::cluster_size() == static_cast<uint32_t>(a.n_splits);
   int prev = 0;
-  if (!in_cluster && tid == 0) prev = split_arrive(a, hk);
+  if (!in_cluster && !a.coop && tid == 0) prev = split_arrive(a, hk);
   const uint32_t epoch = s_epoch, tag = split_tag(epoch);
   float *cpart = reinterpret_cast<float *>(smem + WS::PT);      // m[G], l[G], o'[G][DVP]
   for (int i = tid; i < G * DVP; i += NT) {
@@ -706,6 +706,10 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   }
   if (in_cluster) {
     cluster_merge<G, NBV, NT>(a, hk, cpart, qrot);
+  } else if (a.coop) {
+    // every CTA is resident: the head's output blocks are merged by its first
+    // CTAs, one block each, as soon as all partials are there
+    if (tid < 128) coop_merge(a, hk, split, epoch, qrot);
   } else {
     __shared__ int s_last;
     if (tid == 0) s_last = (prev == a.n_splits - 1);
@@ -733,8 +737,11 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  // one cluster per KV head, all resident together (else the last-CTA merge)
+  // one cluster per KV head, all resident together; else, when the whole grid
+  // fits on the GPU at once, a cooperative launch (every CTA merges a share);
+  // else the last-CTA merge
   const int want = min(a.n_kv_heads, max(1, sm_count() / a.n_splits));
+  DecodeArgs b = a;
   if (a.n_splits > 1 && cluster_merge_ok(reinterpret_cast<const void *>(kern), a.n_splits,
                                          WarpStage<T, NBK, NBV>::NT, bytes, want)) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -743,8 +750,14 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    b.coop = 0;
+  } else if (a.coop) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
   }
-  e = cudaLaunchKernelEx(&cfg, kern, a);
+  e = cudaLaunchKernelEx(&cfg, kern, b);
   return e == cudaSuccess ? cudaGetLastError() : e;
 }
 

@@ -84,8 +84,10 @@ DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int6
   DecodeWorkspaceLayout L;
   // about one CTA per SM (with at most 16 splits per KV head the splits run as
   // one thread-block cluster and merge on chip, see the decode kernels)
+  // at most one CTA per SM in all, so that the grid can run as one cooperative launch
   const int target_ctas = sm_count();
-  int per_head = (target_ctas + n_kv_heads - 1) / n_kv_heads;
+  int per_head = target_ctas / n_kv_heads;
+  if (per_head < 1) per_head = 1;
   if (per_head > 256) per_head = 256;
   int64_t chunk = (kv_len + per_head - 1) / per_head;
   chunk = (chunk + 63) / 64 * 64;
@@ -424,6 +426,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.part_stride = 128 * v->n_blocks;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.v_thresh = v_thresh;
+  a.coop = static_cast<int64_t>(L.n_splits) * k->n_kv_heads <= sm_count();
   a.v_log2_thresh = v_thresh > 0.f ? log2f(v_thresh) : -INFINITY;
   a.cbk = to_dev(cbk);
   a.cbv = to_dev(cbv);

@@ -70,6 +70,7 @@ struct DecodeArgs {
   const int64_t *cell_id;
   int32_t src_type;
   int32_t row_async;      // every head's source rows start 16-byte aligned: staged by cp.async
+  int32_t coop;           // the grid fits on the GPU at once: cooperative launch, merge by every CTA
 };
 
 struct PrefillArgs {
