@@ -154,7 +154,9 @@ size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_h
  *   out[h][:] = softmax_t(scale * q[h] . k_t) v_t      k_t, v_t dequantised rows
  * with query head h reading KV head h / (n_q_heads / n_kv_heads).  The key range
  * is split across CTAs; each split keeps a running max/sum and the merge is a
- * log-sum-exp combination done by the last CTA of each KV head.
+ * log-sum-exp combination (in a cluster over distributed shared memory; else,
+ * when the grid fits on the GPU at once, a cooperative launch in which each
+ * output block is merged by one CTA; else by the last CTA of each KV head).
  * q    device f32 [n_q_heads][k->head_dim]
  * out  device f32 [n_q_heads][v->head_dim]
  * algo tq_decode_algo.  kv_len = 0 writes zeros.

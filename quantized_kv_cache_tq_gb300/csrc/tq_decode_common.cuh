@@ -80,7 +80,8 @@ __device__ __forceinline__ void store_partial_o(const DecodeArgs &a, int h, int 
   st_tagged(a.part + (static_cast<size_t>(h) * a.n_splits + s) * a.part_stride + d, o, tag);
 }
 
-// Run by every thread of the last CTA of KV head hk to arrive (its own partial
+// Run, when the grid is larger than the GPU holds at once (no cooperative launch),
+// by every thread of the last CTA of KV head hk to arrive (its own partial
 // stored and a CTA barrier passed).  Merges the splits
 //   M = max_s m_s,  L = sum_s l_s 2^(m_s - M),  o' = sum_s o'_s 2^(m_s - M) / L
 // (scores are kept in the log2 domain), rotates back with the V codebook,
