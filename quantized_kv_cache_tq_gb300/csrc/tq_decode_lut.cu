@@ -260,6 +260,13 @@ cudaError_t launch_kt_vt(const DecodeArgs &a, cudaStream_t s) {
     cfg.numAttrs = 1;
   }
   e = cudaLaunchKernelEx(&cfg, decode_lut_kernel<KT, VT>, a);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {          // fewer SMs available than the device has
+    cudaGetLastError();
+    DecodeArgs b = a;
+    b.coop = 0;
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, decode_lut_kernel<KT, VT>, b);
+  }
   return e == cudaSuccess ? cudaGetLastError() : e;
 }
 

@@ -758,6 +758,12 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
     cfg.numAttrs = 1;
   }
   e = cudaLaunchKernelEx(&cfg, kern, b);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {          // fewer SMs available than the device has
+    cudaGetLastError();
+    b.coop = 0;
+    cfg.numAttrs = 0;
+    e = cudaLaunchKernelEx(&cfg, kern, b);
+  }
   return e == cudaSuccess ? cudaGetLastError() : e;
 }
 

@@ -130,3 +130,22 @@ def test_graph_replay_and_workspace_reuse():
     ref = O.decode(kc, vc, sk, sv, O.centroids(3), O.centroids(3), q.cpu().numpy().astype(np.float64),
                    4096, scale_of(128))
     compare_outputs(out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_more_kv_heads_than_sms_uses_last_cta_merge(algo):
+    # 160 KV heads of one query head each: one split per head and 160 CTAs, more
+    # than the GPU holds at once, so no cooperative launch; the last CTA of each
+    # head (here its only one) merges
+    sh = W.AttnShape("many_heads", 160, 160, 128, 128, 600, seed=17)
+    kc, vc, sk, sv = _setup(sh, 3, 3)
+    q = W.decode_query(sh)
+    out, ref = _decode_pair(kc, vc, sk, sv, q, sh.kv_len, algo)
+    compare_outputs(out, ref)
+
+
+def test_more_than_256_kv_heads_rejected():
+    import quantized_kv_cache_tq_gb300 as tq
+    from quantized_kv_cache_tq_gb300 import _lib
+    c = tq.TqCache(3, 257, 128, 64)
+    assert _lib.tq_fattn_decode_workspace(c.c, c.c, 257, 64) == 0
