@@ -285,12 +285,12 @@ def run_tq(args):
     ws = tq.workspace(ws_bytes, dev)
     scale = 1.0 / math.sqrt(D)
 
-    def token(decode_only=False):
+    def token(decode_only=False, qs=q_all, kr=newk, vr=newv):
         for b in range(B):
             if decode_only:
-                tq.fattn_decode(ks[b], vs[b], cbk, cbv, q_all[b], KV_LEN, scale, algo=algo, out=out[b], ws=ws)
+                tq.fattn_decode(ks[b], vs[b], cbk, cbv, qs[b], KV_LEN, scale, algo=algo, out=out[b], ws=ws)
             else:   # SET_ROWS of the token's K and V rows + decode, one call
-                tq.fattn_decode_append(ks[b], vs[b], cbk, cbv, newk[b][0], newv[b][0], cell, q_all[b], KV_LEN,
+                tq.fattn_decode_append(ks[b], vs[b], cbk, cbv, kr[b][0], vr[b][0], cell, qs[b], KV_LEN,
                                        scale, algo=algo, out=out[b], ws=ws)
 
     def capture(fn):
@@ -305,13 +305,13 @@ def run_tq(args):
             fn()
         return g
 
-    g_token = capture(token)
-    g_decode = capture(lambda: token(decode_only=True))
     T = args.tokens_per_step
+    # one graph per step: T tokens x B layers of launches
+    g_step = capture(lambda: [token() for _ in range(T)])
+    g_decode = capture(lambda: token(decode_only=True))
 
     def step():
-        for _ in range(T):
-            g_token.replay()
+        g_step.replay()
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -355,7 +355,9 @@ def run_tq(args):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
     # e2e through the public API with host buffers: per step the T tokens' inputs go
-    # host->device from pinned memory and the last token's outputs come back
+    # host->device from pinned memory into the step's device buffers, which the step
+    # graph reads (token t of layer b from d_q[t][b], d_k[t][b], d_v[t][b]), and the
+    # last token's outputs come back
     h_q = torch.empty((T, B, N_Q, D), dtype=torch.float32).pin_memory()
     h_k = torch.empty((T, B, 1, N_KV, D), dtype=torch.float32).pin_memory()
     h_v = torch.empty((T, B, 1, N_KV, D), dtype=torch.float32).pin_memory()
@@ -366,16 +368,16 @@ def run_tq(args):
     d_q = torch.empty((T, B, N_Q, D), dtype=torch.float32, device=dev)
     d_k = torch.empty((T, B, 1, N_KV, D), dtype=torch.float32, device=dev)
     d_v = torch.empty((T, B, 1, N_KV, D), dtype=torch.float32, device=dev)
+    d_q.copy_(h_q)
+    d_k.copy_(h_k)
+    d_v.copy_(h_v)
+    g_step_e2e = capture(lambda: [token(qs=d_q[t], kr=d_k[t], vr=d_v[t]) for t in range(T)])
 
     def e2e_step():
         d_q.copy_(h_q, non_blocking=True)
         d_k.copy_(h_k, non_blocking=True)
         d_v.copy_(h_v, non_blocking=True)
-        for t in range(T):
-            q_all.copy_(d_q[t])
-            newk.copy_(d_k[t])
-            newv.copy_(d_v[t])
-            g_token.replay()
+        g_step_e2e.replay()
         h_out.copy_(out, non_blocking=True)
 
     e2e_step()
