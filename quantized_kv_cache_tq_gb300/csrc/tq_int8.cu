@@ -51,15 +51,22 @@ constexpr int NWARP = 9;                        // 0-3 softmax, 4-7 gather, 8 co
 constexpr int NT = NWARP * 32;
 constexpr int RING = 4;                         // raw-row ring depth (tiles)
 constexpr int LOOK = RING - 1;                  // copies run this many tiles ahead
-constexpr int NB = 3;                           // K'/V' tiles, scales and S / P' buffers in flight
 constexpr uint32_t SQ = 0;                      // Q       [d/8][row/8]            32 KB
-constexpr uint32_t SK = SQ + 32768;             // K'      NB x [key/8][d/8]      NB x 16 KB
-constexpr uint32_t SV = SK + NB * 16384;        // V'      NB x [key/8][d/8]      NB x 16 KB
-constexpr uint32_t SR = SV + NB * 16384;        // raw     RING x [K|V][key][128 B]
 constexpr uint32_t RSTAGE = 2 * BN * D;
-constexpr uint32_t SSC = SR + RING * RSTAGE;    // scales  NB x [key][k, v] floats
-constexpr uint32_t TOTAL = SSC + NB * BN * 2 * 4;
-constexpr int TMEM_COLS = 512;                  // O: 128 columns, S / P': NB x 64 columns
+// Shared-memory layout per cache mode.  int8 rows pass through the raw ring
+// (RING x 16 KB) and keep three K'/V' buffers; binary16 rows go straight to the
+// operand tiles, so that space holds two more buffers and the copies run four
+// tiles ahead instead of two.
+template <bool F16>
+struct Lay {
+  static constexpr int NB = F16 ? 5 : 3;        // K'/V' tiles, scales and S / P' buffers in flight
+  static constexpr uint32_t SK = SQ + 32768;    // K'      NB x [key/8][d/8]      NB x 16 KB
+  static constexpr uint32_t SV = SK + NB * 16384;   // V'  NB x [key/8][d/8]      NB x 16 KB
+  static constexpr uint32_t SR = SV + NB * 16384;   // raw RING x [K|V][key][128 B] (int8 only)
+  static constexpr uint32_t SSC = SR + (F16 ? 0 : RING * RSTAGE);   // scales  NB x [key][k, v] floats
+  static constexpr uint32_t TOTAL = SSC + NB * BN * 2 * 4;
+};
+constexpr int TMEM_COLS = 512;                  // O: 128 columns, S / P': NB x 64 columns (NB <= 6)
 constexpr uint32_t SP0 = 128;
 
 __device__ __forceinline__ long long i64min(long long x, long long y) { return x < y ? x : y; }
@@ -116,6 +123,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
       : "r"(taddr));
 }
 
+template <int NB>
 struct Bars {               // buffer j % NB, phase (j / NB) & 1
   uint64_t cv[NB];         // K'/V' tile and its scales written (4 gather warps)
   uint64_t sf[NB];         // S_j computed (mma commit)
@@ -127,8 +135,12 @@ struct Bars {               // buffer j % NB, phase (j / NB) & 1
 // (the second cache mode of the same prompt attention).
 template <bool F16>
 __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
+  using L = Lay<F16>;
+  constexpr int NB = L::NB;
+  constexpr uint32_t SK = L::SK, SV = L::SV, SR = L::SR, SSC = L::SSC;
+  static_assert(SP0 + NB * BN <= TMEM_COLS, "tensor memory");
   extern __shared__ __align__(1024) unsigned char smem[];
-  __shared__ __align__(8) Bars bars;
+  __shared__ __align__(8) Bars<NB> bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_fail;
 
@@ -232,6 +244,7 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
       // straight to its core-matrix slot of the K'/V' tile, LOOK16 tiles ahead,
       // once that tile's buffer is free (PV of the tile NB before it is done)
       constexpr int LOOK16 = NB - 1;
+      constexpr int RING16 = LOOK16 + 2;          // cell ids: loaded two tiles before their copies
       const uint8_t *src = reinterpret_cast<const uint8_t *>(is_v ? a.v : a.k) + static_cast<int64_t>(hk) * D * 2;
       const int64_t row_stride = static_cast<int64_t>(a.n_kv_heads) * D * 2;
       auto cell_load = [&](int j) -> int64_t {
@@ -253,18 +266,18 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
         scl[2 * i] = a.scale_log2;
         scl[2 * i + 1] = 1.f;
       }
-      int64_t cb[RING];                           // cb[t % RING]: cell of tile t
+      int64_t cb[RING16];                         // cb[t % RING16]: cell of tile t
 #pragma unroll
-      for (int k = 0; k < RING; ++k) cb[k] = cell_load(k);
+      for (int k = 0; k < RING16; ++k) cb[k] = cell_load(k);
 #pragma unroll
       for (int k = 0; k < LOOK16; ++k) {
         if (k < n_tiles) fetch(k, cb[k]);
         cp_async_commit();
       }
       bool ok = true;
-      for (int j0 = 0; j0 < n_tiles && ok; j0 += RING) {
+      for (int j0 = 0; j0 < n_tiles && ok; j0 += RING16) {
 #pragma unroll
-        for (int u = 0; u < RING; ++u) {
+        for (int u = 0; u < RING16; ++u) {
           const int j = j0 + u;
           if (j >= n_tiles) break;
           // tile j first: the control thread issues PV_{j-1} only after S_j, so
@@ -278,10 +291,10 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
             if (jn >= NB) ok = tc::mbar_wait(&bars.pv[(jn - NB) % NB], ((jn - NB) / NB) & 1);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; s_fail = 1; break; }
             tc::fence_after_sync();
-            fetch(jn, cb[(u + LOOK16) % RING]);
+            fetch(jn, cb[(u + LOOK16) % RING16]);
           }
           cp_async_commit();
-          cb[u] = cell_load(j + RING);
+          cb[u] = cell_load(j + RING16);
         }
       }
     } else {
@@ -488,14 +501,14 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
 }  // namespace i8
 
 cudaError_t launch_int8_attn(const Int8Args &a, cudaStream_t s) {
-  static_assert(i8::TOTAL <= 227 * 1024, "shared memory");
+  static_assert(i8::Lay<false>::TOTAL <= 227 * 1024 && i8::Lay<true>::TOTAL <= 227 * 1024, "shared memory");
   auto kern = a.f16 ? i8::prompt_attn_kernel<true> : i8::prompt_attn_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)i8::TOTAL);
+  const uint32_t total = a.f16 ? i8::Lay<true>::TOTAL : i8::Lay<false>::TOTAL;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)total);
   if (e != cudaSuccess) return e;
   const int rows = a.nq * a.group;
   dim3 grid((rows + i8::BM - 1) / i8::BM, a.n_kv_heads);
-  kern<<<grid, i8::NT, i8::TOTAL, s>>>(a);
+  kern<<<grid, i8::NT, total, s>>>(a);
   return cudaGetLastError();
 }
 
