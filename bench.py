@@ -119,6 +119,11 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def whole_job_rate(units_per_rank: int, world: int, seconds_max: float) -> float:
+    """Units all ranks processed, divided by the slowest rank's time (weak scaling)."""
+    return units_per_rank * world / seconds_max
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -343,7 +348,7 @@ def run_tq(args):
     dec_us = d0.elapsed_time(d1) * 1000.0 / (R * B)
 
     calls = args.steps * T * B
-    value = calls * world / (ms / 1000.0)
+    value = whole_job_rate(calls, world, ms / 1000.0)
     dec_bytes = cache_bytes + 4 * (N_Q * D * 2)
     achieved = dec_bytes / (dec_us * 1e-6) / 1e9
     peaks = {}
