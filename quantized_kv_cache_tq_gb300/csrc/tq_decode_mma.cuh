@@ -672,8 +672,10 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   __syncthreads();
   // CTA partial over the warps.  Launched as one cluster per KV head (cluster
   // size == n_splits) the partial stays in this CTA's shared memory for the
-  // cluster merge; otherwise it goes to the workspace, tagged, for the last-CTA
-  // merge.  The CTA arrives at its head's counter first, so that the atomic's
+  // cluster merge; otherwise it goes to the workspace, tagged, for the
+  // cooperative merge (every CTA resident: each output block merged by one CTA
+  // of the head) or, for a grid larger than the GPU holds, the last-CTA merge.
+  // There the CTA arrives at its head's counter first, so that the atomic's
   // round trip overlaps the CTA merge and the stores.
   const bool in_cluster = tc::cluster_size() == static_cast<uint32_t>(a.n_splits);
   int prev = 0;
