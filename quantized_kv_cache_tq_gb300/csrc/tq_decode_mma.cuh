@@ -481,12 +481,14 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   float m_run = -INFINITY, l_run = 0.f;
   bool timed_out = false;
 
+  // the group of this warp that holds the appended cell, if any
+  const int patch_it = (owner && cell >= w0 && cell < w1) ? static_cast<int>((cell - w0) / WK) : -1;
   for (int it = 0; it < n_it; ++it) {
     const int si = it / WS::SUB, j = it % WS::SUB;             // stage, 32-key group inside it
     if (j == 0 || (WS::SUB == 2 && it == 1)) {
-      const bool ok = (it == 1 && WS::SUB == 2) ? tc::mbar_wait(&first_b[warp], 0)
-                                                : tc::mbar_wait(&full[warp][si % STAGES], (si / STAGES) & 1);
-      if (!__all_sync(0xffffffffu, ok)) { timed_out = true; break; }
+      const bool ok = (it == 1 && WS::SUB == 2) ? tc::mbar_wait_warp(&first_b[warp], 0)
+                                                : tc::mbar_wait_warp(&full[warp][si % STAGES], (si / STAGES) & 1);
+      if (!ok) { timed_out = true; break; }
       // the other stages only once the first has landed: issued earlier, every
       // CTA's later stages compete with the other CTAs' first stages for HBM
       if (it == 0 && lane == 0)
@@ -494,10 +496,10 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     }
     const unsigned char *st = ring + (si % STAGES) * WS::BYTES;
     const int64_t key0 = w0 + static_cast<int64_t>(it) * WK;
-    if (owner && cell >= key0 && cell < key0 + WK && cell < w1) {
+    if (it == patch_it) {
       // the appended cell is in this group (landed): its freshly quantised bytes
       // replace whatever the bulk copy read
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&patch_bar, 0))) { timed_out = true; break; }
+      if (!tc::mbar_wait_warp(&patch_bar, 0)) { timed_out = true; break; }
       const int row = static_cast<int>(cell - key0) + j * WK;                 // row inside the stage
       unsigned char *sw = ring + (si % STAGES) * WS::BYTES;
       constexpr int QW = QSB / 4, SW = SGB / 4;

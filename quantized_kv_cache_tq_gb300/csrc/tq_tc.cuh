@@ -119,6 +119,22 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 }
 
 // Bounded wait for phase `parity` of `bar` without a suspend-time hint: each
+// mbar_wait for a whole warp (all 32 lanes call it): the loop condition is a
+// warp vote, so the lanes never diverge.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, long long limit = 1ll << 20) {
+  const uint32_t a = smem_u32(bar);
+  for (long long it = 0; it < limit; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity), "r"(20000u)
+        : "memory");
+    if (__all_sync(0xffffffffu, ok != 0)) return true;
+  }
+  return false;
+}
+
 // 16-byte asynchronous copy global -> shared reading `src_bytes` (0..16) bytes and
 // zero-filling the rest; both addresses 16-byte aligned.  CTA barriers do not wait
 // for it: cp_async_wait_all does.
