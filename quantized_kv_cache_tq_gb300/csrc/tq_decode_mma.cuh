@@ -491,8 +491,11 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
       if (!ok) { timed_out = true; break; }
       // the other stages only once the first has landed: issued earlier, every
       // CTA's later stages compete with the other CTAs' first stages for HBM
-      if (it == 0 && lane == 0)
-        for (int i = 1; i < STAGES && i < n_st; ++i) issue(i);
+      if (it == 0) {
+        if (lane == 0)
+          for (int i = 1; i < STAGES && i < n_st; ++i) issue(i);
+        __syncwarp();
+      }
     }
     const unsigned char *st = ring + (si % STAGES) * WS::BYTES;
     const int64_t key0 = w0 + static_cast<int64_t>(it) * WK;
@@ -646,7 +649,10 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     }
     __syncwarp();
     // the stage is free again after its last group
-    if (lane == 0 && (j == WS::SUB - 1 || it == n_it - 1) && si + STAGES < n_st) issue(si + STAGES);
+    if ((j == WS::SUB - 1 || it == n_it - 1) && si + STAGES < n_st) {     // warp-uniform
+      if (lane == 0) issue(si + STAGES);
+      __syncwarp();
+    }
   }
 
   // ---- per-warp results -> this warp's ring (all its copies have landed), CTA merge
