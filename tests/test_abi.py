@@ -121,3 +121,20 @@ def test_decode_workspace_grows_with_splits():
     big = L.tq_fattn_decode_workspace(k, k, 32, 32768)
     assert 0 < small < big
     assert big % 256 == 0
+
+
+def test_sparse_v_and_head_limit_checks_reject_before_launch():
+    L = _lib()
+    cb = L.tq_codebook_init(3, [1, 2, 3, 4])
+    k, v = _fake_cache(L), _fake_cache(L)
+    need = L.tq_fattn_decode_workspace(k, v, 4, 64)
+    assert need >= 256 + 1024                      # status header + the per-head epoch words
+    for thr in (-1e-3, float("nan"), float("inf")):
+        assert L.tq_fattn_decode_sparse_v(k, v, cb, cb, 1 << 23, 4, 64, 0.1, thr, 0, 1 << 24, 1 << 25, need,
+                                          None) == L.TQ_ERR_INVALID_ARG
+    # more than 256 KV heads: no decode workspace, decode rejected
+    big = _fake_cache(L, h=257)
+    assert L.tq_fattn_decode_workspace(big, big, 257, 64) == 0
+    assert L.tq_fattn_decode(big, big, cb, cb, 1 << 23, 257, 64, 0.1, 0, 1 << 24, 1 << 25, 1 << 30,
+                             None) == L.TQ_ERR_INVALID_ARG
+    assert L.tq_fattn_decode_workspace(_fake_cache(L, h=256), _fake_cache(L, h=256), 256, 64) > 0
