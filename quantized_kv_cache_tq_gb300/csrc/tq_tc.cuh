@@ -145,23 +145,6 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_b
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// try_wait returns after a short system-defined time when the phase is not
-// complete, and the loop tries again.  false if the limit was reached (well
-// under a minute).
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, long long limit = 1ll << 24) {
-  const uint32_t a = smem_u32(bar);
-  for (long long it = 0; it < limit; ++it) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
-
 // Bounded wait for phase `parity` of `bar`; false if the limit was reached.
 // Each try_wait may suspend the thread for up to ~20 us (suspend-time hint), so a
 // waiting warp does not spin on the issue slots its neighbours need; the
