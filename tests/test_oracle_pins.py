@@ -446,3 +446,102 @@ def test_nmse_definition():
     b = np.array([1.0, 2.0, 2.0])
     a = b + np.array([0.0, 0.3, 0.0])
     assert abs(O.nmse(a, b) - 0.09 / 9.0) < 1e-15
+
+
+# ---------------------------------------------- rotation order and prefill pins
+
+def test_rotation_applies_signs_before_the_hadamard():
+    # y = H S x / sqrt(128): for x = e_j with sign bit j set, S e_j = -e_j, so
+    # y = -H[:, j] / sqrt(128); with bit j clear and another bit set, y = +H[:, j] / sqrt(128)
+    # (the other order, S H x, would flip one element of H[:, j] instead)
+    H = O.hadamard()
+    for j, bits in ((5, {5}), (5, {9}), (77, {77, 3}), (0, {0, 127})):
+        sb = np.zeros(4, np.uint32)
+        for b in bits:
+            sb[b // 32] |= np.uint32(1 << (b % 32))
+        x = np.zeros(128)
+        x[j] = 1.0
+        want = (-1.0 if j in bits else 1.0) * H[:, j] / math.sqrt(128)
+        assert np.array_equal(O.rotation(sb) @ x, want)
+        _, _, y = O.quantize_blocks(x, sb, O.centroids(3))
+        assert np.allclose(y, want, atol=1e-15)
+    # random x against the page's butterfly applied to the sign-flipped input
+    sb = W.sign_bits(12, W.S_SIGNS_K)
+    x = W.normal(12, 1, 6 * 128).reshape(6, 128)
+    s = np.where([(int(sb[i // 32]) >> (i % 32)) & 1 for i in range(128)], -1.0, 1.0)
+    assert np.allclose(x @ O.rotation(sb).T, O.butterfly_wht(x * s) / math.sqrt(128), atol=1e-14)
+
+
+def _dequant_rows_by_loops(cache, sign_bits, cents, n, head):
+    """Rows of cells 0..n-1 of one head, rebuilt element by element: value of each
+    code (sign-magnitude), the page's butterfly on the block, the sign flips, the
+    norm, and the padding columns dropped."""
+    s = [-1.0 if (int(sign_bits[i // 32]) >> (i % 32)) & 1 else 1.0 for i in range(128)]
+    half = len(cents) // 2
+    rows = []
+    for t in range(n):
+        row = []
+        for b in range(cache.n_blocks):
+            codes = O.unpack_codes(cache.qs[head, t, b], None if cache.signs is None else cache.signs[head, t, b],
+                                   cache.tq_type)
+            vals = [(1.0 if k >= half else -1.0) * cents[half + (k % half)] for k in codes]
+            hv = O.butterfly_wht(np.array(vals))          # H is symmetric: H^T c = H c
+            nrm = float(np.array(cache.norms[head, t, b], np.uint16).view(np.float16))
+            row += [nrm * s[i] * hv[i] / math.sqrt(128) for i in range(128)]
+        rows.append(row[:cache.head_dim])
+    return np.array(rows)
+
+
+def _tiny_asym_caches(seed):
+    # 2 KV heads, Dk = 192 (two blocks, the second zero-padded), Dv = 128; 12 cells
+    # written, of which the calls below attend the first kv_len
+    c = O.centroids(3)
+    sk, sv = W.sign_bits(seed, W.S_SIGNS_K), W.sign_bits(seed, W.S_SIGNS_V)
+    kc = O.empty_cache(3, 2, 192, 64)
+    vc = O.empty_cache(3, 2, 128, 64)
+    O.set_rows(kc, W.gaussian_with_outliers(seed, W.S_K, W.S_K_OUT, 12, 2, 192), np.arange(12), sk, c)
+    O.set_rows(vc, W.gaussian_with_outliers(seed, W.S_V, W.S_V_OUT, 12, 2, 128), np.arange(12), sv, c)
+    return kc, vc, sk, sv, c
+
+
+def test_prefill_causal_gqa_asymmetric_by_loops():
+    # C2's causal rule: query i of nq sits at position kv_len - nq + i and sees keys
+    # 0 .. kv_len - nq + i; query head h reads KV head h // (Hq / Hkv); Dk = 192, Dv = 128
+    kc, vc, sk, sv, c = _tiny_asym_caches(31)
+    kv_len, nq, hq = 9, 3, 4
+    q = W.normal(31, W.S_Q, nq * hq * 192).reshape(nq, hq, 192) * 2.0
+    scale = 1 / math.sqrt(192)
+    out = O.prefill(kc, vc, sk, sv, c, c, q, kv_len, scale, causal=True)
+    assert out.shape == (nq, hq, 128)
+    for hk in range(2):
+        k = _dequant_rows_by_loops(kc, sk, c, kv_len, hk)
+        v = _dequant_rows_by_loops(vc, sv, c, kv_len, hk)
+        for h in (2 * hk, 2 * hk + 1):
+            for i in range(nq):
+                last = kv_len - nq + i                   # 6, 7, 8
+                ref = _loop_attention(q[i:i + 1, h], k[:last + 1], v[:last + 1], scale)[0]
+                assert np.allclose(out[i, h], ref, atol=1e-12)
+    # the rows= subset gives the same rows and zeros elsewhere
+    sub = O.prefill(kc, vc, sk, sv, c, c, q, kv_len, scale, causal=True, rows=np.array([2]))
+    assert np.allclose(sub[2], out[2], atol=1e-14) and not sub[:2].any()
+
+
+def test_prefill_non_causal_by_loops():
+    kc, vc, sk, sv, c = _tiny_asym_caches(32)
+    kv_len, nq, hq = 10, 4, 2                            # GQA 1: head h reads KV head h
+    q = W.normal(32, W.S_Q, nq * hq * 192).reshape(nq, hq, 192)
+    scale = 0.11
+    out = O.prefill(kc, vc, sk, sv, c, c, q, kv_len, scale, causal=False)
+    for h in range(hq):
+        k = _dequant_rows_by_loops(kc, sk, c, kv_len, h)
+        v = _dequant_rows_by_loops(vc, sv, c, kv_len, h)
+        assert np.allclose(out[:, h], _loop_attention(q[:, h], k, v, scale), atol=1e-12)
+
+
+def test_dequantize_cache_matches_loops():
+    kc, vc, sk, sv, c = _tiny_asym_caches(33)
+    for hk in range(2):
+        assert np.allclose(O.dequantize_cache(kc, sk, c, 12, hk), _dequant_rows_by_loops(kc, sk, c, 12, hk),
+                           atol=1e-13)
+        assert np.allclose(O.dequantize_cache(vc, sv, c, 12, hk), _dequant_rows_by_loops(vc, sv, c, 12, hk),
+                           atol=1e-13)
