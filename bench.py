@@ -162,36 +162,59 @@ def per_cache_bytes(tq_type=3):
 
 # ------------------------------------------------------------------ CPU oracle
 
-class OracleSample:
-    """The CPU oracle on a bounded sample of the workload: n_heads of the 8 KV heads
-    (with their 4 query heads each); one step = SET_ROWS of the new token's K/V
-    rows, then decode over all 32768 cells.  Throughput is scaled to 8 heads."""
+def _oracle_worker(head, conn):
+    """One KV head of the oracle in its own process: its K/V rows quantised into
+    32768 cells, its 4 query heads and the new token's rows; each "step" message
+    runs one token-layer (SET_ROWS of the new token's K and V rows into the last
+    cell, then decode of the 4 query heads over 32768 cells)."""
+    import numpy as np
+    import oracle as O
+    import workloads as W
+    sh = W.decode_32k()
+    k = W.gaussian_with_outliers(sh.seed, W.S_K, W.S_K_OUT, KV_LEN, N_KV, D)[:, head:head + 1]
+    v = W.gaussian_with_outliers(sh.seed, W.S_V, W.S_V_OUT, KV_LEN, N_KV, D)[:, head:head + 1]
+    sk, sv = W.codebook_signs(sh)
+    c = O.centroids(3)
+    kc, vc = O.empty_cache(3, 1, D, KV_LEN), O.empty_cache(3, 1, D, KV_LEN)
+    O.set_rows(kc, W.to_f32(k), np.arange(KV_LEN), sk, c)
+    O.set_rows(vc, W.to_f32(v), np.arange(KV_LEN), sv, c)
+    q = W.to_f32(W.decode_query(sh))[4 * head:4 * head + 4].astype(np.float64)
+    newk, newv = W.to_f32(k[-1:]), W.to_f32(v[-1:])
+    cell = np.array([KV_LEN - 1])
+    conn.send("ready")
+    while conn.recv() == "step":
+        O.set_rows(kc, newk, cell, sk, c)
+        O.set_rows(vc, newv, cell, sv, c)
+        O.decode(kc, vc, sk, sv, c, c, q, KV_LEN, 1 / math.sqrt(D))
+        conn.send("done")
 
-    def __init__(self, n_heads=1):
-        import numpy as np
-        import oracle as O
-        import workloads as W
-        self.np, self.O = np, O
-        sh = W.decode_32k()
-        self.hs = hs = n_heads
-        k = W.gaussian_with_outliers(sh.seed, W.S_K, W.S_K_OUT, KV_LEN, N_KV, D)[:, :hs]
-        v = W.gaussian_with_outliers(sh.seed, W.S_V, W.S_V_OUT, KV_LEN, N_KV, D)[:, :hs]
-        self.sk, self.sv = W.codebook_signs(sh)
-        self.c = O.centroids(3)
-        self.kc = O.empty_cache(3, hs, D, KV_LEN)
-        self.vc = O.empty_cache(3, hs, D, KV_LEN)
-        O.set_rows(self.kc, W.to_f32(k), np.arange(KV_LEN), self.sk, self.c)
-        O.set_rows(self.vc, W.to_f32(v), np.arange(KV_LEN), self.sv, self.c)
-        self.q = W.to_f32(W.decode_query(sh))[: 4 * hs].astype(np.float64)
-        self.newk = W.to_f32(k[-1:])
-        self.newv = W.to_f32(v[-1:])
+
+class OracleSample:
+    """The CPU oracle on the decode_32k workload, one single-threaded process per
+    KV head (8 processes, started with spawn): one step = SET_ROWS of the new
+    token's K/V rows, then decode over all 32768 cells, for all 8 KV heads and 32
+    query heads."""
+
+    def __init__(self):
+        import multiprocessing as mp
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = "1"        # one core per worker process
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        for h in range(N_KV):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(h, b), daemon=True)
+            p.start()
+            self.conns.append(a)
+            self.procs.append(p)
+        for a in self.conns:
+            assert a.recv() == "ready"
 
     def step(self):
-        O, np = self.O, self.np
-        cell = np.array([KV_LEN - 1])
-        O.set_rows(self.kc, self.newk, cell, self.sk, self.c)
-        O.set_rows(self.vc, self.newv, cell, self.sv, self.c)
-        O.decode(self.kc, self.vc, self.sk, self.sv, self.c, self.c, self.q, KV_LEN, 1 / math.sqrt(D))
+        for a in self.conns:
+            a.send("step")
+        for a in self.conns:
+            assert a.recv() == "done"
 
     def timed(self, steps, budget_s):
         done, t0 = 0, time.perf_counter()
@@ -201,33 +224,39 @@ class OracleSample:
             el = time.perf_counter() - t0
             if done >= steps or el >= budget_s:
                 break
-        return done / el * self.hs / N_KV, el, done
+        return done / el, el, done
+
+    def cores(self):
+        return N_KV
 
     def describe(self, done):
-        return (f"{done} oracle steps (SET_ROWS of the new token + decode over 32768 cells) on "
-                f"{self.hs} of 8 KV heads, throughput scaled x{N_KV // self.hs}")
+        return (f"{done} oracle steps of the whole workload (SET_ROWS of the new token's K/V rows + decode over "
+                f"32768 cells, 8 KV x 32 query heads), one single-threaded process per KV head")
 
-
-def host_threads():
-    return int(os.environ.get("OMP_NUM_THREADS") or os.cpu_count() or 1)
+    def close(self):
+        for a in self.conns:
+            a.send("stop")
+        for p in self.procs:
+            p.join(timeout=30)
 
 
 def run_reference(args):
     rank, world, _ = dist_setup()
     if rank != 0:
         return
-    sample = OracleSample(1)
+    sample = OracleSample()
     warm = max(0, args.warmup)
     for _ in range(warm):
         sample.step()
     tok_s, el, done = sample.timed(max(1, args.steps), budget_s=90.0)
+    sample.close()
     line = {
         "impl": "reference", "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": args.gpus,
         "steps": done, "warmup": warm, "ms_per_step": 1000 * el / done, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "decode_32k", "kv_heads": N_KV, "q_heads": N_Q, "head_dim": D,
                    "kv_len": KV_LEN, "type": "turbo3"},
-        "cpu_baseline": {"value": tok_s, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+        "cpu_baseline": {"value": tok_s, "unit": UNIT, "cores": sample.cores(), "kind": "oracle",
                          "sample": sample.describe(done)},
         "e2e": {"value": tok_s, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -396,6 +425,38 @@ def run_tq(args):
     h2d = h_q.numel() * 4 + h_k.numel() * 4 + h_v.numel() * 4
     d2h = h_out.numel() * 4
 
+    # the same, without a graph: every token-layer is its own tq_fattn_decode_append
+    # call through the C ABI (host argument checks and launch on each call)
+    from quantized_kv_cache_tq_gb300 import _lib
+    cstream = stream.cuda_stream
+    ws_ptr, ws_n = ws.data_ptr(), ws.numel()
+    call_args = [[(ks[b].c, vs[b].c, d_k[t][b][0].data_ptr(), d_v[t][b][0].data_ptr(), d_q[t][b].data_ptr(),
+                   out[b].data_ptr()) for b in range(B)] for t in range(T)]
+    algo_code = algo
+
+    def e2e_eager_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        for t in range(T):
+            for kc_, vc_, kr_, vr_, q_, o_ in call_args[t]:
+                st = _lib.tq_fattn_decode_append(kc_, vc_, cbk, cbv, kr_, vr_, tq.TQ_F32, cell.data_ptr(), q_, N_Q,
+                                                 KV_LEN, scale, algo_code, o_, ws_ptr, ws_n, cstream)
+                if st:
+                    raise RuntimeError(_lib.status_string(st))
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_eager_step()
+    torch.cuda.synchronize()
+    eager_steps = max(1, args.steps // 4)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(eager_steps):
+        e2e_eager_step()
+    torch.cuda.synchronize()
+    eager_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+    out_checksum = tq.checksum(out)
+
     extras = {}
     if not args.no_extras and rank == 0:
         extras = run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak,
@@ -403,10 +464,11 @@ def run_tq(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = OracleSample(1)
+        sample = OracleSample()
         sample.step()
-        tok_s, el, done = sample.timed(3, budget_s=15.0)
-        cpu = {"value": tok_s, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
+        tok_s, el, done = sample.timed(100, budget_s=20.0)
+        sample.close()
+        cpu = {"value": tok_s, "unit": UNIT, "cores": sample.cores(), "kind": "oracle",
                "sample": sample.describe(done)}
 
     if rank == 0:
@@ -425,7 +487,13 @@ def run_tq(args):
                          "frac": achieved / hbm_peak, "traffic": decode_traffic(), "kernel": "decode",
                          "kernel_us": dec_us, "bytes_per_launch": dec_bytes, "peak_source": peak_src},
             "e2e": {"value": calls * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "how": "step graph of the C-ABI calls replayed, pinned copies of "
+                                                    "the step's inputs and outputs inside the timed region"},
+            "e2e_eager": {"value": eager_steps * T * B * world / eager_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                          "d2h_bytes_per_step": d2h, "steps": eager_steps,
+                          "how": "one tq_fattn_decode_append C-ABI call per token-layer from Python (ctypes), no "
+                                 "graph; pinned copies of the step's inputs and outputs inside the timed region"},
+            "checksum": {"out_last_step": out_checksum, "hash": "FNV-1a 64 of the output bytes"},
             "gpu_launches": calls * (1 if args.algo != "lut" else 3),
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -451,6 +519,37 @@ def time_graph(torch, fn, reps=20, warm=3):
     return a.elapsed_time(b) / reps / 1000.0
 
 
+class L2Flush:
+    """Writes a buffer of twice the L2 size: called before every timed launch of
+    an extra, so that no launch finds its inputs in L2."""
+
+    def __init__(self, torch, dev):
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+        self.note = f"L2 flushed before every timed launch (write of {2 * l2 / 1e6:.0f} MB)"
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_flushed(torch, fn, flush, reps=10, warm=3):
+    """Median device time (s) of fn() over `reps` launches, each after an L2 flush,
+    with CUDA events on the current stream right around fn()."""
+    s = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn()
+    evs = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs) / 1000.0
+
+
 def _device_gaussian(torch, gen, shape, dev, outliers=True):
     """N(0,1) on the device with 4 outlier channels per 128 scaled by 8 (per head)."""
     x = torch.randn(shape, generator=gen, device=dev)
@@ -461,6 +560,98 @@ def _device_gaussian(torch, gen, shape, dev, outliers=True):
             ch = torch.randperm(dim, generator=gen, device=dev)[:n_out]
             x[..., h, ch] *= 8.0
     return x
+
+
+def _copy_cache(tq, src, dev):
+    c = tq.TqCache(src.tq_type, src.n_kv_heads, src.head_dim, src.n_cells, dev)
+    for d, s_ in zip(c.planes(), src.planes()):
+        if d is not None:
+            d.copy_(s_)
+    return c
+
+
+def decode_config(tq, torch, dev, kc, vc, cbk, cbv, q, algo, hbm_peak, name, l2):
+    """Decode kernel time on one workload: a graph of B launches over B copies of
+    the cache pair (B so that the copies exceed 4x L2), replayed 20 times."""
+    from quantized_kv_cache_tq_gb300 import _lib
+    kv_len = kc.n_cells
+    per_block = {2: 34, 3: 50, 4: 66}
+    nbytes = kc.n_kv_heads * kv_len * (kc.n_blocks * per_block[kc.tq_type] + vc.n_blocks * per_block[vc.tq_type])
+    B = max(2, math.ceil(4 * l2 / nbytes))
+    pairs = [(kc, vc)] + [(_copy_cache(tq, kc, dev), _copy_cache(tq, vc, dev)) for _ in range(B - 1)]
+    n_q = q.shape[0]
+    out = torch.empty((B, n_q, vc.head_dim), dtype=torch.float32, device=dev)
+    ws = tq.workspace(_lib.tq_fattn_decode_workspace(kc.c, vc.c, n_q, kv_len), dev)
+    scale = 1.0 / math.sqrt(kc.head_dim)
+
+    def once():
+        for b, (k_, v_) in enumerate(pairs):
+            tq.fattn_decode(k_, v_, cbk, cbv, q, kv_len, scale, algo=algo, out=out[b], ws=ws)
+    once()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        once()
+    t = time_graph(torch, g.replay, reps=20) / B
+    nbytes += 4 * n_q * (kc.head_dim + vc.head_dim)
+    res = {"workload": name, "us": t * 1e6, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak,
+           "tokens/s": 1.0 / t, "bytes_per_launch": nbytes,
+           "l2": f"{B} cache copies x {nbytes / 1e6:.1f} MB cycled (> 4x L2)", "checksum": tq.checksum(out[0])}
+    del pairs
+    return res
+
+
+def run_decode_configs(tq, torch, dev, k_src, v_src, cells_all, hbm_peak, flush):
+    """Decode on every workload of the sweep: tiny_decode; decode_32k at turbo3,
+    turbo2 and turbo4 on the same inputs with the tensor-core kernel and with the
+    shared-memory Q x centroid LUT kernel; asym_8k (K 192 / V 128)."""
+    import workloads as W
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+    sh = W.decode_32k()
+    sk, sv = W.codebook_signs(sh)
+    q = torch.from_numpy(W.to_f32(W.normal(sh.seed, W.S_EXTRA, N_Q * D)).reshape(N_Q, D)).to(dev)
+    for t in (3, 2, 4):
+        cbk, cbv = tq.codebook(t, sk), tq.codebook(t, sv)
+        kc, vc = tq.TqCache(t, N_KV, D, KV_LEN, dev), tq.TqCache(t, N_KV, D, KV_LEN, dev)
+        tq.set_rows(kc, cbk, k_src, cells_all)
+        tq.set_rows(vc, cbv, v_src, cells_all)
+        for algo, code in (("mma", tq.TQ_DECODE_MMA), ("lut", tq.TQ_DECODE_LUT)):
+            res[f"decode_32k_turbo{t}_{algo}"] = decode_config(
+                tq, torch, dev, kc, vc, cbk, cbv, q, code, hbm_peak,
+                f"decode_32k turbo{t}, 8 KV x 32 Q heads, D=128, 32768 cells, {algo} kernel", l2)
+        del kc, vc
+    # asym_8k: K head dim 192 (two blocks), V 128, 16 = 16 heads, 8192 cells
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20263)
+    sha = W.asym_8k()
+    ska, sva = W.codebook_signs(sha)
+    cbk, cbv = tq.codebook(3, ska), tq.codebook(3, sva)
+    L = sha.kv_len
+    kc, vc = tq.TqCache(3, 16, 192, L, dev), tq.TqCache(3, 16, 128, L, dev)
+    cells = torch.arange(L, dtype=torch.int64, device=dev)
+    tq.set_rows(kc, cbk, _device_gaussian(torch, gen, (L, 16, 192), dev), cells)
+    tq.set_rows(vc, cbv, _device_gaussian(torch, gen, (L, 16, 128), dev), cells)
+    qa = _device_gaussian(torch, gen, (1, 16, 192), dev)[0].contiguous()
+    res["decode_asym_8k"] = decode_config(tq, torch, dev, kc, vc, cbk, cbv, qa, tq.TQ_DECODE_AUTO, hbm_peak,
+                                          "asym_8k decode: Dk=192 / Dv=128, 16 = 16 heads, 8192 cells, turbo3", l2)
+    # tiny_decode: 1 KV head, 512 cells (25.6 KB of cache: launch-bound), L2 flushed
+    sht = W.tiny_decode()
+    skt, svt = W.codebook_signs(sht)
+    cbk, cbv = tq.codebook(3, skt), tq.codebook(3, svt)
+    kr, vr = W.kv_inputs(sht)
+    kc, vc = tq.TqCache(3, 1, 128, 512, dev), tq.TqCache(3, 1, 128, 512, dev)
+    cells = torch.arange(512, dtype=torch.int64, device=dev)
+    tq.set_rows(kc, cbk, torch.from_numpy(W.to_f32(kr)).to(dev), cells)
+    tq.set_rows(vc, cbv, torch.from_numpy(W.to_f32(vr)).to(dev), cells)
+    qt = torch.from_numpy(W.to_f32(W.decode_query(sht))).to(dev)
+    out = torch.empty((1, 128), device=dev)
+    ws = tq.workspace(tq._lib.tq_fattn_decode_workspace(kc.c, vc.c, 1, 512), dev)
+    t = time_flushed(torch, lambda: tq.fattn_decode(kc, vc, cbk, cbv, qt, 512, out=out, ws=ws), flush, reps=50)
+    res["decode_tiny"] = {"workload": "tiny_decode: 1 KV / 1 Q head, D=128, 512 cells, turbo3", "us": t * 1e6,
+                          "tokens/s": 1.0 / t, "l2": flush.note, "checksum": tq.checksum(out),
+                          "note": "launch-bound (25.6 KB of cache)"}
+    return res
 
 
 def run_sparse_v_extra(tq, torch, dev, n_sets=6, thr=5e-3):
@@ -503,8 +694,15 @@ def run_sparse_v_extra(tq, torch, dev, n_sets=6, thr=5e-3):
     return res
 
 
-def run_prefill_extra(tq, torch, dev, tflops_peak, nqs=(4096, 512)):
-    """Prefill over the 4K-context turbo3 cache (8 KV x 16 query heads, D = 256, causal)."""
+def _prefill_flop(nq, kv_len, n_q, dk, dv, causal=True):
+    pairs = sum(min(kv_len, kv_len - nq + i + 1) for i in range(nq)) if causal else nq * kv_len
+    return 2.0 * (dk + dv) * pairs * n_q
+
+
+def run_prefill_extra(tq, torch, dev, tflops_peak, flush, nqs=(3, 64, 512, 2048, 4096)):
+    """Prefill over the 4K-context turbo3 cache (8 KV x 16 query heads, D = 256,
+    causal) at every query count of the sweep, and the asym_8k prefill (K 192 /
+    V 128, 16 = 16 heads, 8192 cells, 512 queries)."""
     import workloads as W
     gen = torch.Generator(device=dev)
     gen.manual_seed(20262)
@@ -516,81 +714,109 @@ def run_prefill_extra(tq, torch, dev, tflops_peak, nqs=(4096, 512)):
     cells = torch.arange(L, dtype=torch.int64, device=dev)
     tq.set_rows(kc, cbk, _device_gaussian(torch, gen, (L, HK, DD), dev), cells)
     tq.set_rows(vc, cbv, _device_gaussian(torch, gen, (L, HK, DD), dev), cells)
-    res = {}
+    res = {"workload": "prefill_4k: 8 KV x 16 Q heads, D=256, 4096 cells, turbo3, causal, bf16 Q",
+           "flops": "2 (Dk + Dv) per visible (query, key) pair per query head; hi/lo fp16 operand splits not counted",
+           "l2": flush.note}
     for nq in nqs:
         q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.bfloat16)
         out = torch.empty((nq, HQ, DD), device=dev)
         ws = tq.workspace(tq._lib.tq_fattn_prefill_workspace(kc.c, vc.c, nq, HQ, L), dev)
-        t = time_graph(torch, lambda: tq.fattn_prefill(kc, vc, cbk, cbv, q, L, out=out, ws=ws), reps=5)
-        pairs = sum(min(L, L - nq + i + 1) for i in range(nq))
-        flop = 4.0 * DD * pairs * HQ
+        t = time_flushed(torch, lambda: tq.fattn_prefill(kc, vc, cbk, cbv, q, L, out=out, ws=ws), flush, reps=7)
+        flop = _prefill_flop(nq, L, HQ, DD, DD)
         res[f"nq{nq}"] = {"ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
-                          "algorithmic_GFLOP": flop / 1e9}
-    return {"workload": "prefill_4k: 8 KV x 16 Q heads, D=256, 4096 cells, turbo3, causal, bf16 Q",
-            "flops": "4*D per visible (query, key) pair per query head; hi/lo fp16 operand splits not counted",
-            **res}
+                          "algorithmic_GFLOP": flop / 1e9, "tokens/s": nq / t, "checksum": tq.checksum(out)}
+    # asym_8k prefill, nq = 512
+    sha = W.asym_8k(512)
+    ska, sva = W.codebook_signs(sha)
+    cbk, cbv = tq.codebook(3, ska), tq.codebook(3, sva)
+    La = sha.kv_len
+    kc, vc = tq.TqCache(3, 16, 192, La, dev), tq.TqCache(3, 16, 128, La, dev)
+    cells = torch.arange(La, dtype=torch.int64, device=dev)
+    tq.set_rows(kc, cbk, _device_gaussian(torch, gen, (La, 16, 192), dev), cells)
+    tq.set_rows(vc, cbv, _device_gaussian(torch, gen, (La, 16, 128), dev), cells)
+    q = torch.randn((512, 16, 192), generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.empty((512, 16, 128), device=dev)
+    ws = tq.workspace(tq._lib.tq_fattn_prefill_workspace(kc.c, vc.c, 512, 16, La), dev)
+    t = time_flushed(torch, lambda: tq.fattn_prefill(kc, vc, cbk, cbv, q, La, out=out, ws=ws), flush, reps=7)
+    flop = _prefill_flop(512, La, 16, 192, 128)
+    res["asym_8k_nq512"] = {"workload": "asym_8k prefill: Dk=192 / Dv=128, 16 = 16 heads, 8192 cells, 512 queries",
+                            "ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
+                            "algorithmic_GFLOP": flop / 1e9, "checksum": tq.checksum(out)}
+    return res
 
 
-def run_int8_extra(tq, torch, dev, tflops_peak, ctx=140000, nq=2048):
-    """int8 prompt attention: 8 KV x 32 Q heads, D = 128, 2048 queries over `ctx` scattered cells."""
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(20264)
-    HK, HQ, DD = 8, 32, 128
-    res = {}
+def _int8_cache(torch, gen, ctx, dev, HK=8, DD=128):
     raw = _device_gaussian(torch, gen, (ctx, HK, DD), dev)
-    amax = raw.abs().amax(-1)
-    sk = (amax / 127).to(torch.float16)
+    sk = (raw.abs().amax(-1) / 127).to(torch.float16)
     k = torch.clamp(torch.round(raw / sk.float().unsqueeze(-1)), -127, 127).to(torch.int8)
     raw = _device_gaussian(torch, gen, (ctx, HK, DD), dev)
     sv = (raw.abs().amax(-1) / 127).to(torch.float16)
     v = torch.clamp(torch.round(raw / sv.float().unsqueeze(-1)), -127, 127).to(torch.int8)
-    del raw
-    perm = torch.randperm(ctx, generator=gen, device=dev).to(torch.int32)
-    q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.float16)
-    out = torch.empty((nq, HQ, DD), device=dev)
-    ws = tq.workspace(tq._lib.tq_int8_prompt_attn_workspace(nq, HQ, HK, DD, ctx), dev)
-    t = time_graph(torch, lambda: tq.int8_prompt_attn(k, sk, v, sv, perm, ctx, q, out=out, ws=ws), reps=3)
-    pairs = sum(min(ctx, ctx - nq + i + 1) for i in range(nq))
-    flop = 4.0 * DD * pairs * HQ
-    return {"workload": f"int8_prompt: 8 KV x 32 Q heads, D=128, {nq} queries, ctx {ctx} scattered cells, fp16 Q",
-            "ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
-            "algorithmic_GFLOP": flop / 1e9}
+    return k, sk, v, sv
 
 
-def run_f16_prompt_extra(tq, torch, dev, tflops_peak, ctx=40000, nq=2048):
+def run_int8_extra(tq, torch, dev, tflops_peak, flush, ctxs=(4096, 40000, 140000), nq=2048):
+    """int8 prompt attention: 8 KV x 32 Q heads, D = 128, 2048 queries over each
+    context of the sweep, rows gathered through a random permutation of the cells."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20264)
+    HK, HQ, DD = 8, 32, 128
+    res = {"workload": "int8_prompt: 8 KV x 32 Q heads, D=128, 2048 queries, scattered int8 rows + fp16 scales, "
+                       "fp16 Q, causal", "l2": flush.note}
+    for ctx in ctxs:
+        k, sk, v, sv = _int8_cache(torch, gen, ctx, dev)
+        perm = torch.randperm(ctx, generator=gen, device=dev).to(torch.int32)
+        q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.float16)
+        out = torch.empty((nq, HQ, DD), device=dev)
+        ws = tq.workspace(tq._lib.tq_int8_prompt_attn_workspace(nq, HQ, HK, DD, ctx), dev)
+        t = time_flushed(torch, lambda: tq.int8_prompt_attn(k, sk, v, sv, perm, ctx, q, out=out, ws=ws), flush,
+                         reps=5)
+        flop = _prefill_flop(nq, ctx, HQ, DD, DD)
+        res[f"ctx{ctx}"] = {"ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
+                            "algorithmic_GFLOP": flop / 1e9, "checksum": tq.checksum(out)}
+        del k, v, sk, sv
+    return res
+
+
+def run_f16_prompt_extra(tq, torch, dev, tflops_peak, flush, ctxs=(4096, 40000), nq=2048):
     """Prompt attention over binary16 rows (the int8 path's other cache mode)."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(20265)
     HK, HQ, DD = 8, 32, 128
-    k = _device_gaussian(torch, gen, (ctx, HK, DD), dev).to(torch.float16)
-    v = _device_gaussian(torch, gen, (ctx, HK, DD), dev).to(torch.float16)
-    perm = torch.randperm(ctx, generator=gen, device=dev).to(torch.int32)
-    q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.float16)
-    out = torch.empty((nq, HQ, DD), device=dev)
-    ws = tq.workspace(tq._lib.tq_int8_prompt_attn_workspace(nq, HQ, HK, DD, ctx), dev)
-    t = time_graph(torch, lambda: tq.f16_prompt_attn(k, v, perm, ctx, q, out=out, ws=ws), reps=3)
-    pairs = sum(min(ctx, ctx - nq + i + 1) for i in range(nq))
-    flop = 4.0 * DD * pairs * HQ
-    return {"workload": f"f16_prompt: 8 KV x 32 Q heads, D=128, {nq} queries, ctx {ctx} scattered binary16 rows",
-            "ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
-            "algorithmic_GFLOP": flop / 1e9}
+    res = {"workload": "f16_prompt: 8 KV x 32 Q heads, D=128, 2048 queries, scattered binary16 rows, causal",
+           "l2": flush.note}
+    for ctx in ctxs:
+        k = _device_gaussian(torch, gen, (ctx, HK, DD), dev).to(torch.float16)
+        v = _device_gaussian(torch, gen, (ctx, HK, DD), dev).to(torch.float16)
+        perm = torch.randperm(ctx, generator=gen, device=dev).to(torch.int32)
+        q = torch.randn((nq, HQ, DD), generator=gen, device=dev).to(torch.float16)
+        out = torch.empty((nq, HQ, DD), device=dev)
+        ws = tq.workspace(tq._lib.tq_int8_prompt_attn_workspace(nq, HQ, HK, DD, ctx), dev)
+        t = time_flushed(torch, lambda: tq.f16_prompt_attn(k, v, perm, ctx, q, out=out, ws=ws), flush, reps=5)
+        flop = _prefill_flop(nq, ctx, HQ, DD, DD)
+        res[f"ctx{ctx}"] = {"ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
+                            "algorithmic_GFLOP": flop / 1e9, "checksum": tq.checksum(out)}
+    return res
 
 
 def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak, tflops_peak):
-    """Other rows of the hot path, measured on their own workloads."""
+    """Other rows of the hot path and the other workloads of the sweep, each on its own inputs."""
+    flush = L2Flush(torch, dev)
     ex = {}
     # SET_ROWS over the whole 32K cache (K and V): read fp32 rows, write packed planes
     def bulk():
         tq.set_rows(base_k, cbk, k_src, cells_all)
         tq.set_rows(base_v, cbv, v_src, cells_all)
-    t = time_graph(torch, bulk, reps=10)
+    t = time_flushed(torch, bulk, flush, reps=10)
     nbytes = 2 * (k_src.numel() * 4 + N_KV * KV_LEN * 50) + 2 * KV_LEN * 8
     ex["set_rows_bulk"] = {"workload": "32768 rows x 8 KV heads x 128, K and V, f32 -> turbo3",
-                           "ms": t * 1e3, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak}
+                           "ms": t * 1e3, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak,
+                           "l2": flush.note, "checksum": tq.checksum(base_k.qs)}
+    ex["decode_configs"] = run_decode_configs(tq, torch, dev, k_src, v_src, cells_all, hbm_peak, flush)
     ex["sparse_v"] = run_sparse_v_extra(tq, torch, dev)
-    ex["prefill"] = run_prefill_extra(tq, torch, dev, tflops_peak)
-    ex["int8_prompt"] = run_int8_extra(tq, torch, dev, tflops_peak)
-    ex["f16_prompt"] = run_f16_prompt_extra(tq, torch, dev, tflops_peak)
+    ex["prefill"] = run_prefill_extra(tq, torch, dev, tflops_peak, flush)
+    ex["int8_prompt"] = run_int8_extra(tq, torch, dev, tflops_peak, flush)
+    ex["f16_prompt"] = run_f16_prompt_extra(tq, torch, dev, tflops_peak, flush)
     return ex
 
 

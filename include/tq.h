@@ -220,13 +220,25 @@ tq_status tq_fattn_decode_sparse_v(const tq_cache *k, const tq_cache *v, const t
  * (tq_fattn_decode_workspace) exceeds 4 MiB return TQ_ERR_WORKSPACE and launch
  * nothing.  The first call on a device looks up the array's address with that
  * device current; make it before any stream capture.  Each call clears the
- * counters and status word on `stream` before the kernel.  All calls share the
- * array, so calls that overlap on the GPU (different streams) race and give
- * wrong results.  Other arguments, results and errors as tq_fattn_decode. */
+ * split counters on `stream` just before the kernel, after its argument checks
+ * (a rejected call writes nothing).  Device-side errors (a bounded wait that
+ * timed out) collect in a status word at the start of the array, which
+ * tq_noalloc_status reads.  All calls share the array, so calls that overlap
+ * on the GPU (different streams) race and give wrong results.  Other
+ * arguments, results and errors as tq_fattn_decode. */
 tq_status tq_fattn_decode_noalloc(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
                                   const tq_codebook *cbv, const float *q, int n_q_heads,
                                   int64_t kv_len, float scale, int algo, float *out,
                                   tq_stream stream);
+
+/* Reads and clears the status word of the array tq_fattn_decode_noalloc uses
+ * on the current device, like tq_workspace_status: waits for `stream`, so it
+ * must not be called while the stream is being captured.  *status_out
+ * receives TQ_OK or the first device-side error of the calls since the last
+ * read (TQ_ERR_TIMEOUT).  Like the entry point it serves, an addition of this
+ * library with no counterpart on the pages.  Errors: TQ_ERR_INVALID_ARG,
+ * TQ_ERR_CUDA. */
+tq_status tq_noalloc_status(int32_t *status_out, tq_stream stream);
 
 /* Bytes of workspace tq_fattn_prefill needs (0 if the shape is invalid);
  * same alignment and zero-fill rule as the decode workspace. */
@@ -281,6 +293,13 @@ tq_status tq_f16_prompt_attn(const uint16_t *k, const uint16_t *v, int64_t n_cel
                              const int32_t *cell_of_pos, int64_t ctx, const uint16_t *q, int nq,
                              int n_q_heads, int n_kv_heads, int head_dim, float scale, int causal,
                              float *out, void *workspace, size_t workspace_bytes, tq_stream stream);
+
+/* Host only.  64-bit FNV-1a hash of n_bytes host bytes (offset basis
+ * 0xcbf29ce484222325, prime 0x100000001b3), so that two builds' outputs can be
+ * compared bit for bit from one printed number ([QSA#1821] "Measured": each
+ * mode prints a checksum of its output).  Errors: TQ_ERR_INVALID_ARG for a
+ * NULL pointer with n_bytes > 0 or a NULL out. */
+tq_status tq_checksum_fnv1a64(const void *host_bytes, size_t n_bytes, uint64_t *out);
 
 /* Reads (and clears) the device status word kept in a workspace of the
  * calls above: waits for `stream`, so it must not be called while the stream

@@ -160,3 +160,10 @@ def f16_prompt_attn(k, v, cell_of_pos, ctx: int, q, scale: float | None = None, 
                                  _stream(stream))
     _lib.check("tq_f16_prompt_attn", st)
     return out
+
+
+def checksum(t) -> str:
+    """FNV-1a 64 of a tensor's bytes (copied to the host), as 16 hex digits."""
+    import numpy as np
+    a = np.ascontiguousarray(t.detach().cpu().numpy())
+    return f"{_lib.tq_checksum_fnv1a64(a.ctypes.data, a.nbytes):016x}"

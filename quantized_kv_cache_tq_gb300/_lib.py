@@ -85,6 +85,12 @@ _SIGS = {
     "tq_f16_prompt_attn": (C.c_int, [_P, _P, C.c_int64, _P, C.c_int64, _P, C.c_int, C.c_int, C.c_int, C.c_int,
                                      C.c_float, C.c_int, _P, _P, C.c_size_t, _P]),
     "tq_workspace_status": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_int32), _P]),
+    "tq_noalloc_status": (C.c_int, [C.POINTER(C.c_int32), _P]),
+    "tq_checksum_fnv1a64": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_uint64)]),
+    # test hook (include/tq_testing.h)
+    "tq_testing_decode_drop_split": (C.c_int, [C.POINTER(tq_cache), C.POINTER(tq_cache), C.POINTER(tq_codebook),
+                                               C.POINTER(tq_codebook), _P, C.c_int, C.c_int64, C.c_float, C.c_int,
+                                               _P, _P, C.c_size_t, C.c_int, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -201,3 +207,22 @@ def tq_workspace_status(ws: int, ws_bytes: int, stream: int | None) -> int:
     st = C.c_int32()
     check("tq_workspace_status", lib.tq_workspace_status(ws, ws_bytes, C.byref(st), stream))
     return st.value
+
+
+def tq_noalloc_status(stream: int | None) -> int:
+    st = C.c_int32()
+    check("tq_noalloc_status", lib.tq_noalloc_status(C.byref(st), stream))
+    return st.value
+
+
+def tq_testing_decode_drop_split(k: tq_cache, v: tq_cache, cbk: tq_codebook, cbv: tq_codebook, q: int,
+                                 n_q_heads: int, kv_len: int, scale: float, algo: int, out: int, ws: int,
+                                 ws_bytes: int, drop_split: int, stream: int | None) -> int:
+    return lib.tq_testing_decode_drop_split(C.byref(k), C.byref(v), C.byref(cbk), C.byref(cbv), q, n_q_heads,
+                                            kv_len, scale, algo, out, ws, ws_bytes, drop_split, stream)
+
+
+def tq_checksum_fnv1a64(host_ptr: int, n_bytes: int) -> int:
+    h = C.c_uint64()
+    check("tq_checksum_fnv1a64", lib.tq_checksum_fnv1a64(host_ptr, n_bytes, C.byref(h)))
+    return h.value

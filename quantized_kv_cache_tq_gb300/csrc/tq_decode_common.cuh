@@ -71,12 +71,16 @@ __device__ __forceinline__ int split_arrive(const DecodeArgs &a, int hk) {
 }
 
 // Partial of query head h = hk * group + g, split s: (m, l) and o'[d].
+// (a.test_drop_split names a split whose partial is skipped: a test's way to make
+// the merging CTAs' bounded waits run out; 0 in every product call)
 __device__ __forceinline__ void store_partial_ml(const DecodeArgs &a, int h, int s, float m, float l, uint32_t tag) {
+  if (s + 1 == a.test_drop_split) return;
   uint64_t *p = a.part_ml + (static_cast<size_t>(h) * a.n_splits + s) * 2;
   st_tagged(p, m, tag);
   st_tagged(p + 1, l, tag);
 }
 __device__ __forceinline__ void store_partial_o(const DecodeArgs &a, int h, int s, int d, float o, uint32_t tag) {
+  if (s + 1 == a.test_drop_split) return;
   st_tagged(a.part + (static_cast<size_t>(h) * a.n_splits + s) * a.part_stride + d, o, tag);
 }
 

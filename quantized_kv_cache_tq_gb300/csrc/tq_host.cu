@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "tq_internal.h"
+#include "../../include/tq_testing.h"
 
 namespace tq {
 
@@ -353,10 +354,14 @@ size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_h
 
 // Decode, optionally with the new token's rows appended first (k_row != null):
 // fused into the tensor-core kernel, else as two SET_ROWS launches before it.
+// clear_counters: zero the workspace's split counters on the stream right before
+// the decode kernel, after every argument check (the allocation-free entry point,
+// whose shared array may hold counters of an interrupted call).
 static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk, const tq_codebook *cbv,
                              const void *k_row, const void *v_row, int src_type, const int64_t *cell_id,
                              const float *q, int n_q_heads, int64_t kv_len, float scale, float v_thresh,
-                             int algo, float *out, void *workspace, size_t workspace_bytes, tq_stream stream) {
+                             int algo, float *out, void *workspace, size_t workspace_bytes, tq_stream stream,
+                             bool clear_counters = false, int drop_split = -1) {
   tq_status st = check_decode_pair(k, v, n_q_heads, kv_len);
   if (st != TQ_OK) return st;
   if (!codebook_ok(cbk, k->type) || !codebook_ok(cbv, v->type)) return TQ_ERR_INVALID_ARG;
@@ -427,6 +432,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.scale_log2 = scale * 1.4426950408889634f;
   a.v_thresh = v_thresh;
   a.coop = static_cast<int64_t>(L.n_splits) * k->n_kv_heads <= sm_count();
+  a.test_drop_split = drop_split + 1;
   a.v_log2_thresh = v_thresh > 0.f ? log2f(v_thresh) : -INFINITY;
   a.cbk = to_dev(cbk);
   a.cbv = to_dev(cbv);
@@ -440,10 +446,27 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
     const int es = (src_type == TQ_F32) ? 4 : 2;
     a.row_async = (k->head_dim * es) % 16 == 0 && (v->head_dim * es) % 16 == 0;
   }
+  if (clear_counters &&
+      cudaMemsetAsync(static_cast<char *>(workspace) + L.counters_off, 0, L.ml_off - L.counters_off, s) != cudaSuccess)
+    return TQ_ERR_CUDA;
   cudaError_t e = (use == TQ_DECODE_MMA) ? launch_decode_mma(k->type, v->type, a, s)
                                          : launch_decode_lut(k->type, v->type, a, s);
   return map_cuda(e);
 }
+
+}  // extern "C"
+
+namespace tq {
+tq_status decode_counters_cleared(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                                  const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
+                                  float scale, int algo, float *out, void *workspace, size_t workspace_bytes,
+                                  tq_stream stream) {
+  return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, q, n_q_heads, kv_len, scale, 0.f, algo, out,
+                     workspace, workspace_bytes, stream, true);
+}
+}  // namespace tq
+
+extern "C" {
 
 tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
                           const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
@@ -451,6 +474,15 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
                           size_t workspace_bytes, tq_stream stream) {
   return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, q, n_q_heads, kv_len, scale, 0.f, algo, out,
                      workspace, workspace_bytes, stream);
+}
+
+tq_status tq_testing_decode_drop_split(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                                       const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
+                                       float scale, int algo, float *out, void *workspace, size_t workspace_bytes,
+                                       int drop_split, tq_stream stream) {
+  if (drop_split < 0) return TQ_ERR_INVALID_ARG;
+  return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, q, n_q_heads, kv_len, scale, 0.f, algo, out,
+                     workspace, workspace_bytes, stream, false, drop_split);
 }
 
 tq_status tq_fattn_decode_sparse_v(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
@@ -529,6 +561,18 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   code_byte_tables(cbk, k->type, a.tabk);
   code_byte_tables(cbv, v->type, a.tabv);
   return map_cuda(launch_prefill(k->type, a, s));
+}
+
+tq_status tq_checksum_fnv1a64(const void *host_bytes, size_t n_bytes, uint64_t *out) {
+  if (!out || (!host_bytes && n_bytes > 0)) return TQ_ERR_INVALID_ARG;
+  const unsigned char *p = static_cast<const unsigned char *>(host_bytes);
+  uint64_t h = 0xcbf29ce484222325ull;
+  for (size_t i = 0; i < n_bytes; ++i) {
+    h ^= p[i];
+    h *= 0x100000001b3ull;
+  }
+  *out = h;
+  return TQ_OK;
 }
 
 tq_status tq_workspace_status(void *workspace, size_t workspace_bytes, int32_t *status_out,

@@ -71,6 +71,8 @@ struct DecodeArgs {
   int32_t src_type;
   int32_t row_async;      // every head's source rows start 16-byte aligned: staged by cp.async
   int32_t coop;           // the grid fits on the GPU at once: cooperative launch, merge by every CTA
+  int32_t test_drop_split;  // 1 + a split whose partial is never stored (0: none); set only by
+                            // tq_testing_decode_drop_split, to make the merge's bounded waits run out
 };
 
 struct PrefillArgs {
@@ -135,5 +137,11 @@ struct PrefillWorkspaceLayout {
 };
 PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t kv_len, int nbk, int nbv);
 cudaError_t launch_prefill(int ktype, const PrefillArgs &a, cudaStream_t s);
+// tq_fattn_decode that also zeroes the workspace's split counters on the stream
+// just before the kernel, once every argument has been checked.
+tq_status decode_counters_cleared(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                                  const tq_codebook *cbv, const float *q, int n_q_heads, int64_t kv_len,
+                                  float scale, int algo, float *out, void *workspace, size_t workspace_bytes,
+                                  tq_stream stream);
 
 }  // namespace tq

@@ -15,9 +15,11 @@
 //   - The first call on each device looks up the array's device address (with
 //     that device current).  Make that first call before any stream capture.
 //   - All calls share the array and it keeps the last call's contents.  Each call
-//     clears the counters and the status word itself (cudaMemsetAsync on the
-//     caller's stream).  Calls that overlap on the GPU, on different streams,
-//     race on the array and produce wrong results.
+//     clears the split counters itself (cudaMemsetAsync on the caller's stream,
+//     after its argument checks).  The status word at the start of the array
+//     collects the first device-side error (e.g. a bounded wait that timed out)
+//     until tq_noalloc_status reads and clears it.  Calls that overlap on the
+//     GPU, on different streams, race on the array and produce wrong results.
 #include <atomic>
 
 #include "tq_internal.h"
@@ -64,15 +66,20 @@ extern "C" tq_status tq_fattn_decode_noalloc(const tq_cache *k, const tq_cache *
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
-  // the status word and the counters start at zero (the array keeps the last
-  // call's contents); the epochs carry on from call to call
-  const DecodeWorkspaceLayout L = decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, algo);
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, L.epochs_off, s) != cudaSuccess ||
-      cudaMemsetAsync(static_cast<char *>(ws) + L.counters_off, 0, L.ml_off - L.counters_off, s) != cudaSuccess) {
+  // the counters start at zero: they are cleared on the stream once every argument
+  // has passed its check, just before the kernel; the epochs carry on from call to
+  // call and the status word keeps the first device-side error until
+  // tq_noalloc_status reads it
+  return decode_counters_cleared(k, v, cbk, cbv, q, n_q_heads, kv_len, scale, algo, out, ws,
+                                 kNoAllocScratchBytes, stream);
+}
+
+extern "C" tq_status tq_noalloc_status(int32_t *status_out, tq_stream stream) {
+  if (!status_out) return TQ_ERR_INVALID_ARG;
+  void *ws = nullptr;
+  if (scratch_address(&ws) != cudaSuccess) {
     cudaGetLastError();
     return TQ_ERR_CUDA;
   }
-  return tq_fattn_decode(k, v, cbk, cbv, q, n_q_heads, kv_len, scale, algo, out, ws, kNoAllocScratchBytes,
-                         stream);
+  return tq_workspace_status(ws, kNoAllocScratchBytes, status_out, stream);
 }

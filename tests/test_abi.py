@@ -22,7 +22,7 @@ def _lib():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "tq.h")).read()
+    src = "".join(open(os.path.join(ROOT, "include", h)).read() for h in ("tq.h", "tq_testing.h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(tq_[a-z0-9_]+)\s*\(", src)))
 
@@ -138,3 +138,13 @@ def test_sparse_v_and_head_limit_checks_reject_before_launch():
     assert L.tq_fattn_decode(big, big, cb, cb, 1 << 23, 257, 64, 0.1, 0, 1 << 24, 1 << 25, 1 << 30,
                              None) == L.TQ_ERR_INVALID_ARG
     assert L.tq_fattn_decode_workspace(_fake_cache(L, h=256), _fake_cache(L, h=256), 256, 64) > 0
+
+
+def test_fnv1a64_known_values():
+    # published FNV-1a 64 test vectors: "" and "a"
+    L = _lib()
+    assert L.tq_checksum_fnv1a64(None, 0) == 0xcbf29ce484222325
+    buf = C.create_string_buffer(b"a", 1)
+    assert L.tq_checksum_fnv1a64(C.addressof(buf), 1) == 0xaf63dc4c8601ec8c
+    buf = C.create_string_buffer(b"foobar", 6)
+    assert L.tq_checksum_fnv1a64(C.addressof(buf), 6) == 0x85944171f73967e8

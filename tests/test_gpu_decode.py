@@ -1,5 +1,7 @@
 """Split-KV single-query decode on the GPU vs the f64 oracle, on the same
 oracle-quantised cache (max-abs <= 2e-3, NMSE <= 1e-6)."""
+import functools
+
 import numpy as np
 import pytest
 
@@ -149,3 +151,41 @@ def test_more_than_256_kv_heads_rejected():
     from quantized_kv_cache_tq_gb300 import _lib
     c = tq.TqCache(3, 257, 128, 64)
     assert _lib.tq_fattn_decode_workspace(c.c, c.c, 257, 64) == 0
+
+
+@functools.lru_cache(maxsize=2)
+def _full_32k(tq_type):
+    # the 32K decode workload's inputs quantised by the oracle and its result,
+    # shared by the two kernels' tests of one code type
+    sh = W.decode_32k()
+    kc, vc, sk, sv = _setup(sh, tq_type, tq_type)
+    q = W.decode_query(sh)
+    ref = O.decode(kc, vc, sk, sv, O.centroids(tq_type), O.centroids(tq_type), W.to_f32(q).astype(np.float64),
+                   sh.kv_len, scale_of(sh.head_dim_k))
+    return kc, vc, sk, sv, q, ref
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("tq_type", [2, 4])
+def test_full_decode_32k_turbo2_turbo4(tq_type, algo):
+    # the same 32K workload (8 KV x 32 query heads, D = 128) at turbo2 and turbo4
+    import torch
+    import quantized_kv_cache_tq_gb300 as tq
+    kc, vc, sk, sv, q, ref = _full_32k(tq_type)
+    gk, gv = upload(kc), upload(vc)
+    out = tq.fattn_decode(gk, gv, tq.codebook(tq_type, sk), tq.codebook(tq_type, sv),
+                          torch.from_numpy(W.to_f32(q)).cuda(), kc.n_cells, scale_of(128), algo=_algo(algo))
+    torch.cuda.synchronize()
+    err, nm = compare_outputs(out.cpu().numpy(), ref)
+    print(f"decode 32K turbo{tq_type} {algo}: max-abs {err:.2e} nmse {nm:.2e}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_full_asym_8k_decode(algo):
+    # K head dim 192 (two blocks, the second zero-padded), V 128, 16 = 16 heads, 8192 cells
+    sh = W.asym_8k()
+    kc, vc, sk, sv = _setup(sh, 3, 3)
+    q = W.decode_query(sh)
+    out, ref = _decode_pair(kc, vc, sk, sv, q, sh.kv_len, algo)
+    err, nm = compare_outputs(out, ref)
+    print(f"decode asym 8K {algo}: max-abs {err:.2e} nmse {nm:.2e}")
