@@ -142,10 +142,12 @@ tq_status tq_set_rows(const tq_cache *dst, const tq_codebook *cb, const void *sr
  * the next one (the split counters reset themselves and a per-KV-head launch
  * epoch advances), so it can be reused across calls, shapes and graph replays
  * but not by two calls that run concurrently.  The split partials are stored
- * with the epoch as a tag, and the merging CTA takes a value only when its tag
- * is this launch's: a prefill or prompt-attention call may share the workspace
- * between decode calls (their data never carries a decode tag, short of a
- * 32-bit pattern coincidence), and keeps the epoch words intact. */
+ * with a tag made of the KV head's epoch and the head's index, and the merging
+ * CTA takes a value only when its tag is this launch's: decode calls of
+ * different shapes (head counts, lengths, types) may share one workspace, and
+ * a prefill or prompt-attention call may share it between decode calls (their
+ * data never carries a decode tag, short of a 32-bit pattern coincidence) and
+ * keeps the epoch words intact. */
 size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_heads,
                                  int64_t kv_len);
 

@@ -28,16 +28,22 @@ __host__ __device__ inline int merge_smem_floats(int group, int nbv, int n_split
 
 // ---- split partials.  Each 32-bit value of a partial (m, l, o') is stored with
 // a 32-bit tag in one 64-bit word, which a single access reads or writes whole.
-// The tag is the KV head's launch epoch + 1 (never 0, so a zero-filled workspace
-// holds no valid word): the merging CTA loads every partial of its head in one
-// round trip and knows from the tags alone which ones are this launch's, so a
-// CTA that stored its partial needs no fence and no second counter, and the
-// arrival counter can be bumped before the partial is even computed.  A stale
-// word of this head carries an older epoch; the epoch of head hk changes only
-// after all CTAs of head hk have arrived, i.e. after all of them have read it.
-__device__ __forceinline__ uint32_t split_tag(uint32_t epoch) {
-  const uint32_t t = epoch + 1u;
-  return t ? t : 1u;
+// The tag holds the KV head's launch epoch + 1 (24 bits, never 0, so a
+// zero-filled workspace holds no valid word) above the KV head index (8 bits):
+// the merging CTA loads every partial of its head in one round trip and knows
+// from the tags alone which ones are this launch's, so a CTA that stored its
+// partial needs no fence and no second counter, and the arrival counter can be
+// bumped before the partial is even computed.  A stale word of this head
+// carries an older epoch (the epoch of head hk changes only after all CTAs of
+// head hk have read it); a word that another head wrote carries another head
+// index, whatever the two heads' epochs -- so calls of different shapes (head
+// counts, lengths) may share one workspace.  An older word of this head is
+// mistaken for a current one only after 2^24 launches of the head that never
+// rewrote its slot.
+__device__ __forceinline__ uint32_t split_tag(uint32_t epoch, int hk) {
+  uint32_t t = (epoch + 1u) & 0xFFFFFFu;
+  if (t == 0u) t = 1u;
+  return (t << 8) | static_cast<uint32_t>(hk & 0xFF);
 }
 
 __device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t tag) {
@@ -99,7 +105,7 @@ __device__ __forceinline__ void store_partial_o(const DecodeArgs &a, int h, int 
 // `smem` must hold merge_smem_floats(group, nbv, n_splits) floats.
 template <int NT>
 __device__ void decode_merge(const DecodeArgs &a, int hk, uint32_t epoch, float *smem) {
-  const uint32_t tag = split_tag(epoch);
+  const uint32_t tag = split_tag(epoch, hk);
   const int G = a.group, ns = a.n_splits, dvp = QK * a.nbv;
   const int stride = a.part_stride;
   float *orot = smem;                     // [G][dvp]
@@ -248,7 +254,7 @@ __device__ __forceinline__ void coop_merge(const DecodeArgs &a, int hk, int spli
   const int t = threadIdx.x;
   bool arrived = true;
   for (int u = split; u < a.group * a.nbv; u += a.n_splits)
-    arrived = merge_block(a, hk, u / a.nbv, u % a.nbv, split_tag(epoch), t, 1, buf) && arrived;
+    arrived = merge_block(a, hk, u / a.nbv, u % a.nbv, split_tag(epoch, hk), t, 1, buf) && arrived;
   if (!arrived && (t & 31) == 0) set_status(a.status, TQ_ERR_TIMEOUT);
   if (split == 0 && t == 0) a.epochs[hk] = epoch + 1u;
 }

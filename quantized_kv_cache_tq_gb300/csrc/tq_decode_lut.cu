@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads) decode_lut_kernel(const DecodeArgs a
   }
   int prev = 0;
   if (!a.coop && tid == 0) prev = split_arrive(a, hk);
-  const uint32_t epoch = s_epoch, tag = split_tag(epoch);
+  const uint32_t epoch = s_epoch, tag = split_tag(epoch, hk);
   if (kr == 0) {
     for (int g = 0; g < G; ++g) {
       store_partial_o(a, hk * G + g, split, d, acc[g], tag);

@@ -688,7 +688,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   const bool in_cluster = tc::cluster_size() == static_cast<uint32_t>(a.n_splits);
   int prev = 0;
   if (!in_cluster && !a.coop && tid == 0) prev = split_arrive(a, hk);
-  const uint32_t epoch = s_epoch, tag = split_tag(epoch);
+  const uint32_t epoch = s_epoch, tag = split_tag(epoch, hk);
   float *cpart = reinterpret_cast<float *>(smem + WS::PT);      // m[G], l[G], o'[G][DVP]
   for (int i = tid; i < G * DVP; i += NT) {
     const int h = i / DVP, d = i % DVP;

@@ -110,7 +110,7 @@ PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t
   PrefillWorkspaceLayout L;
   const int64_t qt = (static_cast<int64_t>(nq) * group + 127) / 128;
   const int64_t ctas = qt * n_kv_heads;
-  const int bn = (nbk == 2) ? 32 : 64;
+  const int bn = (nbk == 2) ? 64 : 128;        // the prefill kernel's key tile
   const int64_t tiles = (kv_len + bn - 1) / bn;
   int64_t sp = ctas > 0 ? (sm_count() + ctas - 1) / ctas : 1;
   if (sp > 16) sp = 16;
@@ -529,6 +529,7 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   if (kv_len == 0)
     return map_cuda(cudaMemsetAsync(out, 0, sizeof(float) * nq * n_q_heads * v->head_dim, s));
   if (static_cast<int64_t>(nq) * group > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(nq) * group + 127) / 128 > 65535) return TQ_ERR_UNSUPPORTED;   // query tiles: grid y
   PrefillArgs a;
   memset(&a, 0, sizeof(a));
   a.kn = static_cast<const uint16_t *>(k->norms);

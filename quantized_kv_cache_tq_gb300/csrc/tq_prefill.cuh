@@ -5,25 +5,31 @@
 //
 // One CTA = one KV head x 128 query rows (128/G queries x the G query heads of
 // the GQA group, row r = query (r / G), head (r % G)) x one range of key tiles
-// (BN = 64 keys, 32 for 256-dim heads).  Warp roles, connected by mbarriers
-// only (no CTA barrier inside the key loop):
-//   control warp (one thread): cp.async.bulk of the packed K/V planes into a
-//     3-stage ring; issues S_j = Q'K'_j^T into tensor memory, then
-//     O += P'_{j-1} V'_{j-1} -- the tensor cores compute S_j while the softmax
-//     warps work on tile j-1;
-//   4 dequant warps: expand tile j into binary16 K'/V' tiles (exact centroid
-//     values; double buffered; one key-block row per thread);
-//   4 softmax warps (one query row per thread, TMEM lanes 0..127): read S_j,
-//     form s = sum_b |k_b| S_b, apply the causal mask and the online softmax
-//     (log2 domain; the reference maximum is raised only when the row maximum
-//     grows by more than 2^8, then O is rescaled in tensor memory), and write
-//     P'_b = p |v_b| as binary16 hi + lo straight into tensor memory over S_j,
-//     where the PV mma reads it as its A operand.
+// (BN = 64 keys for 256-dim K rows, 128 for 128-dim rows).  Warp roles,
+// connected by mbarriers only (no CTA barrier inside the key loop):
+//   control warp (one thread): issues S_j = Q'K'_j^T into tensor memory as soon
+//     as K'_j is expanded, then O += P'_{j-1} V'_{j-1} once the softmax warps
+//     have written P'_{j-1} -- the tensor cores compute S_{j+1} while the
+//     softmax warps work on tile j;
+//   4 dequant warps: expand the packed K/V tiles (staged by cp.async.bulk in
+//     two small rings, K with both tiles' norms, V) into binary16 K'/V' operand
+//     tiles (exact centroid values), one key-block row per thread.  K' and V'
+//     are single-buffered: K'_{j+1} is written as soon as S_j is done, before
+//     V'_j (which waits for PV_{j-1}), so the next S never waits for a V tile;
+//   8 softmax warps, two per TMEM lane quarter (one query row, half the tile's
+//     keys per thread): read S_j, form s = sum_b |k_b| S_b, apply the causal
+//     mask and the online softmax (log2 domain; the row maximum is exchanged
+//     between the two halves through shared memory; the reference maximum is
+//     raised only when it grows by more than 2^8, then O is rescaled in tensor
+//     memory), and write P'_b = p |v_b| as binary16 hi + lo straight into tensor
+//     memory over S_j, where the PV mma reads it as its A operand.
 // Precision: Q' and P' are split into binary16 hi + lo parts and both go
 // through the tensor cores; K'/V' are exact; accumulation is fp32.
-// Few query tiles (short prompts, verify batches) split the key range over
-// several CTAs; the last CTA to finish a query tile merges the partial
-// (max, sum, O) rows (4 + 128 nbv floats each) with log-sum-exp weights.
+// Query tiles are scheduled longest first (the causal tiles near the end of the
+// prompt attend the most keys).  Few query tiles (short prompts, verify
+// batches) split the key range over several CTAs; the last CTA to finish a
+// query tile merges the partial (max, sum, O) rows (4 + 128 nbv floats each)
+// with log-sum-exp weights.
 // Epilogue: o = S H (O / l) / sqrt(128) per 128-dim block (V codebook), fp32.
 //
 // Shared-memory operands (SWIZZLE_NONE core matrices of 8 rows x 16 B):
@@ -31,7 +37,7 @@
 //   K'_b           B, K-major   [key/8][d/8]   LBO 128 (along d)     SBO 2048
 //   V'_b           B, MN-major  [key/8][d/8]   LBO 2048 (along keys) SBO 128
 // Tensor memory (fp32 columns): O_b at 128 b; per buffer S_b at BN b, aliased by
-// P'_(b, part) at (2b + part) BN/2 (fp16 pairs, row = lane).
+// P'_(b, part) at (2b + part) BN/2 (fp16 pairs of keys, row = lane).
 #pragma once
 
 #include "tq_common.cuh"
@@ -41,32 +47,40 @@ namespace tq {
 namespace pf {
 
 constexpr int BM = 128;          // query rows per CTA (TMEM lanes)
-constexpr int NWARP = 9;         // 0-3 softmax, 4-7 dequant, 8 control
+constexpr int NSM = 8;           // softmax warps 0..7 (warps w and w + 4 share TMEM lane quarter w)
+constexpr int DQ0 = 8;           // dequant warps 8..11
+constexpr int CTRL = 12;         // control warp
+constexpr int NWARP = 13;
 constexpr int NT = NWARP * 32;
-constexpr int STAGES = 3;
 constexpr float kLazyRescale = 8.f;   // log2 units
 
 template <int T, int NBK, int NBV>
 struct Cfg {
-  static constexpr int BN = (NBK == 2) ? 32 : 64;
+  static constexpr int BN = (NBK == 2) ? 64 : 128;         // keys per tile
+  static constexpr int HB = BN / 2;                        // keys per softmax thread
   static constexpr int QSB = TypeTraits<T>::QSB, SGB = TypeTraits<T>::SGB;
   static constexpr uint32_t QBLK = 32768;                  // 128 rows x 128 dims fp16
   static constexpr uint32_t TBLK = BN * 256;               // BN keys x 128 dims fp16
-  static constexpr uint32_t KVBUF = (NBK + NBV) * TBLK;    // one K'/V' buffer
   static constexpr uint32_t Q = 0;                         // [part][NBK] blocks
-  static constexpr uint32_t KV = Q + 2 * NBK * QBLK;       // 2 buffers: K'_b then V'_b
-  // packed staging ring: K qs, K signs, K norms, V qs, V signs, V norms
-  static constexpr uint32_t S_KQS = 0;
-  static constexpr uint32_t S_KSG = S_KQS + BN * NBK * QSB;
-  static constexpr uint32_t S_KN = S_KSG + BN * NBK * SGB;
-  static constexpr uint32_t S_VQS = S_KN + BN * NBK * 2;
-  static constexpr uint32_t S_VSG = S_VQS + BN * NBV * QSB;
-  static constexpr uint32_t S_VN = S_VSG + BN * NBV * SGB;
-  static constexpr uint32_t STAGE = (S_VN + BN * NBV * 2 + 127) / 128 * 128;
-  static constexpr uint32_t STG = KV + 2 * KVBUF;
-  static constexpr uint32_t NRM = STG + STAGES * STAGE;    // floats [2][BN][NBK + NBV]
-  static constexpr uint32_t TOTAL = NRM + 2 * BN * (NBK + NBV) * 4;
-  static constexpr uint32_t TX = BN * (NBK + NBV) * (QSB + SGB + 2);
+  static constexpr uint32_t KT = Q + 2 * NBK * QBLK;       // K'_b tiles
+  static constexpr uint32_t VT = KT + NBK * TBLK;          // V'_b tiles
+  // K staging: K qs, K signs, K norms, V norms; V staging: V qs, V signs
+  static constexpr uint32_t K_QS = 0;
+  static constexpr uint32_t K_SG = K_QS + BN * NBK * QSB;
+  static constexpr uint32_t K_KN = K_SG + BN * NBK * SGB;
+  static constexpr uint32_t K_VN = K_KN + BN * NBK * 2;
+  static constexpr uint32_t KSTAGE = (K_VN + BN * NBV * 2 + 127) / 128 * 128;
+  static constexpr uint32_t V_QS = 0;
+  static constexpr uint32_t V_SG = V_QS + BN * NBV * QSB;
+  static constexpr uint32_t VSTAGE = (V_SG + BN * NBV * SGB + 127) / 128 * 128;
+  static constexpr int KST = 2;
+  static constexpr int VST = (T == 4 && NBK == 2) ? 1 : 2;
+  static constexpr uint32_t KSTG = VT + NBV * TBLK;
+  static constexpr uint32_t VSTG = KSTG + KST * KSTAGE;
+  static constexpr uint32_t NRM = VSTG + VST * VSTAGE;     // floats [2][BN][4]: |k_0|, |k_1|, |v_0|, |v_1|
+  static constexpr uint32_t TOTAL = NRM + 2 * BN * 4 * 4;
+  static constexpr uint32_t KTX = BN * (NBK * (QSB + SGB + 2) + NBV * 2);   // bytes of a full K stage
+  static constexpr uint32_t VTX = BN * NBV * (QSB + SGB);                   // bytes of a full V stage
   // tensor memory
   static constexpr uint32_t SPW = (NBK > NBV ? NBK : NBV) * BN;   // columns per S/P' buffer
   static constexpr uint32_t SP0 = NBV * 128;
@@ -107,50 +121,106 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 }
 
 struct Bars {
-  uint64_t full[STAGES];   // packed tile staged (tx)
-  uint64_t dq[2];          // K'/V' tile expanded (4 dequant warps)
+  uint64_t kfull[2];       // packed K stage (and both tiles' norms) landed (tx)
+  uint64_t vfull[2];       // packed V stage landed (tx)
+  uint64_t dqk;            // K'_j expanded (4 dequant warps)
+  uint64_t dqv;            // V'_j expanded (4 dequant warps)
+  uint64_t nrmf[2];        // norms of tile j in buffer j & 1 (4 dequant warps)
   uint64_t sf[2];          // S_j computed (mma commit)
-  uint64_t pf[2];          // P'_j written (4 softmax warps)
+  uint64_t pf[2];          // P'_j written (8 softmax warps)
   uint64_t pv[2];          // PV_j computed (mma commit)
 };
 
-// o = S H o' / sqrt(128) of one 128-dim block held by one thread, stored as fp32
-__device__ __forceinline__ void rotate_store_block(float o[128], float scale, const DevCodebook &cbv, float *dst,
-                                                   int dmax, bool store) {
+// Output rows of one warp: 32 rows x one 128-dim V block in shared memory (row
+// r at stg + r * stride floats, already divided by l and by sqrt(128); with SWZ
+// the 16-byte chunk c of row r sits at chunk c ^ (r & 7), so that 32 threads
+// writing one row each do not collide on a bank).  Each row is rotated back by
+// the whole warp (o = S H o', 4 dims per lane, the page's butterflies with
+// shuffles) and stored as 512 contiguous bytes.
+template <bool SWZ>
+__device__ __forceinline__ void rotate_store_rows(const float *stg, int stride, const PrefillArgs &a, int row0, int q0,
+                                                  int hk, int b, int lane) {
+  const int G = a.group;
+  for (int r = 0; r < 32; ++r) {
+    const int rr = row0 + r, qi = q0 + rr / G;
+    if (qi >= a.nq) break;                     // rows are in query order
+    const int chunk = SWZ ? (lane ^ (r & 7)) : lane;
+    const float4 x = *reinterpret_cast<const float4 *>(stg + r * stride + 4 * chunk);
+    float v[4] = {x.x, x.y, x.z, x.w};
+    wht128_warp(v, lane);
+    apply_signs(v, a.cbv, lane);
+    const int d = b * QK + 4 * lane;
+    float *o = a.out + (static_cast<size_t>(qi) * a.n_q_heads + hk * G + rr % G) * a.dv + d;
+    if (d + 4 <= a.dv) *reinterpret_cast<float4 *>(o) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+// One key-block row of a packed tile (qs row, signs row) -> 128 binary16 values
+// in the core-matrix layout of an operand tile (`dst` = the row's first core
+// matrix; the 16 d-octets follow at 128-byte steps).
+template <int T>
+__device__ __forceinline__ void expand_row(const uint8_t *qrow, const uint8_t *srow, const Tab &tb, unsigned char *dst) {
+  if (T == 4) {
 #pragma unroll
-  for (int hb = 1; hb < 128; hb <<= 1)
+    for (int w4 = 0; w4 < 4; ++w4) {
+      const uint4 w = reinterpret_cast<const uint4 *>(qrow)[w4];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int i = 0; i < 128; ++i)
-      if (!(i & hb)) {
-        const float x = o[i], y = o[i | hb];
-        o[i] = x + y;
-        o[i | hb] = x - y;
+      for (int i = 0; i < 4; ++i) {
+        uint4 o;
+        dq4<4>(ws[i], tb, o.x, o.y);
+        dq4<4>(ws[i] >> 16, tb, o.z, o.w);
+        *reinterpret_cast<uint4 *>(dst + (4 * w4 + i) * 128) = o;
       }
+    }
+  } else {
+    uint32_t sgw[4] = {0u, 0u, 0u, 0u};
+    if (T == 3) {
+      const uint4 sg4 = *reinterpret_cast<const uint4 *>(srow);
+      sgw[0] = sg4.x; sgw[1] = sg4.y; sgw[2] = sg4.z; sgw[3] = sg4.w;
+    }
 #pragma unroll
-  for (int i = 0; i < 128; i += 4) {
-    float4 w;
-    w.x = ((cbv.sign_bits[i >> 5] >> ((i + 0) & 31)) & 1u) ? -o[i] * scale : o[i] * scale;
-    w.y = ((cbv.sign_bits[i >> 5] >> ((i + 1) & 31)) & 1u) ? -o[i + 1] * scale : o[i + 1] * scale;
-    w.z = ((cbv.sign_bits[i >> 5] >> ((i + 2) & 31)) & 1u) ? -o[i + 2] * scale : o[i + 2] * scale;
-    w.w = ((cbv.sign_bits[i >> 5] >> ((i + 3) & 31)) & 1u) ? -o[i + 3] * scale : o[i + 3] * scale;
-    if (store && i + 4 <= dmax) *reinterpret_cast<float4 *>(dst + i) = w;
+    for (int hq = 0; hq < 2; ++hq) {
+      const uint4 w = reinterpret_cast<const uint4 *>(qrow)[hq];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int wi = 4 * hq + i;                       // qs word: elements 16 wi ..
+        uint32_t s0, s1;
+        sel_words<T>(ws[i], sgw[wi >> 1], (wi & 1) != 0, s0, s1);
+        uint4 o0, o1;
+        dq4<T>(s0, tb, o0.x, o0.y);
+        dq4<T>(s0 >> 16, tb, o0.z, o0.w);
+        dq4<T>(s1, tb, o1.x, o1.y);
+        dq4<T>(s1 >> 16, tb, o1.z, o1.w);
+        *reinterpret_cast<uint4 *>(dst + (2 * wi) * 128) = o0;
+        *reinterpret_cast<uint4 *>(dst + (2 * wi + 1) * 128) = o1;
+      }
+    }
   }
 }
 
 template <int T, int NBK, int NBV>
 __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
   using C = Cfg<T, NBK, NBV>;
-  constexpr int BN = C::BN, QSB = C::QSB, SGB = C::SGB, DVP = C::DVP;
+  constexpr int BN = C::BN, HB = C::HB, QSB = C::QSB, SGB = C::SGB, DVP = C::DVP;
   extern __shared__ __align__(1024) unsigned char smem[];
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_fail;
   __shared__ int s_last;
+  // exchange between the two softmax warps of a row (value per row, flag per warp),
+  // double-buffered by the parity of the exchange count
+  __shared__ float xv[2][2][BM];
+  __shared__ int xf[2][2][4];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hk = blockIdx.y, split = blockIdx.z, n_split = gridDim.z;
+  // grid: (KV head, query tile, split); the longest query tiles (last in the
+  // prompt) are launched first
+  const int hk = blockIdx.x, split = blockIdx.z, n_split = gridDim.z;
+  const int qt = gridDim.y - 1 - blockIdx.y;
   const int G = a.group;
-  const int q0 = blockIdx.x * (BM / G);
+  const int q0 = qt * (BM / G);
   const int q_last = min(a.nq, q0 + BM / G) - 1;
   const int64_t pos0 = a.kv_len - a.nq;
   const int64_t kv_hi = a.causal ? i64min(a.kv_len, pos0 + q_last + 1) : a.kv_len;
@@ -166,32 +236,50 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
   const uint8_t *vsg = SGB ? a.vsg + static_cast<size_t>(hk) * a.n_cells * NBV * SGB : nullptr;
   const uint16_t *vn = a.vn + static_cast<size_t>(hk) * a.n_cells * NBV;
 
-  auto issue = [&](int j) {       // local tile j -> stage j % STAGES
-    unsigned char *st = smem + C::STG + (j % STAGES) * C::STAGE;
-    uint64_t *bar = &bars.full[j % STAGES];
+  // bulk copies of local tile j (keys past n_cells are not read; n_cells is a
+  // multiple of 64, so every copy stays a multiple of 16 bytes)
+  auto tile_keys = [&](int j) -> int {
     const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
-    tc::mbar_expect_tx(bar, C::TX);
-    tc::bulk_g2s(st + C::S_KQS, kqs + key0 * NBK * QSB, BN * NBK * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + C::S_KSG, ksg + key0 * NBK * SGB, BN * NBK * SGB, bar);
-    tc::bulk_g2s(st + C::S_KN, kn + key0 * NBK, BN * NBK * 2, bar);
-    tc::bulk_g2s(st + C::S_VQS, vqs + key0 * NBV * QSB, BN * NBV * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + C::S_VSG, vsg + key0 * NBV * SGB, BN * NBV * SGB, bar);
-    tc::bulk_g2s(st + C::S_VN, vn + key0 * NBV, BN * NBV * 2, bar);
+    return static_cast<int>(i64min(BN, a.n_cells - key0));
+  };
+  auto issue_k = [&](int j) {
+    unsigned char *st = smem + C::KSTG + (j % C::KST) * C::KSTAGE;
+    uint64_t *bar = &bars.kfull[j % C::KST];
+    const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
+    const int nk = tile_keys(j);
+    tc::mbar_expect_tx(bar, nk * (NBK * (QSB + SGB + 2) + NBV * 2));
+    tc::bulk_g2s(st + C::K_QS, kqs + key0 * NBK * QSB, nk * NBK * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + C::K_SG, ksg + key0 * NBK * SGB, nk * NBK * SGB, bar);
+    tc::bulk_g2s(st + C::K_KN, kn + key0 * NBK, nk * NBK * 2, bar);
+    tc::bulk_g2s(st + C::K_VN, vn + key0 * NBV, nk * NBV * 2, bar);
+  };
+  auto issue_v = [&](int j) {
+    unsigned char *st = smem + C::VSTG + (j % C::VST) * C::VSTAGE;
+    uint64_t *bar = &bars.vfull[j % C::VST];
+    const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
+    const int nk = tile_keys(j);
+    tc::mbar_expect_tx(bar, nk * NBV * (QSB + SGB));
+    tc::bulk_g2s(st + C::V_QS, vqs + key0 * NBV * QSB, nk * NBV * QSB, bar);
+    if (SGB) tc::bulk_g2s(st + C::V_SG, vsg + key0 * NBV * SGB, nk * NBV * SGB, bar);
   };
 
   if (warp == 0) tc::tmem_alloc<C::TMEM_COLS>(&tmem_slot);
-  if (tid == NT - 32) {
+  if (tid == CTRL * 32) {
     s_fail = 0;
-    for (int s = 0; s < STAGES; ++s) tc::mbar_init(&bars.full[s], 1);
-    for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(&bars.dq[b], 4);
-      tc::mbar_init(&bars.sf[b], 1);
-      tc::mbar_init(&bars.pf[b], 4);
-      tc::mbar_init(&bars.pv[b], 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&bars.kfull[s], 1);
+      tc::mbar_init(&bars.vfull[s], 1);
+      tc::mbar_init(&bars.nrmf[s], 4);
+      tc::mbar_init(&bars.sf[s], 1);
+      tc::mbar_init(&bars.pf[s], NSM);
+      tc::mbar_init(&bars.pv[s], 1);
     }
+    tc::mbar_init(&bars.dqk, 4);
+    tc::mbar_init(&bars.dqv, 4);
     tc::mbar_init_fence();
     tc::fence_async_smem();
-    for (int i = 0; i < STAGES && i < n_tiles; ++i) issue(i);
+    for (int i = 0; i < C::KST && i < n_tiles; ++i) issue_k(i);
+    for (int i = 0; i < C::VST && i < n_tiles; ++i) issue_v(i);
   }
 
   // ---- Q' = q rotated per block (scale * log2(e) / sqrt(128) folded in), binary16 hi + lo
@@ -242,15 +330,16 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
   const uint32_t sbase = tc::smem_u32(smem);
   float *nrm = reinterpret_cast<float *>(smem + C::NRM);
 
-  // softmax state (warps 0..3: row = tid)
-  const int row = tid & (BM - 1);
+  // softmax state (warps 0..7: row = 32 (warp % 4) + lane, keys half * HB .. of each tile)
+  const int row = 32 * (warp & 3) + lane;
+  const int half = (warp >> 2) & 1;
   const int row_q = q0 + row / G;
-  const bool row_ok = warp < 4 && row_q < a.nq;
+  const bool row_ok = warp < NSM && row_q < a.nq;
   const int64_t row_end = a.causal ? (pos0 + row_q + 1) : a.kv_len;
   float m_used = -INFINITY, l_sum = 0.f;
 
-  if (warp == 8) {
-    // ===================== control: copies and mma issue =====================
+  if (warp == CTRL) {
+    // ===================== control: mma issue =====================
     if (lane == 0) {
       constexpr uint32_t ID_S = tc::idesc_f16(BM, BN, false, false);
       constexpr uint32_t ID_PV = tc::idesc_f16(BM, 128, false, true);
@@ -258,18 +347,17 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
       // operand crosses 256 KB, so an operand at base + off has the descriptor
       // desc(base) + (off >> 4) -- one add per mma instead of a rebuild.
       const uint64_t q_desc = tc::sdesc(sbase + C::Q, 2048, 128);
-      const uint64_t k_desc = tc::sdesc(sbase + C::KV, 128, 2048);
-      const uint64_t v_desc = tc::sdesc(sbase + C::KV + NBK * C::TBLK, 2048, 128);
+      const uint64_t k_desc = tc::sdesc(sbase + C::KT, 128, 2048);
+      const uint64_t v_desc = tc::sdesc(sbase + C::VT, 2048, 128);
       auto issue_pv = [&](int j) {
         const uint32_t pbuf = tmem + C::SP0 + (j & 1) * C::SPW;
-        const uint64_t vb = v_desc + (((j & 1) * C::KVBUF) >> 4);
 #pragma unroll
         for (int b = 0; b < NBV; ++b)
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int ks = 0; ks < BN / 16; ++ks) {
-              const uint64_t bd = vb + ((b * C::TBLK + ks * 4096) >> 4);
+              const uint64_t bd = v_desc + ((b * C::TBLK + ks * 4096) >> 4);
               mma_f16_ta(tmem + b * 128, pbuf + (2 * b + part) * (BN / 2) + ks * 8, bd, ID_PV,
                          j > 0 || part > 0 || ks > 0);
             }
@@ -277,12 +365,10 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
       };
       bool ok = true;
       for (int j = 0; j < n_tiles && ok; ++j) {
-        ok = tc::mbar_wait(&bars.dq[j & 1], (j >> 1) & 1);
-        if (ok && j >= 2) ok = tc::mbar_wait(&bars.pv[j & 1], ((j - 2) >> 1) & 1);
+        ok = tc::mbar_wait(&bars.dqk, j & 1);                       // K'_j expanded
         if (!ok) break;
         tc::fence_after_sync();
         const uint32_t sbuf = tmem + C::SP0 + (j & 1) * C::SPW;
-        const uint64_t kb = k_desc + (((j & 1) * C::KVBUF) >> 4);
 #pragma unroll
         for (int b = 0; b < NBK; ++b)
 #pragma unroll
@@ -290,12 +376,12 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint64_t ad = q_desc + (((part * NBK + b) * C::QBLK + ks * 4096) >> 4);
-              const uint64_t bd = kb + ((b * C::TBLK + ks * 256) >> 4);
+              const uint64_t bd = k_desc + ((b * C::TBLK + ks * 256) >> 4);
               tc::mma_f16(sbuf + b * BN, ad, bd, ID_S, part > 0 || ks > 0);
             }
         tc::mma_commit(&bars.sf[j & 1]);
         if (j >= 1) {
-          ok = tc::mbar_wait(&bars.pf[(j - 1) & 1], ((j - 1) >> 1) & 1);
+          ok = tc::mbar_wait(&bars.pf[(j - 1) & 1], ((j - 1) >> 1) & 1) && tc::mbar_wait(&bars.dqv, (j - 1) & 1);
           if (!ok) break;
           tc::fence_after_sync();
           issue_pv(j - 1);
@@ -303,7 +389,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
       }
       if (ok && n_tiles > 0) {
         const int j = n_tiles - 1;
-        ok = tc::mbar_wait(&bars.pf[j & 1], (j >> 1) & 1);
+        ok = tc::mbar_wait(&bars.pf[j & 1], (j >> 1) & 1) && tc::mbar_wait(&bars.dqv, j & 1);
         if (ok) {
           tc::fence_after_sync();
           issue_pv(j);
@@ -311,120 +397,143 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
       }
       if (!ok) s_fail = 1;
     }
-  } else if (warp >= 4) {
+  } else if (warp >= DQ0) {
     // ===================== dequant: one key-block row per thread =====================
-    const int dt = tid - 128;                                  // 0..127
+    // program order K'_0, then K'_{j+1} before V'_j: S_{j+1} never waits for a V tile
+    const int dt = tid - DQ0 * 32;                             // 0..127
     const Tab tab_k{a.tabk[0], a.tabk[1], a.tabk[2], a.tabk[3]};
     const Tab tab_v{a.tabv[0], a.tabv[1], a.tabv[2], a.tabv[3]};
-    for (int j = 0; j < n_tiles; ++j) {
-      bool ok = tc::mbar_wait(&bars.full[j % STAGES], (j / STAGES) & 1);
-      if (ok && j >= 2) ok = tc::mbar_wait(&bars.pv[j & 1], ((j - 2) >> 1) & 1);
-      if (!__all_sync(0xffffffffu, ok)) { s_fail = 1; break; }
+    unsigned char *kt = smem + C::KT;
+    unsigned char *vt = smem + C::VT;
+    auto k_phase = [&](int j) -> bool {
+      bool ok = tc::mbar_wait(&bars.kfull[j % C::KST], (j / C::KST) & 1);
+      if (ok && j >= 1) ok = tc::mbar_wait(&bars.sf[(j - 1) & 1], ((j - 1) >> 1) & 1);    // K' tile free
+      if (ok && j >= 2) ok = tc::mbar_wait(&bars.pf[(j - 2) & 1], ((j - 2) >> 1) & 1);    // norm buffer free
+      if (!__all_sync(0xffffffffu, ok)) return false;
       tc::fence_after_sync();
-      const unsigned char *st = smem + C::STG + (j % STAGES) * C::STAGE;
-      unsigned char *buf = smem + C::KV + (j & 1) * C::KVBUF;
-      for (int r = dt; r < (NBK + NBV) * BN; r += 128) {
-        const bool is_v = r >= NBK * BN;
-        const int rr = is_v ? r - NBK * BN : r;
-        const int b = rr / BN, key = rr % BN;
-        const int nb = is_v ? NBV : NBK;
-        const Tab &tb = is_v ? tab_v : tab_k;
-        const uint8_t *qrow = st + (is_v ? C::S_VQS : C::S_KQS) + (key * nb + b) * QSB;
-        unsigned char *dst = buf + (is_v ? NBK + b : b) * C::TBLK + (key >> 3) * 2048 + (key & 7) * 16;
-        if (T == 4) {
-#pragma unroll
-          for (int w4 = 0; w4 < 4; ++w4) {
-            const uint4 w = reinterpret_cast<const uint4 *>(qrow)[w4];
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 o;
-              dq4<4>(ws[i], tb, o.x, o.y);
-              dq4<4>(ws[i] >> 16, tb, o.z, o.w);
-              *reinterpret_cast<uint4 *>(dst + (4 * w4 + i) * 128) = o;
-            }
-          }
-        } else {
-          uint32_t sgw[4] = {0u, 0u, 0u, 0u};
-          if (T == 3) {
-            const uint4 sg4 =
-                *reinterpret_cast<const uint4 *>(st + (is_v ? C::S_VSG : C::S_KSG) + (key * nb + b) * SGB);
-            sgw[0] = sg4.x; sgw[1] = sg4.y; sgw[2] = sg4.z; sgw[3] = sg4.w;
-          }
-#pragma unroll
-          for (int hq = 0; hq < 2; ++hq) {
-            const uint4 w = reinterpret_cast<const uint4 *>(qrow)[hq];
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int wi = 4 * hq + i;                       // qs word: elements 16 wi ..
-              uint32_t s0, s1;
-              sel_words<T>(ws[i], sgw[wi >> 1], (wi & 1) != 0, s0, s1);
-              uint4 o0, o1;
-              dq4<T>(s0, tb, o0.x, o0.y);
-              dq4<T>(s0 >> 16, tb, o0.z, o0.w);
-              dq4<T>(s1, tb, o1.x, o1.y);
-              dq4<T>(s1 >> 16, tb, o1.z, o1.w);
-              *reinterpret_cast<uint4 *>(dst + (2 * wi) * 128) = o0;
-              *reinterpret_cast<uint4 *>(dst + (2 * wi + 1) * 128) = o1;
-            }
-          }
-        }
-        const uint16_t *np = reinterpret_cast<const uint16_t *>(st + (is_v ? C::S_VN : C::S_KN));
-        nrm[(j & 1) * BN * (NBK + NBV) + key * (NBK + NBV) + (is_v ? NBK + b : b)] =
-            __half2float(__ushort_as_half(np[key * nb + b]));
+      const unsigned char *st = smem + C::KSTG + (j % C::KST) * C::KSTAGE;
+      for (int r = dt; r < NBK * BN; r += 128) {
+        const int b = r / BN, key = r % BN;
+        expand_row<T>(st + C::K_QS + (key * NBK + b) * QSB, st + C::K_SG + (key * NBK + b) * SGB, tab_k,
+                      kt + b * C::TBLK + (key >> 3) * 2048 + (key & 7) * 16);
+      }
+      if (dt < BN) {
+        const uint16_t *knp = reinterpret_cast<const uint16_t *>(st + C::K_KN) + dt * NBK;
+        const uint16_t *vnp = reinterpret_cast<const uint16_t *>(st + C::K_VN) + dt * NBV;
+        float4 w;
+        w.x = __half2float(__ushort_as_half(knp[0]));
+        w.y = NBK > 1 ? __half2float(__ushort_as_half(knp[NBK > 1 ? 1 : 0])) : 0.f;
+        w.z = __half2float(__ushort_as_half(vnp[0]));
+        w.w = NBV > 1 ? __half2float(__ushort_as_half(vnp[NBV > 1 ? 1 : 0])) : 0.f;
+        reinterpret_cast<float4 *>(nrm)[(j & 1) * BN + dt] = w;
       }
       tc::fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.dq[j & 1]);
-      // the stage of tile j is free once all four dequant warps are done with it:
-      // one of them refills it (the control thread only issues mma)
-      if (warp == 4 && lane == 0 && j + STAGES < n_tiles) {
-        if (tc::mbar_wait(&bars.dq[j & 1], (j >> 1) & 1)) issue(j + STAGES);
+      if (lane == 0) {
+        mbar_arrive(&bars.nrmf[j & 1]);
+        mbar_arrive(&bars.dqk);
+      }
+      // the K stage of tile j is free once all four dequant warps are done with it
+      if (warp == DQ0 && lane == 0 && j + C::KST < n_tiles) {
+        if (tc::mbar_wait(&bars.dqk, j & 1)) issue_k(j + C::KST);
         else s_fail = 1;
       }
+      return true;
+    };
+    auto v_phase = [&](int j) -> bool {
+      bool ok = tc::mbar_wait(&bars.vfull[j % C::VST], (j / C::VST) & 1);
+      if (ok && j >= 1) ok = tc::mbar_wait(&bars.pv[(j - 1) & 1], ((j - 1) >> 1) & 1);    // V' tile free
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      tc::fence_after_sync();
+      const unsigned char *st = smem + C::VSTG + (j % C::VST) * C::VSTAGE;
+      for (int r = dt; r < NBV * BN; r += 128) {
+        const int b = r / BN, key = r % BN;
+        expand_row<T>(st + C::V_QS + (key * NBV + b) * QSB, st + C::V_SG + (key * NBV + b) * SGB, tab_v,
+                      vt + b * C::TBLK + (key >> 3) * 2048 + (key & 7) * 16);
+      }
+      tc::fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.dqv);
+      if (warp == DQ0 && lane == 0 && j + C::VST < n_tiles) {
+        if (tc::mbar_wait(&bars.dqv, j & 1)) issue_v(j + C::VST);
+        else s_fail = 1;
+      }
+      return true;
+    };
+    bool ok = n_tiles == 0 || k_phase(0);
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      if (j + 1 < n_tiles) ok = k_phase(j + 1);
+      if (ok) ok = v_phase(j);
     }
+    if (!ok) s_fail = 1;
   } else {
-    // ===================== softmax: one query row per thread =====================
-    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    // ===================== softmax: one query row, half the keys per thread =====================
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int bar_id = 1 + (warp & 3);                     // named barrier of the warp pair
+    int xc = 0;
+    // swap a value (per row) and a warp-uniform flag with the partner warp; both
+    // warps of a pair make the same sequence of calls, so a failed wait ends both
+    // loops at the same point and no named barrier is left waiting
+    auto exchange = [&](float v, bool f, float &pv, bool &pflag) {
+      const int p = xc & 1;
+      ++xc;
+      xv[p][half][row] = v;
+      if (lane == 0) xf[p][half][warp & 3] = f ? 1 : 0;
+      tc::named_sync(bar_id, 64);
+      pv = xv[p][half ^ 1][row];
+      pflag = xf[p][half ^ 1][warp & 3] != 0;
+    };
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      ok = tc::mbar_wait(&bars.sf[j & 1], (j >> 1) & 1);
-      if (ok) ok = tc::mbar_wait(&bars.dq[j & 1], (j >> 1) & 1);     // norms of tile j are written
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      bool okw = tc::mbar_wait(&bars.sf[j & 1], (j >> 1) & 1);
+      if (okw) okw = tc::mbar_wait(&bars.nrmf[j & 1], (j >> 1) & 1);
+      okw = __all_sync(0xffffffffu, okw);
       tc::fence_after_sync();
       const uint32_t sbuf = tmem + lane_off + C::SP0 + (j & 1) * C::SPW;
-      const float *nr = nrm + (j & 1) * BN * (NBK + NBV);
-      float s[BN];
-#pragma unroll
-      for (int i = 0; i < BN; ++i) s[i] = 0.f;
-      {
-        uint32_t r0[NBK * BN];                                 // all S columns, one wait
-#pragma unroll
-        for (int c0 = 0; c0 < NBK * BN; c0 += 32) tc::tmem_ld32(sbuf + c0, r0 + c0);
-        tc::tmem_wait_ld();
+      const float4 *nr = reinterpret_cast<const float4 *>(nrm) + (j & 1) * BN + half * HB;
+      const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN + half * HB;
+      const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(HB, i64min(row_end, kv_hi) - key0))) : 0;
+      float s[HB];
+      float mt = -INFINITY;
+      if (okw) {
+        uint32_t r0[NBK * HB];                               // this thread's S columns, one wait
 #pragma unroll
         for (int b = 0; b < NBK; ++b)
 #pragma unroll
-          for (int i = 0; i < BN; ++i) s[i] = fmaf(nr[i * (NBK + NBV) + b], __uint_as_float(r0[b * BN + i]), s[i]);
-      }
-      const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
-      const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(BN, row_end - key0))) : 0;
-      float mt = -INFINITY;
+          for (int c0 = 0; c0 < HB; c0 += 32) tc::tmem_ld32(sbuf + b * BN + half * HB + c0, r0 + b * HB + c0);
+        tc::tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < BN; ++i)
-        if (i < nvis) mt = fmaxf(mt, s[i]);
+        for (int i = 0; i < HB; ++i) {
+          const float4 n4 = nr[i];
+          float x = n4.x * __uint_as_float(r0[i]);
+          if (NBK > 1) x = fmaf(n4.y, __uint_as_float(r0[(NBK > 1 ? HB : 0) + i]), x);
+          s[i] = x;
+        }
+#pragma unroll
+        for (int i = 0; i < HB; ++i)
+          if (i < nvis) mt = fmaxf(mt, s[i]);
+      }
+      // row maximum over both halves of the tile
+      float pmt;
+      bool pok;
+      exchange(mt, okw, pmt, pok);
+      if (!(okw && pok)) { ok = false; break; }
+      mt = fmaxf(mt, pmt);
       const bool raise = mt > m_used + kLazyRescale || (m_used == -INFINITY && mt > -INFINITY);
       const float fct = (raise && m_used != -INFINITY) ? exp2f(m_used - mt) : 1.f;
       if (raise) m_used = mt;
-      if (__any_sync(0xffffffffu, fct != 1.f)) {
-        // O must be stable: wait for the PV mma of the previous tile
+      if (__any_sync(0xffffffffu, fct != 1.f)) {           // the same decision in both warps of the pair
+        // O must be stable: wait for the PV mma of the previous tile; each half
+        // rescales its half of the O columns
         bool okp = (j == 0) || tc::mbar_wait(&bars.pv[(j - 1) & 1], ((j - 1) >> 1) & 1);
-        if (!__all_sync(0xffffffffu, okp)) { ok = false; break; }
+        okp = __all_sync(0xffffffffu, okp);
+        float unused;
+        bool pokp;
+        exchange(0.f, okp, unused, pokp);
+        if (!(okp && pokp)) { ok = false; break; }
         tc::fence_after_sync();
-        l_sum *= fct;
 #pragma unroll
-        for (int c = 0; c < DVP; c += 32) {
+        for (int c = half * (DVP / 2); c < (half + 1) * (DVP / 2); c += 32) {
           uint32_t r[32];
           tc::tmem_ld32(tmem + lane_off + c, r);
           tc::tmem_wait_ld();
@@ -433,32 +542,38 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
           tc::tmem_st32(tmem + lane_off + c, r);
         }
       }
+      l_sum *= fct;
       float psum = 0.f;
 #pragma unroll
-      for (int i = 0; i < BN; ++i) {
+      for (int i = 0; i < HB; ++i) {
         s[i] = (i < nvis) ? tc::ex2(s[i] - m_used) : 0.f;
         psum += s[i];
       }
       l_sum += psum;
-      // P'_(b, hi/lo) into tensor memory over S_j: row = lane, fp16 pairs of keys
+      // P'_(b, hi/lo) into tensor memory over S_j: row = lane, fp16 pairs of keys;
+      // this half's keys are columns half * HB/2 .. of each (b, part) region
 #pragma unroll
-      for (int b = 0; b < NBV; ++b) {
-        uint32_t ph[BN / 2], pl[BN / 2];
+      for (int b = 0; b < NBV; ++b)
 #pragma unroll
-        for (int i = 0; i < BN / 2; ++i) {
-          const int k0 = 2 * i;
-          // masked keys may carry garbage norms: select, never multiply, a zero
-          const float x0 = s[k0] > 0.f ? s[k0] * nr[k0 * (NBK + NBV) + NBK + b] : 0.f;
-          const float x1 = s[k0 + 1] > 0.f ? s[k0 + 1] * nr[(k0 + 1) * (NBK + NBV) + NBK + b] : 0.f;
-          const __half2 h = __floats2half2_rn(x0, x1);
-          const float2 hf = __half22float2(h);
-          const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-          ph[i] = *reinterpret_cast<const uint32_t *>(&h);
-          pl[i] = *reinterpret_cast<const uint32_t *>(&l);
+        for (int c16 = 0; c16 < HB / 2; c16 += 16) {        // 16 columns (32 keys) at a time
+          uint32_t ph[16], pl[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int k0 = 2 * (c16 + i);
+            // masked keys may carry garbage norms: select, never multiply, a zero
+            const float vn0 = b == 0 ? nr[k0].z : nr[k0].w;
+            const float vn1 = b == 0 ? nr[k0 + 1].z : nr[k0 + 1].w;
+            const float x0 = s[k0] > 0.f ? s[k0] * vn0 : 0.f;
+            const float x1 = s[k0 + 1] > 0.f ? s[k0 + 1] * vn1 : 0.f;
+            const __half2 h = __floats2half2_rn(x0, x1);
+            const float2 hf = __half22float2(h);
+            const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+            ph[i] = *reinterpret_cast<const uint32_t *>(&h);
+            pl[i] = *reinterpret_cast<const uint32_t *>(&l);
+          }
+          tmem_st<16>(sbuf + (2 * b) * (BN / 2) + half * (HB / 2) + c16, ph);
+          tmem_st<16>(sbuf + (2 * b + 1) * (BN / 2) + half * (HB / 2) + c16, pl);
         }
-        tmem_st<BN / 2>(sbuf + (2 * b) * (BN / 2), ph);
-        tmem_st<BN / 2>(sbuf + (2 * b + 1) * (BN / 2), pl);
-      }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
@@ -478,42 +593,50 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  // row sums of the two halves
+  if (warp < NSM) xv[0][half][row] = l_sum;
+  __syncthreads();
+  const float l_row = (warp < NSM) ? xv[0][0][row] + xv[0][1][row] : 0.f;
   const bool failed = s_fail != 0;
   if (failed && tid == 0) set_status(a.status, TQ_ERR_TIMEOUT);
-  const int h_row = hk * G + row % G;
-  float *orow = a.out + (static_cast<size_t>(row_ok ? row_q : 0) * a.n_q_heads + h_row) * a.dv;
+  const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
+  float *stg = reinterpret_cast<float *>(smem + C::Q) + (warp & 7) * 32 * 128;   // [32][128] per softmax warp
   if (n_split == 1) {
-    if (warp < 4 && !failed) {
-      const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-      const float inv = (l_sum > 0.f ? 1.f / l_sum : 0.f) * kInvSqrtQK;
-#pragma unroll 1
-      for (int b = 0; b < NBV; ++b) {
-        float o[128];
+    // half b stages V block b of its row (divided by l and sqrt(128)), then its
+    // warp rotates the 32 rows back and stores them
+    if (warp < NSM && half < NBV && !failed) {
+      const float inv = (l_row > 0.f ? 1.f / l_row : 0.f) * kInvSqrtQK;
+      const int b = half;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tc::tmem_ld32(tmem + lane_off + b * 128 + 32 * c, r);
-          tc::tmem_wait_ld();
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + lane_off + b * 128 + 32 * c, r);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = n_tiles > 0 ? __uint_as_float(r[i]) : 0.f;
-        }
-        rotate_store_block(o, inv, a.cbv, orow + b * 128, a.dv - b * 128, row_ok);
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4 *>(stg + lane * 128 + 4 * ((8 * c + i / 4) ^ (lane & 7))) =
+              n_tiles > 0 ? make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
+                                        __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      __syncwarp();
+      rotate_store_rows<true>(stg, 128, a, 32 * (warp & 3), q0, hk, b, lane);
     }
   } else {
     // split key range: store (m, l, O) of every row; the last CTA of this query tile merges
-    const size_t tile_id = static_cast<size_t>(blockIdx.x) * a.n_kv_heads + hk;
+    const size_t tile_id = static_cast<size_t>(qt) * a.n_kv_heads + hk;
     const size_t stride = 4 + DVP;             // m, l, 2 pad floats: O rows stay 16-byte aligned
     float *part = a.part + (tile_id * n_split + split) * BM * stride;
-    if (warp < 4) {
-      const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    if (warp < NSM) {
       float *pr = part + static_cast<size_t>(row) * stride;
       const bool has = !failed && n_tiles > 0;
-      pr[0] = has ? m_used : -INFINITY;
-      pr[1] = has ? l_sum : 0.f;
+      if (half == 0) {
+        pr[0] = has ? m_used : -INFINITY;
+        pr[1] = has ? l_row : 0.f;
+      }
 #pragma unroll 1
-      for (int c = 0; c < DVP; c += 32) {
+      for (int c = half * (DVP / 2); c < (half + 1) * (DVP / 2); c += 32) {
         uint32_t r[32];
         tc::tmem_ld32(tmem + lane_off + c, r);
         tc::tmem_wait_ld();
@@ -532,7 +655,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
     if (s_last) {
       __threadfence();
       const float *base = a.part + tile_id * n_split * BM * stride;
-      float *wts = reinterpret_cast<float *>(smem + C::STG);        // [BM][n_split] weights / L
+      float *wts = reinterpret_cast<float *>(smem + C::KSTG);       // [BM][n_split] weights / L
       float *acc = reinterpret_cast<float *>(smem + C::Q);          // [BM][DVP] merged rows
       if (tid < min(BM, (a.nq - q0) * G)) {
         float M = -INFINITY;
@@ -546,7 +669,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
           wts[tid * n_split + s2] = w;
           L += w * __ldcg(p + 1);
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float inv = (L > 0.f ? 1.f / L : 0.f) * kInvSqrtQK;
         for (int s2 = 0; s2 < n_split; ++s2) wts[tid * n_split + s2] *= inv;
       }
       __syncthreads();
@@ -559,15 +682,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
         acc[i] = o;
       }
       __syncthreads();
-      if (warp < 4) {
-#pragma unroll 1
-        for (int b = 0; b < NBV; ++b) {
-          float o[128];
-#pragma unroll
-          for (int i = 0; i < 128; ++i) o[i] = acc[row * DVP + b * 128 + i];
-          rotate_store_block(o, kInvSqrtQK, a.cbv, orow + b * 128, a.dv - b * 128, row_ok);
-        }
-      }
+      if (warp < NSM && half < NBV)           // merged rows of V block b (weights include 1/sqrt(128))
+        rotate_store_rows<false>(acc + 32 * (warp & 3) * DVP + half * 128, DVP, a, 32 * (warp & 3), q0, hk, half,
+                                 lane);
       if (tid == 0) a.counters[tile_id] = 0;
     }
   }
@@ -579,16 +696,16 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
 template <int T, int NBK, int NBV>
 cudaError_t launch_one(const PrefillArgs &a, cudaStream_t s) {
   using C = Cfg<T, NBK, NBV>;
-  static_assert(C::TOTAL <= 227 * 1024, "shared memory");
+  static_assert(C::TOTAL + 4 * 2 * 2 * BM + 512 <= 227 * 1024, "shared memory (dynamic + static)");
   static_assert(C::COLS_NEEDED <= 512, "tensor memory");
-  static_assert(C::BN % 16 == 0 && C::BN <= 64, "key tile");
-  // the merge reuses the Q region for BM x DVP floats and the staging ring for the weights
+  static_assert(C::BN % 64 == 0 && C::HB % 32 == 0, "key tile");
+  // the merge reuses the Q region for BM x DVP floats and the K staging ring for the weights
   static_assert(2 * NBK * C::QBLK >= BM * C::DVP * 4, "merge buffer");
-  static_assert(STAGES * C::STAGE >= BM * 16 * 4, "merge weights");
+  static_assert(C::KST * C::KSTAGE >= BM * 16 * 4, "merge weights");
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, NBK, NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::TOTAL);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.nq * a.group + BM - 1) / BM, a.n_kv_heads, a.n_split);
+  dim3 grid(a.n_kv_heads, (a.nq * a.group + BM - 1) / BM, a.n_split);
   prefill_kernel<T, NBK, NBV><<<grid, NT, C::TOTAL, s>>>(a);
   return cudaGetLastError();
 }

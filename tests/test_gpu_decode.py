@@ -189,3 +189,28 @@ def test_full_asym_8k_decode(algo):
     out, ref = _decode_pair(kc, vc, sk, sv, q, sh.kv_len, algo)
     err, nm = compare_outputs(out, ref)
     print(f"decode asym 8K {algo}: max-abs {err:.2e} nmse {nm:.2e}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_one_workspace_across_shapes(algo):
+    # one workspace shared by calls of different shapes (8 and 2 KV heads, long and
+    # short contexts): a split partial left by an earlier call is never taken for
+    # a later call's, whatever the heads' launch counts
+    import torch
+    import quantized_kv_cache_tq_gb300 as tq
+    cases = {}
+    for name, sh, n in (("big", W.decode_32k(), 8192), ("two", W.AttnShape("two_kv", 2, 8, 128, 128, 1500, seed=41),
+                                                          1500)):
+        kc, vc, sk, sv = _setup(sh, 3, 3, n_rows=n)
+        cases[name] = (upload(kc), upload(vc), tq.codebook(3, sk), tq.codebook(3, sv),
+                       torch.from_numpy(W.to_f32(W.decode_query(sh))).cuda(), kc, vc, sk, sv)
+    ws = tq.workspace(max(tq._lib.tq_fattn_decode_workspace(c[0].c, c[1].c, c[4].shape[0], 8192)
+                          for c in cases.values()))
+    for name, n in (("big", 8192), ("big", 700), ("big", 8192), ("two", 1500), ("big", 129), ("two", 1500),
+                    ("big", 4096)):
+        gk, gv, cbk, cbv, q, kc, vc, sk, sv = cases[name]
+        out = tq.fattn_decode(gk, gv, cbk, cbv, q, n, scale_of(128), algo=_algo(algo), ws=ws)
+        torch.cuda.synchronize()
+        ref = O.decode(kc, vc, sk, sv, O.centroids(3), O.centroids(3), q.cpu().numpy().astype(np.float64), n,
+                       scale_of(128))
+        compare_outputs(out.cpu().numpy(), ref)
