@@ -41,6 +41,10 @@ def parse():
     p.add_argument("--algo", default="auto", choices=["auto", "lut", "mma"])
     p.add_argument("--tokens-per-step", type=int, default=64)
     p.add_argument("--no-extras", action="store_true")
+    p.add_argument("--extras", default="set_rows,decode,sparse_v,prefill,int8,f16",
+                   help="comma-separated extras to run after the main measurement")
+    p.add_argument("--prefill-nq", default="3,64,512,2048,4096", help="query counts of the prefill extra")
+    p.add_argument("--int8-ctx", default="4096,40000,140000", help="contexts of the int8 extra")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -460,7 +464,7 @@ def run_tq(args):
     extras = {}
     if not args.no_extras and rank == 0:
         extras = run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak,
-                            float(peaks.get("bf16_tflops", 1900.0)))
+                            float(peaks.get("bf16_tflops", 1900.0)), args)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -799,24 +803,33 @@ def run_f16_prompt_extra(tq, torch, dev, tflops_peak, flush, ctxs=(4096, 40000),
     return res
 
 
-def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak, tflops_peak):
+def run_extras(tq, torch, dev, base_k, base_v, k_src, v_src, cells_all, cbk, cbv, hbm_peak, tflops_peak, args):
     """Other rows of the hot path and the other workloads of the sweep, each on its own inputs."""
     flush = L2Flush(torch, dev)
+    want = set(args.extras.split(","))
+    nqs = tuple(int(x) for x in args.prefill_nq.split(",") if x)
+    ctxs = tuple(int(x) for x in args.int8_ctx.split(",") if x)
     ex = {}
     # SET_ROWS over the whole 32K cache (K and V): read fp32 rows, write packed planes
     def bulk():
         tq.set_rows(base_k, cbk, k_src, cells_all)
         tq.set_rows(base_v, cbv, v_src, cells_all)
-    t = time_flushed(torch, bulk, flush, reps=10)
-    nbytes = 2 * (k_src.numel() * 4 + N_KV * KV_LEN * 50) + 2 * KV_LEN * 8
-    ex["set_rows_bulk"] = {"workload": "32768 rows x 8 KV heads x 128, K and V, f32 -> turbo3",
-                           "ms": t * 1e3, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak,
-                           "l2": flush.note, "checksum": tq.checksum(base_k.qs)}
-    ex["decode_configs"] = run_decode_configs(tq, torch, dev, k_src, v_src, cells_all, hbm_peak, flush)
-    ex["sparse_v"] = run_sparse_v_extra(tq, torch, dev)
-    ex["prefill"] = run_prefill_extra(tq, torch, dev, tflops_peak, flush)
-    ex["int8_prompt"] = run_int8_extra(tq, torch, dev, tflops_peak, flush)
-    ex["f16_prompt"] = run_f16_prompt_extra(tq, torch, dev, tflops_peak, flush)
+    if "set_rows" in want:
+        t = time_flushed(torch, bulk, flush, reps=10)
+        nbytes = 2 * (k_src.numel() * 4 + N_KV * KV_LEN * 50) + 2 * KV_LEN * 8
+        ex["set_rows_bulk"] = {"workload": "32768 rows x 8 KV heads x 128, K and V, f32 -> turbo3",
+                               "ms": t * 1e3, "GB/s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / hbm_peak,
+                               "l2": flush.note, "checksum": tq.checksum(base_k.qs)}
+    if "decode" in want:
+        ex["decode_configs"] = run_decode_configs(tq, torch, dev, k_src, v_src, cells_all, hbm_peak, flush)
+    if "sparse_v" in want:
+        ex["sparse_v"] = run_sparse_v_extra(tq, torch, dev)
+    if "prefill" in want:
+        ex["prefill"] = run_prefill_extra(tq, torch, dev, tflops_peak, flush, nqs=nqs)
+    if "int8" in want:
+        ex["int8_prompt"] = run_int8_extra(tq, torch, dev, tflops_peak, flush, ctxs=ctxs)
+    if "f16" in want:
+        ex["f16_prompt"] = run_f16_prompt_extra(tq, torch, dev, tflops_peak, flush)
     return ex
 
 

@@ -117,7 +117,8 @@ PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t
   if (sp > tiles / 2) sp = tiles / 2;
   if (sp < 1) sp = 1;
   L.n_split = static_cast<int>(sp);
-  L.counters_off = kWsHeader + kWsEpochBytes;      // the decode epochs stay untouched
+  L.sched_off = kWsHeader + kWsEpochBytes;         // the decode epochs stay untouched
+  L.counters_off = L.sched_off + 256;
   L.part_off = L.counters_off + round_up(sizeof(int32_t) * qt * n_kv_heads, 256);
   L.total = L.part_off;
   if (L.n_split > 1)
@@ -529,7 +530,7 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   if (kv_len == 0)
     return map_cuda(cudaMemsetAsync(out, 0, sizeof(float) * nq * n_q_heads * v->head_dim, s));
   if (static_cast<int64_t>(nq) * group > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;
-  if ((static_cast<int64_t>(nq) * group + 127) / 128 > 65535) return TQ_ERR_UNSUPPORTED;   // query tiles: grid y
+  if ((static_cast<int64_t>(nq) * group + 127) / 128 * k->n_kv_heads * 16 > 0x7fffffffLL) return TQ_ERR_UNSUPPORTED;
   PrefillArgs a;
   memset(&a, 0, sizeof(a));
   a.kn = static_cast<const uint16_t *>(k->norms);
@@ -556,6 +557,9 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   a.n_split = L.n_split;
   a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.part_off);
   a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.counters_off);
+  a.sched = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.sched_off);
+  a.n_qt = static_cast<int32_t>((static_cast<int64_t>(nq) * group + 127) / 128);
+  a.n_items = a.n_qt * k->n_kv_heads * L.n_split;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.cbk = to_dev(cbk);
   a.cbv = to_dev(cbv);

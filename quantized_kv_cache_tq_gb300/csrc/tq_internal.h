@@ -87,6 +87,7 @@ struct PrefillArgs {
   int32_t *status;
   float *part;            // split partials [q tile][kv head][split][128 rows][4 + 128 nbv]
   int32_t *counters;      // [q tile][kv head], self-resetting
+  int32_t *sched;         // [0] next work item, [1] CTAs done (both reset by the last CTA)
   int64_t n_cells;
   int64_t kv_len;
   int32_t q_type;
@@ -98,6 +99,8 @@ struct PrefillArgs {
   int32_t nbk, nbv;
   int32_t causal;
   int32_t n_split;        // key-range splits per query tile
+  int32_t n_qt;           // query tiles of 128 rows
+  int32_t n_items;        // work items: query tiles x KV heads x splits, longest first
   float scale_log2;
   DevCodebook cbk, cbv;
   uint32_t tabk[4], tabv[4];
@@ -133,7 +136,7 @@ cudaError_t launch_decode_mma_t4(const DecodeArgs &a, cudaStream_t s);
 bool prefill_supported(int ktype, int vtype, int group, int nbk, int nbv);
 struct PrefillWorkspaceLayout {
   int n_split;
-  size_t counters_off, part_off, total;
+  size_t sched_off, counters_off, part_off, total;
 };
 PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t kv_len, int nbk, int nbv);
 cudaError_t launch_prefill(int ktype, const PrefillArgs &a, cudaStream_t s);

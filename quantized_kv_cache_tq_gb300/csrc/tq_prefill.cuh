@@ -77,7 +77,7 @@ struct Cfg {
   static constexpr int VST = (T == 4 && NBK == 2) ? 1 : 2;
   static constexpr uint32_t KSTG = VT + NBV * TBLK;
   static constexpr uint32_t VSTG = KSTG + KST * KSTAGE;
-  static constexpr uint32_t NRM = VSTG + VST * VSTAGE;     // floats [2][BN][4]: |k_0|, |k_1|, |v_0|, |v_1|
+  static constexpr uint32_t NRM = VSTG + VST * VSTAGE;     // floats [2][4][BN]: |k_0|, |k_1|, |v_0|, |v_1| of each key
   static constexpr uint32_t TOTAL = NRM + 2 * BN * 4 * 4;
   static constexpr uint32_t KTX = BN * (NBK * (QSB + SGB + 2) + NBV * 2);   // bytes of a full K stage
   static constexpr uint32_t VTX = BN * NBV * (QSB + SGB);                   // bytes of a full V stage
@@ -140,29 +140,45 @@ struct Bars {
 template <bool SWZ>
 __device__ __forceinline__ void rotate_store_rows(const float *stg, int stride, const PrefillArgs &a, int row0, int q0,
                                                   int hk, int b, int lane) {
-  const int G = a.group;
-  for (int r = 0; r < 32; ++r) {
-    const int rr = row0 + r, qi = q0 + rr / G;
-    if (qi >= a.nq) break;                     // rows are in query order
-    const int chunk = SWZ ? (lane ^ (r & 7)) : lane;
-    const float4 x = *reinterpret_cast<const float4 *>(stg + r * stride + 4 * chunk);
-    float v[4] = {x.x, x.y, x.z, x.w};
-    wht128_warp(v, lane);
-    apply_signs(v, a.cbv, lane);
-    const int d = b * QK + 4 * lane;
-    float *o = a.out + (static_cast<size_t>(qi) * a.n_q_heads + hk * G + rr % G) * a.dv + d;
-    if (d + 4 <= a.dv) *reinterpret_cast<float4 *>(o) = make_float4(v[0], v[1], v[2], v[3]);
+  const int G = a.group, g_shift = __ffs(G) - 1;
+  const int n_rows = max(0, min(32, (a.nq - q0) * G - row0));       // rows of queries < nq
+  const int d = b * QK + 4 * lane;
+  for (int r0 = 0; r0 < n_rows; r0 += 4) {                         // four independent rows at a time
+    float v[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u;
+      const int chunk = SWZ ? (lane ^ (r & 7)) : lane;
+      const float4 x = *reinterpret_cast<const float4 *>(stg + r * stride + 4 * chunk);
+      v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      wht128_warp(v[u], lane);
+      apply_signs(v[u], a.cbv, lane);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int rr = row0 + r0 + u;
+      if (r0 + u < n_rows && d + 4 <= a.dv) {
+        float *o = a.out + (static_cast<size_t>(q0 + (rr >> g_shift)) * a.n_q_heads + hk * G + (rr & (G - 1))) * a.dv + d;
+        *reinterpret_cast<float4 *>(o) = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+      }
+    }
   }
 }
 
-// One key-block row of a packed tile (qs row, signs row) -> 128 binary16 values
-// in the core-matrix layout of an operand tile (`dst` = the row's first core
-// matrix; the 16 d-octets follow at 128-byte steps).
+// Half hw (elements 64 hw .. 64 hw + 63) of one key-block row of a packed tile
+// (qs row, signs row) -> 64 binary16 values in the core-matrix layout of an
+// operand tile (`dst` = the row's first core matrix; the 16 d-octets of the row
+// follow at 128-byte steps).
 template <int T>
-__device__ __forceinline__ void expand_row(const uint8_t *qrow, const uint8_t *srow, const Tab &tb, unsigned char *dst) {
+__device__ __forceinline__ void expand_half(const uint8_t *qrow, const uint8_t *srow, const Tab &tb, unsigned char *dst,
+                                            int hw) {
   if (T == 4) {
 #pragma unroll
-    for (int w4 = 0; w4 < 4; ++w4) {
+    for (int w2 = 0; w2 < 2; ++w2) {
+      const int w4 = 2 * hw + w2;
       const uint4 w = reinterpret_cast<const uint4 *>(qrow)[w4];
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -174,29 +190,90 @@ __device__ __forceinline__ void expand_row(const uint8_t *qrow, const uint8_t *s
       }
     }
   } else {
-    uint32_t sgw[4] = {0u, 0u, 0u, 0u};
+    uint32_t sgw[2] = {0u, 0u};
     if (T == 3) {
-      const uint4 sg4 = *reinterpret_cast<const uint4 *>(srow);
-      sgw[0] = sg4.x; sgw[1] = sg4.y; sgw[2] = sg4.z; sgw[3] = sg4.w;
+      const uint2 sg2 = reinterpret_cast<const uint2 *>(srow)[hw];
+      sgw[0] = sg2.x; sgw[1] = sg2.y;
     }
+    const uint4 w = reinterpret_cast<const uint4 *>(qrow)[hw];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-    for (int hq = 0; hq < 2; ++hq) {
-      const uint4 w = reinterpret_cast<const uint4 *>(qrow)[hq];
-      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (int i = 0; i < 4; ++i) {
+      const int wi = 4 * hw + i;                       // qs word: elements 16 wi ..
+      uint32_t s0, s1;
+      sel_words<T>(ws[i], sgw[i >> 1], (wi & 1) != 0, s0, s1);
+      uint4 o0, o1;
+      dq4<T>(s0, tb, o0.x, o0.y);
+      dq4<T>(s0 >> 16, tb, o0.z, o0.w);
+      dq4<T>(s1, tb, o1.x, o1.y);
+      dq4<T>(s1 >> 16, tb, o1.z, o1.w);
+      *reinterpret_cast<uint4 *>(dst + (2 * wi) * 128) = o0;
+      *reinterpret_cast<uint4 *>(dst + (2 * wi + 1) * 128) = o1;
+    }
+  }
+}
+
+// Q'_b of rows pr = warp + NWARP (u0 + u), u < NR, of the CTA's 128 query rows:
+// q rotated per 128-dim block (signs, the page's butterflies across the warp,
+// scale * log2(e) / sqrt(128) folded in), stored as binary16 hi + lo.  The NR
+// rows' loads are all issued before any of them is used.
+template <int NBK, int NR, bool F32>
+__device__ __forceinline__ void prep_q_rows(const PrefillArgs &a, unsigned char *qsm, int u0, int warp, int lane,
+                                            int q0, int hk, int g_shift, float f) {
+  constexpr int NW = F32 ? 4 : 2;
+  constexpr uint32_t QBLK = 32768;
+  const int G = a.group;
+  uint32_t raw[NR][NW];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int wi = 4 * hq + i;                       // qs word: elements 16 wi ..
-        uint32_t s0, s1;
-        sel_words<T>(ws[i], sgw[wi >> 1], (wi & 1) != 0, s0, s1);
-        uint4 o0, o1;
-        dq4<T>(s0, tb, o0.x, o0.y);
-        dq4<T>(s0 >> 16, tb, o0.z, o0.w);
-        dq4<T>(s1, tb, o1.x, o1.y);
-        dq4<T>(s1 >> 16, tb, o1.z, o1.w);
-        *reinterpret_cast<uint4 *>(dst + (2 * wi) * 128) = o0;
-        *reinterpret_cast<uint4 *>(dst + (2 * wi + 1) * 128) = o1;
+  for (int u = 0; u < NR; ++u) {
+    const int pr = warp + NWARP * (u0 + u);
+    const int r = pr % BM, b = pr / BM;
+    const int qi = q0 + (r >> g_shift), h = hk * G + (r & (G - 1));
+    const int d = b * QK + 4 * lane;
+#pragma unroll
+    for (int k = 0; k < NW; ++k) raw[u][k] = 0u;
+    if (pr < BM * NBK && qi < a.nq && d + 4 <= a.dk) {
+      const size_t e = (static_cast<size_t>(qi) * a.n_q_heads + h) * a.dk + d;
+      if (F32) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(static_cast<const float *>(a.q) + e);
+        raw[u][0] = x.x; raw[u][1] = x.y; raw[u][2 % NW] = x.z; raw[u][3 % NW] = x.w;
+      } else {
+        const uint2 x = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.q) + e);
+        raw[u][0] = x.x; raw[u][1] = x.y;
       }
     }
+  }
+#pragma unroll
+  for (int u = 0; u < NR; ++u) {
+    const int pr = warp + NWARP * (u0 + u);
+    if (pr >= BM * NBK) break;                      // warp-uniform
+    const int r = pr % BM, b = pr / BM;
+    float v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (F32) {
+        v[k] = __uint_as_float(raw[u][k % NW]);
+      } else {
+        const uint16_t bits = static_cast<uint16_t>(raw[u][k >> 1] >> (16 * (k & 1)));
+        v[k] = a.q_type == TQ_BF16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
+      }
+    }
+    apply_signs(v, a.cbk, lane);
+    wht128_warp(v, lane);
+    const int d0 = 4 * lane;
+    uint16_t hb[4], lb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float x = v[k] * f;
+      const __half hh = __float2half_rn(x);
+      hb[k] = __half_as_ushort(hh);
+      lb[k] = __half_as_ushort(__float2half_rn(x - __half2float(hh)));
+    }
+    const uint32_t off = b * QBLK + ((d0 >> 3) * 16 + (r >> 3)) * 128 + (r & 7) * 16 + (d0 & 7) * 2;
+    *reinterpret_cast<uint2 *>(qsm + off) =
+        make_uint2(hb[0] | (static_cast<uint32_t>(hb[1]) << 16), hb[2] | (static_cast<uint32_t>(hb[3]) << 16));
+    *reinterpret_cast<uint2 *>(qsm + NBK * QBLK + off) =
+        make_uint2(lb[0] | (static_cast<uint32_t>(lb[1]) << 16), lb[2] | (static_cast<uint32_t>(lb[3]) << 16));
   }
 }
 
@@ -209,59 +286,22 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
   __shared__ uint32_t tmem_slot;
   __shared__ int s_fail;
   __shared__ int s_last;
+  __shared__ int s_item;
   // exchange between the two softmax warps of a row (value per row, flag per warp),
   // double-buffered by the parity of the exchange count
   __shared__ float xv[2][2][BM];
   __shared__ int xf[2][2][4];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // grid: (KV head, query tile, split); the longest query tiles (last in the
-  // prompt) are launched first
-  const int hk = blockIdx.x, split = blockIdx.z, n_split = gridDim.z;
-  const int qt = gridDim.y - 1 - blockIdx.y;
   const int G = a.group;
-  const int q0 = qt * (BM / G);
-  const int q_last = min(a.nq, q0 + BM / G) - 1;
+  const int g_shift = __ffs(G) - 1;              // G is a power of two
+  const int n_split = a.n_split;
   const int64_t pos0 = a.kv_len - a.nq;
-  const int64_t kv_hi = a.causal ? i64min(a.kv_len, pos0 + q_last + 1) : a.kv_len;
-  const int tiles_all = static_cast<int>((kv_hi + BN - 1) / BN);
-  const int t_lo = static_cast<int>(static_cast<long long>(tiles_all) * split / n_split);
-  const int t_hi = static_cast<int>(static_cast<long long>(tiles_all) * (split + 1) / n_split);
-  const int n_tiles = t_hi - t_lo;
-
-  const uint8_t *kqs = a.kqs + static_cast<size_t>(hk) * a.n_cells * NBK * QSB;
-  const uint8_t *ksg = SGB ? a.ksg + static_cast<size_t>(hk) * a.n_cells * NBK * SGB : nullptr;
-  const uint16_t *kn = a.kn + static_cast<size_t>(hk) * a.n_cells * NBK;
-  const uint8_t *vqs = a.vqs + static_cast<size_t>(hk) * a.n_cells * NBV * QSB;
-  const uint8_t *vsg = SGB ? a.vsg + static_cast<size_t>(hk) * a.n_cells * NBV * SGB : nullptr;
-  const uint16_t *vn = a.vn + static_cast<size_t>(hk) * a.n_cells * NBV;
-
-  // bulk copies of local tile j (keys past n_cells are not read; n_cells is a
-  // multiple of 64, so every copy stays a multiple of 16 bytes)
-  auto tile_keys = [&](int j) -> int {
-    const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
-    return static_cast<int>(i64min(BN, a.n_cells - key0));
-  };
-  auto issue_k = [&](int j) {
-    unsigned char *st = smem + C::KSTG + (j % C::KST) * C::KSTAGE;
-    uint64_t *bar = &bars.kfull[j % C::KST];
-    const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
-    const int nk = tile_keys(j);
-    tc::mbar_expect_tx(bar, nk * (NBK * (QSB + SGB + 2) + NBV * 2));
-    tc::bulk_g2s(st + C::K_QS, kqs + key0 * NBK * QSB, nk * NBK * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + C::K_SG, ksg + key0 * NBK * SGB, nk * NBK * SGB, bar);
-    tc::bulk_g2s(st + C::K_KN, kn + key0 * NBK, nk * NBK * 2, bar);
-    tc::bulk_g2s(st + C::K_VN, vn + key0 * NBV, nk * NBV * 2, bar);
-  };
-  auto issue_v = [&](int j) {
-    unsigned char *st = smem + C::VSTG + (j % C::VST) * C::VSTAGE;
-    uint64_t *bar = &bars.vfull[j % C::VST];
-    const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
-    const int nk = tile_keys(j);
-    tc::mbar_expect_tx(bar, nk * NBV * (QSB + SGB));
-    tc::bulk_g2s(st + C::V_QS, vqs + key0 * NBV * QSB, nk * NBV * QSB, bar);
-    if (SGB) tc::bulk_g2s(st + C::V_SG, vsg + key0 * NBV * SGB, nk * NBV * SGB, bar);
-  };
+  const uint32_t sbase = tc::smem_u32(smem);
+  float *nrm = reinterpret_cast<float *>(smem + C::NRM);
+  const int row = 32 * (warp & 3) + lane;        // softmax warps: TMEM lane / query row
+  const int half = (warp >> 2) & 1;              // softmax warps: which half of each tile's keys
+  const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
   if (warp == 0) tc::tmem_alloc<C::TMEM_COLS>(&tmem_slot);
   if (tid == CTRL * 32) {
@@ -277,415 +317,470 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
     tc::mbar_init(&bars.dqk, 4);
     tc::mbar_init(&bars.dqv, 4);
     tc::mbar_init_fence();
-    tc::fence_async_smem();
-    for (int i = 0; i < C::KST && i < n_tiles; ++i) issue_k(i);
-    for (int i = 0; i < C::VST && i < n_tiles; ++i) issue_v(i);
   }
-
-  // ---- Q' = q rotated per block (scale * log2(e) / sqrt(128) folded in), binary16 hi + lo
-  {
-    const float f = a.scale_log2 * kInvSqrtQK;
-    for (int pr = warp; pr < BM * NBK; pr += NWARP) {
-      const int r = pr % BM, b = pr / BM;
-      const int qi = q0 + r / G, h = hk * G + r % G;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (qi < a.nq) {
-        const size_t base = (static_cast<size_t>(qi) * a.n_q_heads + h) * a.dk;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int d = b * QK + 4 * lane + k;
-          if (d < a.dk) {
-            if (a.q_type == TQ_BF16)
-              v[k] = __bfloat162float(__ushort_as_bfloat16(static_cast<const uint16_t *>(a.q)[base + d]));
-            else if (a.q_type == TQ_F16)
-              v[k] = __half2float(__ushort_as_half(static_cast<const uint16_t *>(a.q)[base + d]));
-            else
-              v[k] = static_cast<const float *>(a.q)[base + d];
-          }
-        }
-      }
-      apply_signs(v, a.cbk, lane);
-      wht128_warp(v, lane);
-      const int d0 = 4 * lane;
-      uint16_t hb[4], lb[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float x = v[k] * f;
-        const __half hh = __float2half_rn(x);
-        hb[k] = __half_as_ushort(hh);
-        lb[k] = __half_as_ushort(__float2half_rn(x - __half2float(hh)));
-      }
-      const uint32_t off = b * C::QBLK + ((d0 >> 3) * 16 + (r >> 3)) * 128 + (r & 7) * 16 + (d0 & 7) * 2;
-      *reinterpret_cast<uint2 *>(smem + C::Q + off) =
-          make_uint2(hb[0] | (static_cast<uint32_t>(hb[1]) << 16), hb[2] | (static_cast<uint32_t>(hb[3]) << 16));
-      *reinterpret_cast<uint2 *>(smem + C::Q + NBK * C::QBLK + off) =
-          make_uint2(lb[0] | (static_cast<uint32_t>(lb[1]) << 16), lb[2] | (static_cast<uint32_t>(lb[3]) << 16));
-    }
-  }
-  tc::fence_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  const uint32_t sbase = tc::smem_u32(smem);
-  float *nrm = reinterpret_cast<float *>(smem + C::NRM);
+  int xc = 0;                                    // softmax pair exchanges so far
+  int g0 = 0;                                    // tiles this CTA processed before the current item
+                                                 // (every mbarrier phase follows this running count)
 
-  // softmax state (warps 0..7: row = 32 (warp % 4) + lane, keys half * HB .. of each tile)
-  const int row = 32 * (warp & 3) + lane;
-  const int half = (warp >> 2) & 1;
-  const int row_q = q0 + row / G;
-  const bool row_ok = warp < NSM && row_q < a.nq;
-  const int64_t row_end = a.causal ? (pos0 + row_q + 1) : a.kv_len;
-  float m_used = -INFINITY, l_sum = 0.f;
+  // Persistent loop over work items (query tile, KV head, key split), the longest
+  // query tiles first; each CTA takes the next item when it is done with one.
+  for (;;) {
+    if (tid == 0) s_item = atomicAdd(&a.sched[0], 1);
+    __syncthreads();
+    const int item = s_item;
+    if (item >= a.n_items || s_fail) break;
+    const int per_qt = a.n_kv_heads * n_split;
+    const int qt = a.n_qt - 1 - item / per_qt;
+    const int hk = (item % per_qt) % a.n_kv_heads;
+    const int split = (item % per_qt) / a.n_kv_heads;
+    const int q0 = qt * (BM / G);
+    const int q_last = min(a.nq, q0 + BM / G) - 1;
+    const int64_t kv_hi = a.causal ? i64min(a.kv_len, pos0 + q_last + 1) : a.kv_len;
+    const int tiles_all = static_cast<int>((kv_hi + BN - 1) / BN);
+    const int t_lo = static_cast<int>(static_cast<long long>(tiles_all) * split / n_split);
+    const int t_hi = static_cast<int>(static_cast<long long>(tiles_all) * (split + 1) / n_split);
+    const int n_tiles = t_hi - t_lo;
 
-  if (warp == CTRL) {
-    // ===================== control: mma issue =====================
-    if (lane == 0) {
-      constexpr uint32_t ID_S = tc::idesc_f16(BM, BN, false, false);
-      constexpr uint32_t ID_PV = tc::idesc_f16(BM, 128, false, true);
-      // Descriptors: the start-address field holds addr >> 4 in 14 bits and no
-      // operand crosses 256 KB, so an operand at base + off has the descriptor
-      // desc(base) + (off >> 4) -- one add per mma instead of a rebuild.
-      const uint64_t q_desc = tc::sdesc(sbase + C::Q, 2048, 128);
-      const uint64_t k_desc = tc::sdesc(sbase + C::KT, 128, 2048);
-      const uint64_t v_desc = tc::sdesc(sbase + C::VT, 2048, 128);
-      auto issue_pv = [&](int j) {
-        const uint32_t pbuf = tmem + C::SP0 + (j & 1) * C::SPW;
+    const uint8_t *kqs = a.kqs + static_cast<size_t>(hk) * a.n_cells * NBK * QSB;
+    const uint8_t *ksg = SGB ? a.ksg + static_cast<size_t>(hk) * a.n_cells * NBK * SGB : nullptr;
+    const uint16_t *kn = a.kn + static_cast<size_t>(hk) * a.n_cells * NBK;
+    const uint8_t *vqs = a.vqs + static_cast<size_t>(hk) * a.n_cells * NBV * QSB;
+    const uint8_t *vsg = SGB ? a.vsg + static_cast<size_t>(hk) * a.n_cells * NBV * SGB : nullptr;
+    const uint16_t *vn = a.vn + static_cast<size_t>(hk) * a.n_cells * NBV;
+
+    // bulk copies of local tile j (keys past n_cells are not read; n_cells is a
+    // multiple of 64, so every copy stays a multiple of 16 bytes); ring slots and
+    // phases follow the running tile count g0 + j
+    auto tile_keys = [&](int j) -> int {
+      const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
+      return static_cast<int>(i64min(BN, a.n_cells - key0));
+    };
+    auto issue_k = [&](int j) {
+      const int g = g0 + j;
+      unsigned char *st = smem + C::KSTG + (g % C::KST) * C::KSTAGE;
+      uint64_t *bar = &bars.kfull[g % C::KST];
+      const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
+      const int nk = tile_keys(j);
+      tc::mbar_expect_tx(bar, nk * (NBK * (QSB + SGB + 2) + NBV * 2));
+      tc::bulk_g2s(st + C::K_QS, kqs + key0 * NBK * QSB, nk * NBK * QSB, bar);
+      if (SGB) tc::bulk_g2s(st + C::K_SG, ksg + key0 * NBK * SGB, nk * NBK * SGB, bar);
+      tc::bulk_g2s(st + C::K_KN, kn + key0 * NBK, nk * NBK * 2, bar);
+      tc::bulk_g2s(st + C::K_VN, vn + key0 * NBV, nk * NBV * 2, bar);
+    };
+    auto issue_v = [&](int j) {
+      const int g = g0 + j;
+      unsigned char *st = smem + C::VSTG + (g % C::VST) * C::VSTAGE;
+      uint64_t *bar = &bars.vfull[g % C::VST];
+      const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN;
+      const int nk = tile_keys(j);
+      tc::mbar_expect_tx(bar, nk * NBV * (QSB + SGB));
+      tc::bulk_g2s(st + C::V_QS, vqs + key0 * NBV * QSB, nk * NBV * QSB, bar);
+      if (SGB) tc::bulk_g2s(st + C::V_SG, vsg + key0 * NBV * SGB, nk * NBV * SGB, bar);
+    };
+    if (tid == CTRL * 32) {
+      tc::fence_async_smem();
+      for (int i = 0; i < C::KST && i < n_tiles; ++i) issue_k(i);
+      for (int i = 0; i < C::VST && i < n_tiles; ++i) issue_v(i);
+    }
+
+    // ---- Q' = q rotated per block, binary16 hi + lo (every row of a warp loaded at once)
+    {
+      constexpr int RPW = (BM * NBK + NWARP - 1) / NWARP;          // row blocks per warp
+      const float f = a.scale_log2 * kInvSqrtQK;
+      if (a.q_type == TQ_F32) {
+        prep_q_rows<NBK, (RPW + 1) / 2, true>(a, smem + C::Q, 0, warp, lane, q0, hk, g_shift, f);
+        prep_q_rows<NBK, RPW / 2, true>(a, smem + C::Q, (RPW + 1) / 2, warp, lane, q0, hk, g_shift, f);
+      } else {
+        prep_q_rows<NBK, RPW, false>(a, smem + C::Q, 0, warp, lane, q0, hk, g_shift, f);
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    // softmax state (warps 0..7)
+    const int row_q = q0 + (row >> g_shift);
+    const bool row_ok = warp < NSM && row_q < a.nq;
+    const int64_t row_end = a.causal ? (pos0 + row_q + 1) : a.kv_len;
+    float m_used = -INFINITY, l_sum = 0.f;
+
+    if (warp == CTRL) {
+      // ===================== control: mma issue =====================
+      if (lane == 0) {
+        constexpr uint32_t ID_S = tc::idesc_f16(BM, BN, false, false);
+        constexpr uint32_t ID_PV = tc::idesc_f16(BM, 128, false, true);
+        // Descriptors: the start-address field holds addr >> 4 in 14 bits and no
+        // operand crosses 256 KB, so an operand at base + off has the descriptor
+        // desc(base) + (off >> 4) -- one add per mma instead of a rebuild.
+        const uint64_t q_desc = tc::sdesc(sbase + C::Q, 2048, 128);
+        const uint64_t k_desc = tc::sdesc(sbase + C::KT, 128, 2048);
+        const uint64_t v_desc = tc::sdesc(sbase + C::VT, 2048, 128);
+        auto issue_pv = [&](int j) {
+          const int g = g0 + j;
+          const uint32_t pbuf = tmem + C::SP0 + (g & 1) * C::SPW;
+#pragma unroll
+          for (int b = 0; b < NBV; ++b)
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+              for (int ks = 0; ks < BN / 16; ++ks) {
+                const uint64_t bd = v_desc + ((b * C::TBLK + ks * 4096) >> 4);
+                mma_f16_ta(tmem + b * 128, pbuf + (2 * b + part) * (BN / 2) + ks * 8, bd, ID_PV,
+                           j > 0 || part > 0 || ks > 0);
+              }
+          tc::mma_commit(&bars.pv[g & 1]);
+        };
+        bool ok = true;
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const int g = g0 + j;
+          ok = tc::mbar_wait(&bars.dqk, g & 1);                       // K'_j expanded
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t sbuf = tmem + C::SP0 + (g & 1) * C::SPW;
+#pragma unroll
+          for (int b = 0; b < NBK; ++b)
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t ad = q_desc + (((part * NBK + b) * C::QBLK + ks * 4096) >> 4);
+                const uint64_t bd = k_desc + ((b * C::TBLK + ks * 256) >> 4);
+                tc::mma_f16(sbuf + b * BN, ad, bd, ID_S, part > 0 || ks > 0);
+              }
+          tc::mma_commit(&bars.sf[g & 1]);
+          if (j >= 1) {
+            ok = tc::mbar_wait(&bars.pf[(g - 1) & 1], ((g - 1) >> 1) & 1) && tc::mbar_wait(&bars.dqv, (g - 1) & 1);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_pv(j - 1);
+          }
+        }
+        if (ok && n_tiles > 0) {
+          const int j = n_tiles - 1, g = g0 + j;
+          ok = tc::mbar_wait(&bars.pf[g & 1], (g >> 1) & 1) && tc::mbar_wait(&bars.dqv, g & 1);
+          if (ok) {
+            tc::fence_after_sync();
+            issue_pv(j);
+          }
+        }
+        if (!ok) s_fail = 1;
+      }
+    } else if (warp >= DQ0) {
+      // ===================== dequant: one key-block row per thread =====================
+      // program order K'_0, then K'_{j+1} before V'_j: S_{j+1} never waits for a V tile
+      const int dt = tid - DQ0 * 32;                             // 0..127
+      const Tab tab_k{a.tabk[0], a.tabk[1], a.tabk[2], a.tabk[3]};
+      const Tab tab_v{a.tabv[0], a.tabv[1], a.tabv[2], a.tabv[3]};
+      unsigned char *kt = smem + C::KT;
+      unsigned char *vt = smem + C::VT;
+      auto k_phase = [&](int j) -> bool {
+        const int g = g0 + j;
+        bool ok = tc::mbar_wait(&bars.kfull[g % C::KST], (g / C::KST) & 1);
+        if (ok && j >= 2) ok = tc::mbar_wait(&bars.pf[(g - 2) & 1], ((g - 2) >> 1) & 1);    // norm buffer free
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        tc::fence_after_sync();
+        const unsigned char *st = smem + C::KSTG + (g % C::KST) * C::KSTAGE;
+        if (dt < BN) {
+          // norms of the tile's keys; keys past the last one any row of this
+          // item attends (or past the cells) read as 0, so that a masked key's
+          // weight p = 0 gives p |v| = 0 whatever its bytes
+          const uint16_t *knp = reinterpret_cast<const uint16_t *>(st + C::K_KN) + dt * NBK;
+          const uint16_t *vnp = reinterpret_cast<const uint16_t *>(st + C::K_VN) + dt * NBV;
+          const bool live = static_cast<int64_t>(t_lo + j) * BN + dt < kv_hi;
+          float4 w;
+          w.x = live ? __half2float(__ushort_as_half(knp[0])) : 0.f;
+          w.y = (live && NBK > 1) ? __half2float(__ushort_as_half(knp[NBK > 1 ? 1 : 0])) : 0.f;
+          w.z = live ? __half2float(__ushort_as_half(vnp[0])) : 0.f;
+          w.w = (live && NBV > 1) ? __half2float(__ushort_as_half(vnp[NBV > 1 ? 1 : 0])) : 0.f;
+          reinterpret_cast<float4 *>(nrm)[(g & 1) * BN + dt] = w;
+        }
+        // K' (two threads per key row, half a row each) once S_{j-1} is done with it
+        ok = (j == 0) || tc::mbar_wait(&bars.sf[(g - 1) & 1], ((g - 1) >> 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        tc::fence_after_sync();
+        for (int r = dt; r < 2 * NBK * BN; r += 128) {
+          const int b = r / (2 * BN), key = (r >> 1) % BN, hw = r & 1;
+          expand_half<T>(st + C::K_QS + (key * NBK + b) * QSB, st + C::K_SG + (key * NBK + b) * SGB, tab_k,
+                         kt + b * C::TBLK + (key >> 3) * 2048 + (key & 7) * 16, hw);
+        }
+        tc::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars.nrmf[g & 1]);
+          mbar_arrive(&bars.dqk);
+        }
+        // the K stage of tile j is free once all four dequant warps are done with it
+        if (warp == DQ0 && lane == 0 && j + C::KST < n_tiles) {
+          if (tc::mbar_wait(&bars.dqk, g & 1)) issue_k(j + C::KST);
+          else s_fail = 1;
+        }
+        return true;
+      };
+      auto v_phase = [&](int j) -> bool {
+        const int g = g0 + j;
+        bool ok = tc::mbar_wait(&bars.vfull[g % C::VST], (g / C::VST) & 1);
+        if (ok && j >= 1) ok = tc::mbar_wait(&bars.pv[(g - 1) & 1], ((g - 1) >> 1) & 1);    // V' tile free
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        tc::fence_after_sync();
+        const unsigned char *st = smem + C::VSTG + (g % C::VST) * C::VSTAGE;
+        for (int r = dt; r < 2 * NBV * BN; r += 128) {
+          const int b = r / (2 * BN), key = (r >> 1) % BN, hw = r & 1;
+          expand_half<T>(st + C::V_QS + (key * NBV + b) * QSB, st + C::V_SG + (key * NBV + b) * SGB, tab_v,
+                         vt + b * C::TBLK + (key >> 3) * 2048 + (key & 7) * 16, hw);
+        }
+        tc::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.dqv);
+        if (warp == DQ0 && lane == 0 && j + C::VST < n_tiles) {
+          if (tc::mbar_wait(&bars.dqv, g & 1)) issue_v(j + C::VST);
+          else s_fail = 1;
+        }
+        return true;
+      };
+      bool ok = n_tiles == 0 || k_phase(0);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        if (j + 1 < n_tiles) ok = k_phase(j + 1);
+        if (ok) ok = v_phase(j);
+      }
+      if (!ok) s_fail = 1;
+    } else {
+      // ===================== softmax: one query row, half the keys per thread =====================
+      const int bar_id = 1 + (warp & 3);                     // named barrier of the warp pair
+      // swap a value (per row) and a warp-uniform flag with the partner warp; both
+      // warps of a pair make the same sequence of calls, so a failed wait ends both
+      // loops at the same point and no named barrier is left waiting
+      auto exchange = [&](float v, bool f, float &pv, bool &pflag) {
+        const int p = xc & 1;
+        ++xc;
+        xv[p][half][row] = v;
+        if (lane == 0) xf[p][half][warp & 3] = f ? 1 : 0;
+        tc::named_sync(bar_id, 64);
+        pv = xv[p][half ^ 1][row];
+        pflag = xf[p][half ^ 1][warp & 3] != 0;
+      };
+      bool ok = true;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int g = g0 + j;
+        bool okw = tc::mbar_wait(&bars.sf[g & 1], (g >> 1) & 1);
+        if (okw) okw = tc::mbar_wait(&bars.nrmf[g & 1], (g >> 1) & 1);
+        okw = __all_sync(0xffffffffu, okw);
+        tc::fence_after_sync();
+        const uint32_t sbuf = tmem + lane_off + C::SP0 + (g & 1) * C::SPW;
+        const float4 *nr = reinterpret_cast<const float4 *>(nrm) + (g & 1) * BN + half * HB;
+        const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN + half * HB;
+        const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(HB, i64min(row_end, kv_hi) - key0))) : 0;
+        float s[HB];
+        float mt = -INFINITY;
+        if (okw) {
+          uint32_t r0[NBK * HB];                               // this thread's S columns, one wait
+#pragma unroll
+          for (int b = 0; b < NBK; ++b)
+#pragma unroll
+            for (int c0 = 0; c0 < HB; c0 += 32) tc::tmem_ld32(sbuf + b * BN + half * HB + c0, r0 + b * HB + c0);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < HB; ++i) {
+            const float2 n2 = *reinterpret_cast<const float2 *>(nr + i);
+            float x = n2.x * __uint_as_float(r0[i]);
+            if (NBK > 1) x = fmaf(n2.y, __uint_as_float(r0[(NBK > 1 ? HB : 0) + i]), x);
+            s[i] = (i < nvis) ? x : -INFINITY;               // masked keys: weight exactly 0 below
+            mt = fmaxf(mt, s[i]);
+          }
+        }
+        // row maximum over both halves of the tile
+        float pmt;
+        bool pok;
+        exchange(mt, okw, pmt, pok);
+        if (!(okw && pok)) { ok = false; break; }
+        mt = fmaxf(mt, pmt);
+        const bool raise = mt > m_used + kLazyRescale || (m_used == -INFINITY && mt > -INFINITY);
+        const float fct = (raise && m_used != -INFINITY) ? exp2f(m_used - mt) : 1.f;
+        if (raise) m_used = mt;
+        if (__any_sync(0xffffffffu, fct != 1.f)) {           // the same decision in both warps of the pair
+          // O must be stable: wait for the PV mma of the previous tile; each half
+          // rescales its half of the O columns
+          bool okp = (j == 0) || tc::mbar_wait(&bars.pv[(g - 1) & 1], ((g - 1) >> 1) & 1);
+          okp = __all_sync(0xffffffffu, okp);
+          float unused;
+          bool pokp;
+          exchange(0.f, okp, unused, pokp);
+          if (!(okp && pokp)) { ok = false; break; }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int c = half * (DVP / 2); c < (half + 1) * (DVP / 2); c += 32) {
+            uint32_t r[32];
+            tc::tmem_ld32(tmem + lane_off + c, r);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * fct);
+            tc::tmem_st32(tmem + lane_off + c, r);
+          }
+        }
+        l_sum *= fct;
+        // m_used is finite once any key was visible; a row with no visible key so
+        // far keeps -inf and every weight 0
+        const float msub = m_used == -INFINITY ? 0.f : m_used;
+        float psum = 0.f;
+#pragma unroll
+        for (int i = 0; i < HB; ++i) {
+          s[i] = tc::ex2(s[i] - msub);                       // -inf -> 0
+          psum += s[i];
+        }
+        l_sum += psum;
+        // P'_(b, hi/lo) into tensor memory over S_j: row = lane, fp16 pairs of keys;
+        // this half's keys are columns half * HB/2 .. of each (b, part) region
 #pragma unroll
         for (int b = 0; b < NBV; ++b)
 #pragma unroll
-          for (int part = 0; part < 2; ++part)
+          for (int c16 = 0; c16 < HB / 2; c16 += 16) {        // 16 columns (32 keys) at a time
+            uint32_t ph[16], pl[16];
 #pragma unroll
-            for (int ks = 0; ks < BN / 16; ++ks) {
-              const uint64_t bd = v_desc + ((b * C::TBLK + ks * 4096) >> 4);
-              mma_f16_ta(tmem + b * 128, pbuf + (2 * b + part) * (BN / 2) + ks * 8, bd, ID_PV,
-                         j > 0 || part > 0 || ks > 0);
+            for (int i = 0; i < 16; ++i) {
+              const int k0 = 2 * (c16 + i);
+              const float2 vn0 = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(nr + k0) + 2);
+              const float2 vn1 = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(nr + k0 + 1) + 2);
+              const float x0 = s[k0] * (b == 0 ? vn0.x : vn0.y);
+              const float x1 = s[k0 + 1] * (b == 0 ? vn1.x : vn1.y);
+              const __half2 h = __floats2half2_rn(x0, x1);
+              const float2 hf = __half22float2(h);
+              const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+              ph[i] = *reinterpret_cast<const uint32_t *>(&h);
+              pl[i] = *reinterpret_cast<const uint32_t *>(&l);
             }
-        tc::mma_commit(&bars.pv[j & 1]);
-      };
-      bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        ok = tc::mbar_wait(&bars.dqk, j & 1);                       // K'_j expanded
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint32_t sbuf = tmem + C::SP0 + (j & 1) * C::SPW;
-#pragma unroll
-        for (int b = 0; b < NBK; ++b)
-#pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t ad = q_desc + (((part * NBK + b) * C::QBLK + ks * 4096) >> 4);
-              const uint64_t bd = k_desc + ((b * C::TBLK + ks * 256) >> 4);
-              tc::mma_f16(sbuf + b * BN, ad, bd, ID_S, part > 0 || ks > 0);
-            }
-        tc::mma_commit(&bars.sf[j & 1]);
-        if (j >= 1) {
-          ok = tc::mbar_wait(&bars.pf[(j - 1) & 1], ((j - 1) >> 1) & 1) && tc::mbar_wait(&bars.dqv, (j - 1) & 1);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_pv(j - 1);
-        }
+            tmem_st<16>(sbuf + (2 * b) * (BN / 2) + half * (HB / 2) + c16, ph);
+            tmem_st<16>(sbuf + (2 * b + 1) * (BN / 2) + half * (HB / 2) + c16, pl);
+          }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.pf[g & 1]);
       }
+      // the last PV must be complete before O is read
       if (ok && n_tiles > 0) {
-        const int j = n_tiles - 1;
-        ok = tc::mbar_wait(&bars.pf[j & 1], (j >> 1) & 1) && tc::mbar_wait(&bars.dqv, j & 1);
-        if (ok) {
-          tc::fence_after_sync();
-          issue_pv(j);
-        }
+        const int g = g0 + n_tiles - 1;
+        ok = tc::mbar_wait(&bars.pv[g & 1], (g >> 1) & 1);
+        ok = __all_sync(0xffffffffu, ok);
+        tc::fence_after_sync();
       }
       if (!ok) s_fail = 1;
     }
-  } else if (warp >= DQ0) {
-    // ===================== dequant: one key-block row per thread =====================
-    // program order K'_0, then K'_{j+1} before V'_j: S_{j+1} never waits for a V tile
-    const int dt = tid - DQ0 * 32;                             // 0..127
-    const Tab tab_k{a.tabk[0], a.tabk[1], a.tabk[2], a.tabk[3]};
-    const Tab tab_v{a.tabv[0], a.tabv[1], a.tabv[2], a.tabv[3]};
-    unsigned char *kt = smem + C::KT;
-    unsigned char *vt = smem + C::VT;
-    auto k_phase = [&](int j) -> bool {
-      bool ok = tc::mbar_wait(&bars.kfull[j % C::KST], (j / C::KST) & 1);
-      if (ok && j >= 1) ok = tc::mbar_wait(&bars.sf[(j - 1) & 1], ((j - 1) >> 1) & 1);    // K' tile free
-      if (ok && j >= 2) ok = tc::mbar_wait(&bars.pf[(j - 2) & 1], ((j - 2) >> 1) & 1);    // norm buffer free
-      if (!__all_sync(0xffffffffu, ok)) return false;
-      tc::fence_after_sync();
-      const unsigned char *st = smem + C::KSTG + (j % C::KST) * C::KSTAGE;
-      for (int r = dt; r < NBK * BN; r += 128) {
-        const int b = r / BN, key = r % BN;
-        expand_row<T>(st + C::K_QS + (key * NBK + b) * QSB, st + C::K_SG + (key * NBK + b) * SGB, tab_k,
-                      kt + b * C::TBLK + (key >> 3) * 2048 + (key & 7) * 16);
-      }
-      if (dt < BN) {
-        const uint16_t *knp = reinterpret_cast<const uint16_t *>(st + C::K_KN) + dt * NBK;
-        const uint16_t *vnp = reinterpret_cast<const uint16_t *>(st + C::K_VN) + dt * NBV;
-        float4 w;
-        w.x = __half2float(__ushort_as_half(knp[0]));
-        w.y = NBK > 1 ? __half2float(__ushort_as_half(knp[NBK > 1 ? 1 : 0])) : 0.f;
-        w.z = __half2float(__ushort_as_half(vnp[0]));
-        w.w = NBV > 1 ? __half2float(__ushort_as_half(vnp[NBV > 1 ? 1 : 0])) : 0.f;
-        reinterpret_cast<float4 *>(nrm)[(j & 1) * BN + dt] = w;
-      }
-      tc::fence_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars.nrmf[j & 1]);
-        mbar_arrive(&bars.dqk);
-      }
-      // the K stage of tile j is free once all four dequant warps are done with it
-      if (warp == DQ0 && lane == 0 && j + C::KST < n_tiles) {
-        if (tc::mbar_wait(&bars.dqk, j & 1)) issue_k(j + C::KST);
-        else s_fail = 1;
-      }
-      return true;
-    };
-    auto v_phase = [&](int j) -> bool {
-      bool ok = tc::mbar_wait(&bars.vfull[j % C::VST], (j / C::VST) & 1);
-      if (ok && j >= 1) ok = tc::mbar_wait(&bars.pv[(j - 1) & 1], ((j - 1) >> 1) & 1);    // V' tile free
-      if (!__all_sync(0xffffffffu, ok)) return false;
-      tc::fence_after_sync();
-      const unsigned char *st = smem + C::VSTG + (j % C::VST) * C::VSTAGE;
-      for (int r = dt; r < NBV * BN; r += 128) {
-        const int b = r / BN, key = r % BN;
-        expand_row<T>(st + C::V_QS + (key * NBV + b) * QSB, st + C::V_SG + (key * NBV + b) * SGB, tab_v,
-                      vt + b * C::TBLK + (key >> 3) * 2048 + (key & 7) * 16);
-      }
-      tc::fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.dqv);
-      if (warp == DQ0 && lane == 0 && j + C::VST < n_tiles) {
-        if (tc::mbar_wait(&bars.dqv, j & 1)) issue_v(j + C::VST);
-        else s_fail = 1;
-      }
-      return true;
-    };
-    bool ok = n_tiles == 0 || k_phase(0);
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      if (j + 1 < n_tiles) ok = k_phase(j + 1);
-      if (ok) ok = v_phase(j);
-    }
-    if (!ok) s_fail = 1;
-  } else {
-    // ===================== softmax: one query row, half the keys per thread =====================
-    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const int bar_id = 1 + (warp & 3);                     // named barrier of the warp pair
-    int xc = 0;
-    // swap a value (per row) and a warp-uniform flag with the partner warp; both
-    // warps of a pair make the same sequence of calls, so a failed wait ends both
-    // loops at the same point and no named barrier is left waiting
-    auto exchange = [&](float v, bool f, float &pv, bool &pflag) {
-      const int p = xc & 1;
-      ++xc;
-      xv[p][half][row] = v;
-      if (lane == 0) xf[p][half][warp & 3] = f ? 1 : 0;
-      tc::named_sync(bar_id, 64);
-      pv = xv[p][half ^ 1][row];
-      pflag = xf[p][half ^ 1][warp & 3] != 0;
-    };
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      bool okw = tc::mbar_wait(&bars.sf[j & 1], (j >> 1) & 1);
-      if (okw) okw = tc::mbar_wait(&bars.nrmf[j & 1], (j >> 1) & 1);
-      okw = __all_sync(0xffffffffu, okw);
-      tc::fence_after_sync();
-      const uint32_t sbuf = tmem + lane_off + C::SP0 + (j & 1) * C::SPW;
-      const float4 *nr = reinterpret_cast<const float4 *>(nrm) + (j & 1) * BN + half * HB;
-      const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN + half * HB;
-      const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(HB, i64min(row_end, kv_hi) - key0))) : 0;
-      float s[HB];
-      float mt = -INFINITY;
-      if (okw) {
-        uint32_t r0[NBK * HB];                               // this thread's S columns, one wait
+
+    // ===================== epilogue of the item =====================
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    // row sums of the two halves
+    if (warp < NSM) xv[0][half][row] = l_sum;
+    __syncthreads();
+    const float l_row = (warp < NSM) ? xv[0][0][row] + xv[0][1][row] : 0.f;
+    const bool failed = s_fail != 0;
+    if (failed && tid == 0) set_status(a.status, TQ_ERR_TIMEOUT);
+
+    float *stg = reinterpret_cast<float *>(smem + C::Q) + (warp & 7) * 32 * 128;   // [32][128] per softmax warp
+    if (n_split == 1) {
+      // half b stages V block b of its row (divided by l and sqrt(128)), then its
+      // warp rotates the 32 rows back and stores them
+      if (warp < NSM && half < NBV && !failed) {
+        const float inv = (l_row > 0.f ? 1.f / l_row : 0.f) * kInvSqrtQK;
+        const int b = half;
 #pragma unroll
-        for (int b = 0; b < NBK; ++b)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld32(tmem + lane_off + b * 128 + 32 * c, r);
+          tc::tmem_wait_ld();
 #pragma unroll
-          for (int c0 = 0; c0 < HB; c0 += 32) tc::tmem_ld32(sbuf + b * BN + half * HB + c0, r0 + b * HB + c0);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < HB; ++i) {
-          const float4 n4 = nr[i];
-          float x = n4.x * __uint_as_float(r0[i]);
-          if (NBK > 1) x = fmaf(n4.y, __uint_as_float(r0[(NBK > 1 ? HB : 0) + i]), x);
-          s[i] = x;
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4 *>(stg + lane * 128 + 4 * ((8 * c + i / 4) ^ (lane & 7))) =
+                n_tiles > 0 ? make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
+                                          __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-#pragma unroll
-        for (int i = 0; i < HB; ++i)
-          if (i < nvis) mt = fmaxf(mt, s[i]);
+        __syncwarp();
+        rotate_store_rows<true>(stg, 128, a, 32 * (warp & 3), q0, hk, b, lane);
       }
-      // row maximum over both halves of the tile
-      float pmt;
-      bool pok;
-      exchange(mt, okw, pmt, pok);
-      if (!(okw && pok)) { ok = false; break; }
-      mt = fmaxf(mt, pmt);
-      const bool raise = mt > m_used + kLazyRescale || (m_used == -INFINITY && mt > -INFINITY);
-      const float fct = (raise && m_used != -INFINITY) ? exp2f(m_used - mt) : 1.f;
-      if (raise) m_used = mt;
-      if (__any_sync(0xffffffffu, fct != 1.f)) {           // the same decision in both warps of the pair
-        // O must be stable: wait for the PV mma of the previous tile; each half
-        // rescales its half of the O columns
-        bool okp = (j == 0) || tc::mbar_wait(&bars.pv[(j - 1) & 1], ((j - 1) >> 1) & 1);
-        okp = __all_sync(0xffffffffu, okp);
-        float unused;
-        bool pokp;
-        exchange(0.f, okp, unused, pokp);
-        if (!(okp && pokp)) { ok = false; break; }
-        tc::fence_after_sync();
-#pragma unroll
+    } else {
+      // split key range: store (m, l, O) of every row; the last CTA of this query tile merges
+      const size_t tile_id = static_cast<size_t>(qt) * a.n_kv_heads + hk;
+      const size_t stride = 4 + DVP;             // m, l, 2 pad floats: O rows stay 16-byte aligned
+      float *part = a.part + (tile_id * n_split + split) * BM * stride;
+      if (warp < NSM) {
+        float *pr = part + static_cast<size_t>(row) * stride;
+        const bool has = !failed && n_tiles > 0;
+        if (half == 0) {
+          pr[0] = has ? m_used : -INFINITY;
+          pr[1] = has ? l_row : 0.f;
+        }
+#pragma unroll 1
         for (int c = half * (DVP / 2); c < (half + 1) * (DVP / 2); c += 32) {
           uint32_t r[32];
           tc::tmem_ld32(tmem + lane_off + c, r);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * fct);
-          tc::tmem_st32(tmem + lane_off + c, r);
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4 *>(pr + 4 + c + i) =
+                has ? make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                                  __uint_as_float(r[i + 3]))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      l_sum *= fct;
-      float psum = 0.f;
-#pragma unroll
-      for (int i = 0; i < HB; ++i) {
-        s[i] = (i < nvis) ? tc::ex2(s[i] - m_used) : 0.f;
-        psum += s[i];
-      }
-      l_sum += psum;
-      // P'_(b, hi/lo) into tensor memory over S_j: row = lane, fp16 pairs of keys;
-      // this half's keys are columns half * HB/2 .. of each (b, part) region
-#pragma unroll
-      for (int b = 0; b < NBV; ++b)
-#pragma unroll
-        for (int c16 = 0; c16 < HB / 2; c16 += 16) {        // 16 columns (32 keys) at a time
-          uint32_t ph[16], pl[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int k0 = 2 * (c16 + i);
-            // masked keys may carry garbage norms: select, never multiply, a zero
-            const float vn0 = b == 0 ? nr[k0].z : nr[k0].w;
-            const float vn1 = b == 0 ? nr[k0 + 1].z : nr[k0 + 1].w;
-            const float x0 = s[k0] > 0.f ? s[k0] * vn0 : 0.f;
-            const float x1 = s[k0 + 1] > 0.f ? s[k0 + 1] * vn1 : 0.f;
-            const __half2 h = __floats2half2_rn(x0, x1);
-            const float2 hf = __half22float2(h);
-            const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-            ph[i] = *reinterpret_cast<const uint32_t *>(&h);
-            pl[i] = *reinterpret_cast<const uint32_t *>(&l);
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) s_last = (atomicAdd(&a.counters[tile_id], 1) == n_split - 1);
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        const float *base = a.part + tile_id * n_split * BM * stride;
+        float *wts = reinterpret_cast<float *>(smem + C::KSTG);       // [BM][n_split] weights / L
+        float *acc = reinterpret_cast<float *>(smem + C::Q);          // [BM][DVP] merged rows
+        if (tid < min(BM, (a.nq - q0) * G)) {
+          float M = -INFINITY;
+          for (int s2 = 0; s2 < n_split; ++s2)
+            M = fmaxf(M, __ldcg(base + (static_cast<size_t>(s2) * BM + tid) * stride));
+          float L = 0.f;
+          for (int s2 = 0; s2 < n_split; ++s2) {
+            const float *p = base + (static_cast<size_t>(s2) * BM + tid) * stride;
+            const float m = __ldcg(p);
+            const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+            wts[tid * n_split + s2] = w;
+            L += w * __ldcg(p + 1);
           }
-          tmem_st<16>(sbuf + (2 * b) * (BN / 2) + half * (HB / 2) + c16, ph);
-          tmem_st<16>(sbuf + (2 * b + 1) * (BN / 2) + half * (HB / 2) + c16, pl);
+          const float inv = (L > 0.f ? 1.f / L : 0.f) * kInvSqrtQK;
+          for (int s2 = 0; s2 < n_split; ++s2) wts[tid * n_split + s2] *= inv;
         }
-      tc::tmem_wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.pf[j & 1]);
+        __syncthreads();
+        const int rows_valid = min(BM, (a.nq - q0) * G);          // rows of queries < nq
+        for (int i = tid; i < rows_valid * DVP; i += NT) {
+          const int r = i / DVP, d = i % DVP;
+          float o = 0.f;
+          for (int s2 = 0; s2 < n_split; ++s2)
+            o += wts[r * n_split + s2] * __ldcg(base + (static_cast<size_t>(s2) * BM + r) * stride + 4 + d);
+          acc[i] = o;
+        }
+        __syncthreads();
+        if (warp < NSM && half < NBV)           // merged rows of V block b (weights include 1/sqrt(128))
+          rotate_store_rows<false>(acc + 32 * (warp & 3) * DVP + half * 128, DVP, a, 32 * (warp & 3), q0, hk, half,
+                                   lane);
+        if (tid == 0) a.counters[tile_id] = 0;
+      }
     }
-    // the last PV must be complete before O is read
-    if (ok && n_tiles > 0) {
-      const int j = n_tiles - 1;
-      ok = tc::mbar_wait(&bars.pv[j & 1], (j >> 1) & 1);
-      ok = __all_sync(0xffffffffu, ok);
-      tc::fence_after_sync();
-    }
-    if (!ok) s_fail = 1;
+    g0 += n_tiles;
+    tc::fence_before_sync();
+    __syncthreads();                             // shared memory and tensor memory free for the next item
+    tc::fence_after_sync();
   }
 
-  // ===================== epilogue =====================
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  // row sums of the two halves
-  if (warp < NSM) xv[0][half][row] = l_sum;
-  __syncthreads();
-  const float l_row = (warp < NSM) ? xv[0][0][row] + xv[0][1][row] : 0.f;
-  const bool failed = s_fail != 0;
-  if (failed && tid == 0) set_status(a.status, TQ_ERR_TIMEOUT);
-  const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-
-  float *stg = reinterpret_cast<float *>(smem + C::Q) + (warp & 7) * 32 * 128;   // [32][128] per softmax warp
-  if (n_split == 1) {
-    // half b stages V block b of its row (divided by l and sqrt(128)), then its
-    // warp rotates the 32 rows back and stores them
-    if (warp < NSM && half < NBV && !failed) {
-      const float inv = (l_row > 0.f ? 1.f / l_row : 0.f) * kInvSqrtQK;
-      const int b = half;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + lane_off + b * 128 + 32 * c, r);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4 *>(stg + lane * 128 + 4 * ((8 * c + i / 4) ^ (lane & 7))) =
-              n_tiles > 0 ? make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
-                                        __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      __syncwarp();
-      rotate_store_rows<true>(stg, 128, a, 32 * (warp & 3), q0, hk, b, lane);
-    }
-  } else {
-    // split key range: store (m, l, O) of every row; the last CTA of this query tile merges
-    const size_t tile_id = static_cast<size_t>(qt) * a.n_kv_heads + hk;
-    const size_t stride = 4 + DVP;             // m, l, 2 pad floats: O rows stay 16-byte aligned
-    float *part = a.part + (tile_id * n_split + split) * BM * stride;
-    if (warp < NSM) {
-      float *pr = part + static_cast<size_t>(row) * stride;
-      const bool has = !failed && n_tiles > 0;
-      if (half == 0) {
-        pr[0] = has ? m_used : -INFINITY;
-        pr[1] = has ? l_row : 0.f;
-      }
-#pragma unroll 1
-      for (int c = half * (DVP / 2); c < (half + 1) * (DVP / 2); c += 32) {
-        uint32_t r[32];
-        tc::tmem_ld32(tmem + lane_off + c, r);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4 *>(pr + 4 + c + i) =
-              has ? make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
-                                __uint_as_float(r[i + 3]))
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
+  // the last CTA out resets the work counters for the next launch
+  if (tid == 0) {
     __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = (atomicAdd(&a.counters[tile_id], 1) == n_split - 1);
-    __syncthreads();
-    if (s_last) {
+    if (atomicAdd(&a.sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
+      a.sched[0] = 0;
+      a.sched[1] = 0;
       __threadfence();
-      const float *base = a.part + tile_id * n_split * BM * stride;
-      float *wts = reinterpret_cast<float *>(smem + C::KSTG);       // [BM][n_split] weights / L
-      float *acc = reinterpret_cast<float *>(smem + C::Q);          // [BM][DVP] merged rows
-      if (tid < min(BM, (a.nq - q0) * G)) {
-        float M = -INFINITY;
-        for (int s2 = 0; s2 < n_split; ++s2)
-          M = fmaxf(M, __ldcg(base + (static_cast<size_t>(s2) * BM + tid) * stride));
-        float L = 0.f;
-        for (int s2 = 0; s2 < n_split; ++s2) {
-          const float *p = base + (static_cast<size_t>(s2) * BM + tid) * stride;
-          const float m = __ldcg(p);
-          const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-          wts[tid * n_split + s2] = w;
-          L += w * __ldcg(p + 1);
-        }
-        const float inv = (L > 0.f ? 1.f / L : 0.f) * kInvSqrtQK;
-        for (int s2 = 0; s2 < n_split; ++s2) wts[tid * n_split + s2] *= inv;
-      }
-      __syncthreads();
-      const int rows_valid = min(BM, (a.nq - q0) * G);          // rows of queries < nq
-      for (int i = tid; i < rows_valid * DVP; i += NT) {
-        const int r = i / DVP, d = i % DVP;
-        float o = 0.f;
-        for (int s2 = 0; s2 < n_split; ++s2)
-          o += wts[r * n_split + s2] * __ldcg(base + (static_cast<size_t>(s2) * BM + r) * stride + 4 + d);
-        acc[i] = o;
-      }
-      __syncthreads();
-      if (warp < NSM && half < NBV)           // merged rows of V block b (weights include 1/sqrt(128))
-        rotate_store_rows<false>(acc + 32 * (warp & 3) * DVP + half * 128, DVP, a, 32 * (warp & 3), q0, hk, half,
-                                 lane);
-      if (tid == 0) a.counters[tile_id] = 0;
     }
   }
   tc::fence_before_sync();
@@ -705,7 +800,8 @@ cudaError_t launch_one(const PrefillArgs &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, NBK, NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::TOTAL);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.n_kv_heads, (a.nq * a.group + BM - 1) / BM, a.n_split);
+  // persistent: at most one CTA per SM (each CTA holds most of an SM's shared memory)
+  const int grid = min(a.n_items, sm_count());
   prefill_kernel<T, NBK, NBV><<<grid, NT, C::TOTAL, s>>>(a);
   return cudaGetLastError();
 }
