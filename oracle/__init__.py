@@ -332,7 +332,7 @@ def dequantize_cache(cache: Cache, sign_bits, cents: np.ndarray, n: int, head: i
         codes = unpack_codes(cache.qs[h, :n], None if cache.signs is None else cache.signs[h, :n],
                              cache.tq_type)
         x = dequantize_blocks(cache.norms[h, :n], codes, sign_bits, cents)
-        out.append(x.reshape(n, -1)[:, :cache.head_dim])
+        out.append(x.reshape(n, cache.n_blocks * QK)[:, :cache.head_dim])
     return out[0] if head is not None else np.stack(out)
 
 

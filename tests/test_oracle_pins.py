@@ -545,3 +545,13 @@ def test_dequantize_cache_matches_loops():
                            atol=1e-13)
         assert np.allclose(O.dequantize_cache(vc, sv, c, 12, hk), _dequant_rows_by_loops(vc, sv, c, 12, hk),
                            atol=1e-13)
+
+
+def test_empty_key_range_gives_zero_output():
+    # kv_len = 0: nothing to attend, the output is zero (decode and prefill)
+    kc, vc, sk, sv, c = _tiny_asym_caches(34)
+    q = W.normal(34, W.S_Q, 4 * 192).reshape(4, 192)
+    assert O.dequantize_cache(kc, sk, c, 0).shape == (2, 0, 192)
+    out = O.decode(kc, vc, sk, sv, c, c, q, 0, 0.1)
+    assert out.shape == (4, 128) and not out.any()
+    assert not O.prefill(kc, vc, sk, sv, c, c, q.reshape(1, 4, 192), 0, 0.1, causal=False).any()
