@@ -625,6 +625,41 @@ def run_decode_configs(tq, torch, dev, k_src, v_src, cells_all, hbm_peak, flush)
                 tq, torch, dev, kc, vc, cbk, cbv, q, code, hbm_peak,
                 f"decode_32k turbo{t}, 8 KV x 32 Q heads, D=128, 32768 cells, {algo} kernel", l2)
         del kc, vc
+    # batched decode: 8 sequences of 32768 cells each in one launch (one new token
+    # per sequence), K/V of the decode_32k inputs in every sequence's cells
+    cbk3, cbv3 = tq.codebook(3, sk), tq.codebook(3, sv)
+    n_seq = 8
+    per_pair = n_seq * 2 * N_KV * KV_LEN * 50
+    n_sets = max(2, math.ceil(4 * l2 / per_pair))
+    sets = []
+    for _ in range(n_sets):
+        kc, vc = tq.TqCache(3, N_KV, D, n_seq * KV_LEN, dev), tq.TqCache(3, N_KV, D, n_seq * KV_LEN, dev)
+        for sq in range(n_seq):
+            cells = torch.arange(sq * KV_LEN, (sq + 1) * KV_LEN, dtype=torch.int64, device=dev)
+            tq.set_rows(kc, cbk3, k_src, cells)
+            tq.set_rows(vc, cbv3, v_src, cells)
+        sets.append((kc, vc))
+    qb = q.unsqueeze(0).repeat(n_seq, 1, 1).contiguous()
+    outb = torch.empty((n_seq, N_Q, D), device=dev)
+    offs, lens = [sq * KV_LEN for sq in range(n_seq)], [KV_LEN] * n_seq
+    wsb = tq.workspace(tq._lib.tq_fattn_decode_batch_workspace(sets[0][0].c, sets[0][1].c, N_Q, n_seq, KV_LEN), dev)
+
+    def once_b():
+        for kc, vc in sets:
+            tq.fattn_decode_batch(kc, vc, cbk3, cbv3, qb, offs, lens, 1.0 / math.sqrt(D), out=outb, ws=wsb)
+    once_b()
+    torch.cuda.synchronize()
+    gb = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gb):
+        once_b()
+    t = time_graph(torch, gb.replay, reps=20) / n_sets
+    nbytes = per_pair + 4 * n_seq * N_Q * D * 2
+    res["decode_batch8_32k"] = {"workload": "8 sequences x 32768 cells, 8 KV x 32 Q heads, D=128, turbo3, one launch",
+                                "us": t * 1e6, "tokens/s": n_seq / t, "GB/s": nbytes / t / 1e9,
+                                "frac_hbm": nbytes / t / 1e9 / hbm_peak,
+                                "l2": f"{n_sets} cache pairs x {per_pair / 1e6:.0f} MB cycled (> 4x L2)",
+                                "checksum": tq.checksum(outb)}
+    del sets
     # asym_8k: K head dim 192 (two blocks), V 128, 16 = 16 heads, 8192 cells
     gen = torch.Generator(device=dev)
     gen.manual_seed(20263)
@@ -729,6 +764,26 @@ def run_prefill_extra(tq, torch, dev, tflops_peak, flush, nqs=(3, 64, 512, 2048,
         flop = _prefill_flop(nq, L, HQ, DD, DD)
         res[f"nq{nq}"] = {"ms": t * 1e3, "TFLOP/s": flop / t / 1e12, "frac_bf16_peak": flop / t / 1e12 / tflops_peak,
                           "algorithmic_GFLOP": flop / 1e9, "tokens/s": nq / t, "checksum": tq.checksum(out)}
+    # speculative-decoding verify batches: nq new tokens over the 32K decode cache
+    # (8 KV x 32 query heads, D = 128, f32 queries), through the prefill kernel
+    sh32 = W.decode_32k()
+    sk32, sv32 = W.codebook_signs(sh32)
+    cbk32, cbv32 = tq.codebook(3, sk32), tq.codebook(3, sv32)
+    kc32, vc32 = tq.TqCache(3, 8, 128, 32768, dev), tq.TqCache(3, 8, 128, 32768, dev)
+    cells32 = torch.arange(32768, dtype=torch.int64, device=dev)
+    tq.set_rows(kc32, cbk32, _device_gaussian(torch, gen, (32768, 8, 128), dev), cells32)
+    tq.set_rows(vc32, cbv32, _device_gaussian(torch, gen, (32768, 8, 128), dev), cells32)
+    for nq in (2, 4, 6):
+        q = torch.randn((nq, 32, 128), generator=gen, device=dev)
+        out = torch.empty((nq, 32, 128), device=dev)
+        ws = tq.workspace(tq._lib.tq_fattn_prefill_workspace(kc32.c, vc32.c, nq, 32, 32768), dev)
+        t = time_flushed(torch, lambda: tq.fattn_prefill(kc32, vc32, cbk32, cbv32, q, 32768, out=out, ws=ws), flush,
+                         reps=10)
+        nbytes = 2 * 8 * 32768 * 50
+        res[f"verify_nq{nq}_32k"] = {"us": t * 1e6, "tokens/s": nq / t, "GB/s": nbytes / t / 1e9,
+                                     "workload": f"verify batch: {nq} tokens over the 32K turbo3 cache, causal",
+                                     "checksum": tq.checksum(out)}
+    del kc32, vc32
     # asym_8k prefill, nq = 512
     sha = W.asym_8k(512)
     ska, sva = W.codebook_signs(sha)

@@ -211,6 +211,37 @@ tq_status tq_fattn_decode_sparse_v(const tq_cache *k, const tq_cache *v, const t
                                    float scale, float v_threshold, int algo, float *out, void *workspace,
                                    size_t workspace_bytes, tq_stream stream);
 
+/* Bytes of workspace tq_fattn_decode_batch needs for n_seq sequences of at
+ * most max_len cells (0 if the shape is invalid: n_seq outside 1..32 or more
+ * than 256 sequence x KV head pairs).  Same alignment and zero-fill rule as
+ * the decode workspace. */
+size_t tq_fattn_decode_batch_workspace(const tq_cache *k, const tq_cache *v, int n_q_heads, int n_seq,
+                                       int64_t max_len);
+
+/* Single-query decode of several sequences in one launch ([HIP#28]
+ * "1. Graph-safe decode": decode steps of up to two query rows per sequence
+ * take the decode path; here a batch of sequences, one new token each):
+ * sequence s owns cells seq_cell0[s] .. seq_cell0[s] + seq_len[s] - 1 of the
+ * caches and
+ *   out[s][h][:] = softmax_t(scale * q[s][h] . k_t) v_t   over its cells,
+ * each (sequence, KV head) pair splitting its key range over CTAs like
+ * tq_fattn_decode.
+ * q          device f32 [n_seq][n_q_heads][k->head_dim]
+ * out        device f32 [n_seq][n_q_heads][v->head_dim]
+ * seq_cell0, seq_len  HOST int64 [n_seq]: each seq_cell0 a multiple of 64 and
+ *            seq_cell0 + seq_len rounded up to 64 within n_cells (copied into the
+ *            launch, so a captured graph keeps the values it was captured with)
+ * n_seq      1 .. 32, with n_seq * n_kv_heads <= 256.  A sequence of length 0
+ *            gets a zero output.
+ * algo       TQ_DECODE_AUTO or TQ_DECODE_MMA (the tensor-core kernel; its
+ *            supported shapes are those of tq_fattn_decode's MMA kernel).
+ * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED (LUT kernel, or a shape the
+ * tensor-core kernel does not take), TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
+tq_status tq_fattn_decode_batch(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
+                                const tq_codebook *cbv, const float *q, int n_q_heads, int n_seq,
+                                const int64_t *seq_cell0, const int64_t *seq_len, float scale, int algo,
+                                float *out, void *workspace, size_t workspace_bytes, tq_stream stream);
+
 /* tq_fattn_decode without a caller workspace, for callers that cannot
  * allocate device memory (code inside an allocator or memory-pool callback, a
  * runtime that has reserved all device memory up front, a plugin host that only

@@ -108,6 +108,23 @@ def fattn_decode_append(kc: TqCache, vc: TqCache, cbk, cbv, k_row, v_row, cell_i
     return out
 
 
+def fattn_decode_batch(kc: TqCache, vc: TqCache, cbk, cbv, q, seq_cell0, seq_len, scale: float | None = None,
+                       algo: int = TQ_DECODE_AUTO, out=None, ws=None, stream=None):
+    """Decode of several sequences in one launch: q [n_seq][n_q_heads][Dk];
+    sequence s attends cells seq_cell0[s] .. + seq_len[s] - 1 (host integers)."""
+    torch = _torch()
+    n_seq, n_q, _ = q.shape
+    scale = 1.0 / math.sqrt(kc.head_dim) if scale is None else scale
+    if out is None:
+        out = torch.empty((n_seq, n_q, vc.head_dim), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(_lib.tq_fattn_decode_batch_workspace(kc.c, vc.c, n_q, n_seq, max(seq_len)), q.device)
+    st = _lib.tq_fattn_decode_batch(kc.c, vc.c, cbk, cbv, q.data_ptr(), n_q, list(seq_cell0), list(seq_len), scale,
+                                    algo, out.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream))
+    _lib.check("tq_fattn_decode_batch", st)
+    return out
+
+
 def fattn_prefill(kc: TqCache, vc: TqCache, cbk, cbv, q, kv_len: int, scale: float | None = None,
                   causal: bool = True, out=None, ws=None, stream=None):
     torch = _torch()

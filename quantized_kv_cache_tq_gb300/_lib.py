@@ -87,6 +87,11 @@ _SIGS = {
     "tq_workspace_status": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_int32), _P]),
     "tq_noalloc_status": (C.c_int, [C.POINTER(C.c_int32), _P]),
     "tq_checksum_fnv1a64": (C.c_int, [_P, C.c_size_t, C.POINTER(C.c_uint64)]),
+    "tq_fattn_decode_batch_workspace": (C.c_size_t, [C.POINTER(tq_cache), C.POINTER(tq_cache), C.c_int, C.c_int,
+                                                     C.c_int64]),
+    "tq_fattn_decode_batch": (C.c_int, [C.POINTER(tq_cache), C.POINTER(tq_cache), C.POINTER(tq_codebook),
+                                        C.POINTER(tq_codebook), _P, C.c_int, C.c_int, C.POINTER(C.c_int64),
+                                        C.POINTER(C.c_int64), C.c_float, C.c_int, _P, _P, C.c_size_t, _P]),
     # test hook (include/tq_testing.h)
     "tq_testing_decode_drop_split": (C.c_int, [C.POINTER(tq_cache), C.POINTER(tq_cache), C.POINTER(tq_codebook),
                                                C.POINTER(tq_codebook), _P, C.c_int, C.c_int64, C.c_float, C.c_int,
@@ -226,3 +231,17 @@ def tq_checksum_fnv1a64(host_ptr: int, n_bytes: int) -> int:
     h = C.c_uint64()
     check("tq_checksum_fnv1a64", lib.tq_checksum_fnv1a64(host_ptr, n_bytes, C.byref(h)))
     return h.value
+
+
+def tq_fattn_decode_batch_workspace(k: tq_cache, v: tq_cache, n_q_heads: int, n_seq: int, max_len: int) -> int:
+    return lib.tq_fattn_decode_batch_workspace(C.byref(k), C.byref(v), n_q_heads, n_seq, max_len)
+
+
+def tq_fattn_decode_batch(k: tq_cache, v: tq_cache, cbk: tq_codebook, cbv: tq_codebook, q: int, n_q_heads: int,
+                          seq_cell0, seq_len, scale: float, algo: int, out: int, ws: int, ws_bytes: int,
+                          stream: int | None) -> int:
+    n = len(seq_cell0)
+    c0 = (C.c_int64 * n)(*[int(x) for x in seq_cell0])
+    ln = (C.c_int64 * n)(*[int(x) for x in seq_len])
+    return lib.tq_fattn_decode_batch(C.byref(k), C.byref(v), C.byref(cbk), C.byref(cbv), q, n_q_heads, n, c0, ln,
+                                     scale, algo, out, ws, ws_bytes, stream)

@@ -260,9 +260,16 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
+  // launch head hk: the KV head itself, or (batched decode) sequence hk / hkv and
+  // KV head hk % hkv, whose cells start at seq_cell0; q, out and the split
+  // bookkeeping are indexed by the launch head either way
   const int hk = blockIdx.y, split = blockIdx.x;
+  const bool batched = a.n_seq > 0;
+  const int hk_cache = batched ? hk % a.hkv : hk;
+  const int64_t cell0 = batched ? a.seq_cell0[hk / a.hkv] : 0;
+  const int64_t len = batched ? a.seq_len[hk / a.hkv] : a.kv_len;
   const int64_t t0 = static_cast<int64_t>(split) * a.chunk;
-  const int64_t t1 = min(a.kv_len, t0 + a.chunk);
+  const int64_t t1 = min(len, t0 + a.chunk);
   // this warp's key range [w0, w1): the CTA's groups of WK keys dealt out evenly
   // (warps differ by at most one group).  The warps with an extra group are the
   // first ones, so that they fall on different SM sub-partitions (warp w runs on
@@ -279,12 +286,13 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   uint32_t *pw32 = reinterpret_cast<uint32_t *>(smem + WS::PT + warp * WS::PTW);   // P' pairs [NBV][8][PSTR]
   float *qrot = reinterpret_cast<float *>(smem + WS::QR);
 
-  const uint8_t *kqs = a.kqs + static_cast<size_t>(hk) * a.n_cells * NBK * QSB;
-  const uint8_t *ksg = SGB ? a.ksg + static_cast<size_t>(hk) * a.n_cells * NBK * SGB : nullptr;
-  const uint16_t *kn = a.kn + static_cast<size_t>(hk) * a.n_cells * NBK;
-  const uint8_t *vqs = a.vqs + static_cast<size_t>(hk) * a.n_cells * NBV * QSB;
-  const uint8_t *vsg = SGB ? a.vsg + static_cast<size_t>(hk) * a.n_cells * NBV * SGB : nullptr;
-  const uint16_t *vn = a.vn + static_cast<size_t>(hk) * a.n_cells * NBV;
+  const size_t cbase = static_cast<size_t>(hk_cache) * a.n_cells + cell0;     // first cell of this head's keys
+  const uint8_t *kqs = a.kqs + cbase * NBK * QSB;
+  const uint8_t *ksg = SGB ? a.ksg + cbase * NBK * SGB : nullptr;
+  const uint16_t *kn = a.kn + cbase * NBK;
+  const uint8_t *vqs = a.vqs + cbase * NBV * QSB;
+  const uint8_t *vsg = SGB ? a.vsg + cbase * NBV * SGB : nullptr;
+  const uint16_t *vn = a.vn + cbase * NBV;
 
   // lane 0 of the warp: bring groups [jg, jg + ng) of stage si (groups SUB si .. of
   // this warp, keys w0 + SK si + 32 jg ..) into ring slot si % STAGES, completing

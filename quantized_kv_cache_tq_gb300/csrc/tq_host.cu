@@ -358,12 +358,15 @@ size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_h
 // clear_counters: zero the workspace's split counters on the stream right before
 // the decode kernel, after every argument check (the allocation-free entry point,
 // whose shared array may hold counters of an interrupted call).
+// n_seq > 0: batched decode of n_seq sequences (host arrays seq_cell0 / seq_len,
+// kv_len their longest length), tensor-core kernel only.
 static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk, const tq_codebook *cbv,
                              const void *k_row, const void *v_row, int src_type, const int64_t *cell_id,
                              const float *q, int n_q_heads, int64_t kv_len, float scale, float v_thresh,
                              int algo, float *out, void *workspace, size_t workspace_bytes, tq_stream stream,
-                             bool clear_counters = false, int drop_split = -1) {
-  tq_status st = check_decode_pair(k, v, n_q_heads, kv_len);
+                             bool clear_counters = false, int drop_split = -1, int n_seq = 0,
+                             const int64_t *seq_cell0 = nullptr, const int64_t *seq_len = nullptr) {
+  tq_status st = check_decode_pair(k, v, n_q_heads, n_seq > 0 ? 0 : kv_len);
   if (st != TQ_OK) return st;
   if (!codebook_ok(cbk, k->type) || !codebook_ok(cbv, v->type)) return TQ_ERR_INVALID_ARG;
   if (!q || !out || !aligned16(q) || !aligned16(out) || !isfinite(scale)) return TQ_ERR_INVALID_ARG;
@@ -381,6 +384,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool ws_ok = workspace && !(reinterpret_cast<uintptr_t>(workspace) & 255u);
   int32_t *status = ws_ok ? static_cast<int32_t *>(workspace) : nullptr;
+  const int n_out = (n_seq > 0 ? n_seq : 1) * n_q_heads;       // query heads of all sequences
   if (kv_len == 0) {             // nothing to attend: append only, zero output
     if (append) {
       st = tq_set_rows(k, cbk, k_row, src_type, cell_id, 1, status, stream);
@@ -388,14 +392,15 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
       st = tq_set_rows(v, cbv, v_row, src_type, cell_id, 1, status, stream);
       if (st != TQ_OK) return st;
     }
-    return map_cuda(cudaMemsetAsync(out, 0, sizeof(float) * n_q_heads * v->head_dim, s));
+    return map_cuda(cudaMemsetAsync(out, 0, sizeof(float) * n_out * v->head_dim, s));
   }
   const bool mma_ok = decode_mma_supported(k->type, v->type, group, k->n_blocks, v->n_blocks);
-  const bool lut_ok = group <= 8 && k->n_blocks <= 2 && v->n_blocks <= 2;
+  const bool lut_ok = n_seq == 0 && group <= 8 && k->n_blocks <= 2 && v->n_blocks <= 2;
   int use = algo;
   if (use == TQ_DECODE_AUTO) use = mma_ok ? TQ_DECODE_MMA : TQ_DECODE_LUT;
   if ((use == TQ_DECODE_MMA && !mma_ok) || (use == TQ_DECODE_LUT && !lut_ok)) return TQ_ERR_UNSUPPORTED;
-  const DecodeWorkspaceLayout L = decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, use);
+  const int launch_heads = (n_seq > 0 ? n_seq : 1) * k->n_kv_heads;
+  const DecodeWorkspaceLayout L = decode_layout(launch_heads, n_out, v->n_blocks, kv_len, use);
   if (!ws_ok || workspace_bytes < L.total) return TQ_ERR_WORKSPACE;
   if (append && use != TQ_DECODE_MMA) {      // the LUT kernel: SET_ROWS launches first
     st = tq_set_rows(k, cbk, k_row, src_type, cell_id, 1, status, stream);
@@ -423,7 +428,13 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.kv_len = kv_len;
   a.chunk = L.chunk;
   a.n_splits = L.n_splits;
-  a.n_kv_heads = k->n_kv_heads;
+  a.n_kv_heads = launch_heads;
+  a.hkv = k->n_kv_heads;
+  a.n_seq = n_seq;
+  for (int i = 0; i < n_seq; ++i) {
+    a.seq_cell0[i] = seq_cell0[i];
+    a.seq_len[i] = seq_len[i];
+  }
   a.group = group;
   a.dk = k->head_dim;
   a.dv = v->head_dim;
@@ -432,7 +443,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.part_stride = 128 * v->n_blocks;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.v_thresh = v_thresh;
-  a.coop = static_cast<int64_t>(L.n_splits) * k->n_kv_heads <= sm_count();
+  a.coop = static_cast<int64_t>(L.n_splits) * launch_heads <= sm_count();
   a.test_drop_split = drop_split + 1;
   a.v_log2_thresh = v_thresh > 0.f ? log2f(v_thresh) : -INFINITY;
   a.cbk = to_dev(cbk);
@@ -475,6 +486,37 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
                           size_t workspace_bytes, tq_stream stream) {
   return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, q, n_q_heads, kv_len, scale, 0.f, algo, out,
                      workspace, workspace_bytes, stream);
+}
+
+size_t tq_fattn_decode_batch_workspace(const tq_cache *k, const tq_cache *v, int n_q_heads, int n_seq,
+                                       int64_t max_len) {
+  if (check_kv_pair(k, v, n_q_heads, 0) != TQ_OK || n_seq < 1 || n_seq > kMaxDecodeSeqs || max_len < 0 ||
+      max_len > k->n_cells || static_cast<int64_t>(n_seq) * k->n_kv_heads > kMaxDecodeKvHeads)
+    return 0;
+  return decode_layout(n_seq * k->n_kv_heads, n_seq * n_q_heads, v->n_blocks, max_len, TQ_DECODE_MMA).total;
+}
+
+tq_status tq_fattn_decode_batch(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk, const tq_codebook *cbv,
+                                const float *q, int n_q_heads, int n_seq, const int64_t *seq_cell0,
+                                const int64_t *seq_len, float scale, int algo, float *out, void *workspace,
+                                size_t workspace_bytes, tq_stream stream) {
+  tq_status st = check_kv_pair(k, v, n_q_heads, 0);
+  if (st != TQ_OK) return st;
+  if (n_seq < 1 || n_seq > kMaxDecodeSeqs || !seq_cell0 || !seq_len ||
+      static_cast<int64_t>(n_seq) * k->n_kv_heads > kMaxDecodeKvHeads)
+    return TQ_ERR_INVALID_ARG;
+  if (algo == TQ_DECODE_LUT) return TQ_ERR_UNSUPPORTED;
+  int64_t max_len = 0;
+  for (int i = 0; i < n_seq; ++i) {
+    // whole 64-cell groups of each sequence lie inside the cache (the kernels
+    // copy keys in groups of 32 and 64)
+    if (seq_cell0[i] < 0 || seq_cell0[i] % 64 != 0 || seq_len[i] < 0 ||
+        seq_cell0[i] + (seq_len[i] + 63) / 64 * 64 > k->n_cells)
+      return TQ_ERR_INVALID_ARG;
+    if (seq_len[i] > max_len) max_len = seq_len[i];
+  }
+  return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, q, n_q_heads, max_len, scale, 0.f, algo, out,
+                     workspace, workspace_bytes, stream, false, -1, n_seq, seq_cell0, seq_len);
 }
 
 tq_status tq_testing_decode_drop_split(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,

@@ -9,6 +9,8 @@
 
 namespace tq {
 
+constexpr int kMaxDecodeSeqs = 32;   // sequences of one batched decode launch
+
 // Codebook as the kernels receive it (by value, in the launch parameters).
 struct DevCodebook {
   uint32_t sign_bits[4];
@@ -73,6 +75,14 @@ struct DecodeArgs {
   int32_t coop;           // the grid fits on the GPU at once: cooperative launch, merge by every CTA
   int32_t test_drop_split;  // 1 + a split whose partial is never stored (0: none); set only by
                             // tq_testing_decode_drop_split, to make the merge's bounded waits run out
+  // several sequences in one launch (tq_fattn_decode_batch; n_seq = 0 otherwise):
+  // launch head y = sequence y / hkv, KV head y % hkv; sequence s attends its
+  // seq_len[s] cells starting at cell seq_cell0[s]; q, out and the split
+  // bookkeeping are indexed by launch head (sequence-major)
+  int32_t n_seq;
+  int32_t hkv;
+  int64_t seq_cell0[kMaxDecodeSeqs];
+  int64_t seq_len[kMaxDecodeSeqs];
 };
 
 struct PrefillArgs {

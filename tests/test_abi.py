@@ -148,3 +148,13 @@ def test_fnv1a64_known_values():
     assert L.tq_checksum_fnv1a64(C.addressof(buf), 1) == 0xaf63dc4c8601ec8c
     buf = C.create_string_buffer(b"foobar", 6)
     assert L.tq_checksum_fnv1a64(C.addressof(buf), 6) == 0x85944171f73967e8
+
+
+def test_batch_decode_workspace_limits():
+    L = _lib()
+    c = L.tq_cache(3, 8, 128, 1, 1024, 1 << 20, 1 << 20, 1 << 20)
+    assert L.tq_fattn_decode_batch_workspace(c, c, 32, 32, 1024) > 0
+    assert L.tq_fattn_decode_batch_workspace(c, c, 32, 33, 1024) == 0      # more than 32 sequences
+    big = L.tq_cache(3, 16, 128, 1, 1024, 1 << 20, 1 << 20, 1 << 20)
+    assert L.tq_fattn_decode_batch_workspace(big, big, 16, 17, 64) == 0    # 272 sequence x head pairs
+    assert L.tq_fattn_decode_batch_workspace(c, c, 32, 2, 2048) == 0       # longer than the cache
