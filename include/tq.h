@@ -286,7 +286,12 @@ size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, 
  *   p_i = kv_len - nq + i when causal, else every t < kv_len.
  * q    device, q_type (TQ_BF16, TQ_F16 or TQ_F32) [nq][n_q_heads][k->head_dim]
  * out  device f32 [nq][n_q_heads][v->head_dim]
- * Requires nq <= kv_len when causal.
+ * Requires nq <= kv_len when causal.  Calls with nq <= 8 (decode steps that
+ * verify draft tokens) run on the decode kernel instead when it takes the
+ * shape ([HIP#28] "1. Graph-safe decode" sends up to two query rows down the
+ * decode path; a 128-row prefill tile would be mostly empty up to eight), each
+ * query row as one sequence of a batched decode; the workspace size returned
+ * below covers both.
  * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
 tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
                            const tq_codebook *cbv, const void *q, int q_type, int nq,

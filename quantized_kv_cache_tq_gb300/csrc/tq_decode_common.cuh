@@ -263,11 +263,16 @@ __device__ __forceinline__ void coop_merge(const DecodeArgs &a, int hk, int spli
 // loads dims 4i .. 4i+3 of the block, zero beyond dk.
 __device__ __forceinline__ void load_query_block(const DecodeArgs &a, int hk, int wb, int lane, float v[4]) {
   const int g = wb / a.nbk, b = wb % a.nbk;
-  const float *q = a.q + static_cast<size_t>(hk * a.group + g) * a.dk;
+  const size_t row = static_cast<size_t>(hk * a.group + g) * a.dk;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int d = b * QK + 4 * lane + r;
-    v[r] = (d < a.dk) ? q[d] : 0.f;
+    if (a.q_type == TQ_F32) {
+      v[r] = (d < a.dk) ? a.q[row + d] : 0.f;
+    } else {
+      const uint16_t bits = (d < a.dk) ? reinterpret_cast<const uint16_t *>(a.q)[row + d] : 0;
+      v[r] = a.q_type == TQ_BF16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
+    }
   }
 }
 

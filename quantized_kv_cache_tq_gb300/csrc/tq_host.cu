@@ -365,7 +365,8 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
                              const float *q, int n_q_heads, int64_t kv_len, float scale, float v_thresh,
                              int algo, float *out, void *workspace, size_t workspace_bytes, tq_stream stream,
                              bool clear_counters = false, int drop_split = -1, int n_seq = 0,
-                             const int64_t *seq_cell0 = nullptr, const int64_t *seq_len = nullptr) {
+                             const int64_t *seq_cell0 = nullptr, const int64_t *seq_len = nullptr,
+                             int q_type = TQ_F32) {
   tq_status st = check_decode_pair(k, v, n_q_heads, n_seq > 0 ? 0 : kv_len);
   if (st != TQ_OK) return st;
   if (!codebook_ok(cbk, k->type) || !codebook_ok(cbv, v->type)) return TQ_ERR_INVALID_ARG;
@@ -431,6 +432,7 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.n_kv_heads = launch_heads;
   a.hkv = k->n_kv_heads;
   a.n_seq = n_seq;
+  a.q_type = q_type;
   for (int i = 0; i < n_seq; ++i) {
     a.seq_cell0[i] = seq_cell0[i];
     a.seq_len[i] = seq_len[i];
@@ -546,10 +548,26 @@ tq_status tq_fattn_decode_append(const tq_cache *k, const tq_cache *v, const tq_
                      workspace, workspace_bytes, stream);
 }
 
+// Prefill calls with few query rows (decode steps of speculative verification)
+// take the decode kernel ([HIP#28] "1. Graph-safe decode" routes up to two query
+// rows to the decode path; here up to eight, where a 128-row prefill tile would
+// be mostly empty): query row i becomes one sequence of a batched decode over
+// cells 0 .. p_i of the same caches.
+constexpr int kPrefillAsDecodeMaxRows = 8;
+static bool prefill_as_decode(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads) {
+  return nq >= 1 && nq <= kPrefillAsDecodeMaxRows && static_cast<int64_t>(nq) * k->n_kv_heads <= kMaxDecodeKvHeads &&
+         decode_mma_supported(k->type, v->type, n_q_heads / k->n_kv_heads, k->n_blocks, v->n_blocks);
+}
+
 size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads,
                                   int64_t kv_len) {
   if (check_kv_pair(k, v, n_q_heads, kv_len) != TQ_OK || nq < 0) return 0;
-  return prefill_layout(nq, n_q_heads / k->n_kv_heads, k->n_kv_heads, kv_len, k->n_blocks, v->n_blocks).total;
+  size_t total = prefill_layout(nq, n_q_heads / k->n_kv_heads, k->n_kv_heads, kv_len, k->n_blocks, v->n_blocks).total;
+  if (prefill_as_decode(k, v, nq, n_q_heads)) {
+    const size_t d = decode_layout(nq * k->n_kv_heads, nq * n_q_heads, v->n_blocks, kv_len, TQ_DECODE_MMA).total;
+    if (d > total) total = d;
+  }
+  return total;
 }
 
 tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
@@ -564,6 +582,13 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   if (nq == 0) return TQ_OK;
   if (!q || !out || !aligned16(q) || !aligned16(out)) return TQ_ERR_INVALID_ARG;
   const int group = n_q_heads / k->n_kv_heads;
+  if (prefill_as_decode(k, v, nq, n_q_heads) && kv_len > 0) {
+    int64_t cell0[kPrefillAsDecodeMaxRows] = {}, len[kPrefillAsDecodeMaxRows];
+    for (int i = 0; i < nq; ++i) len[i] = causal ? kv_len - nq + 1 + i : kv_len;
+    return decode_call(k, v, cbk, cbv, nullptr, nullptr, 0, nullptr, static_cast<const float *>(q), n_q_heads,
+                       kv_len, scale, 0.f, TQ_DECODE_MMA, out, workspace, workspace_bytes, stream, false, -1, nq,
+                       cell0, len, q_type);
+  }
   if (!prefill_supported(k->type, v->type, group, k->n_blocks, v->n_blocks)) return TQ_ERR_UNSUPPORTED;
   const PrefillWorkspaceLayout L = prefill_layout(nq, group, k->n_kv_heads, kv_len, k->n_blocks, v->n_blocks);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)

@@ -81,6 +81,7 @@ struct DecodeArgs {
   // bookkeeping are indexed by launch head (sequence-major)
   int32_t n_seq;
   int32_t hkv;
+  int32_t q_type;         // TQ_F32 (0, decode's own calls), TQ_F16 or TQ_BF16: element type of q
   int64_t seq_cell0[kMaxDecodeSeqs];
   int64_t seq_len[kMaxDecodeSeqs];
 };

@@ -120,3 +120,14 @@ def test_verify_batches_at_32k_context(nq):
     out, ref = _run(sh, nq, 32768, dtype="f32")
     err, nm = compare_outputs(out, ref)
     print(f"verify nq={nq} at 32K: max-abs {err:.2e} nmse {nm:.2e}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("nq,causal", [(1, True), (2, True), (2, False), (8, True), (9, True)])
+def test_few_rows_take_the_decode_path(nq, causal, dtype):
+    # nq <= 8 runs on the decode kernel (one batched-decode sequence per query
+    # row, the causal row seeing kv_len - nq + 1 + i cells), nq = 9 on the
+    # prefill kernel; the same tolerance either way
+    sh = W.decode_32k(4096)
+    out, ref = _run(sh, nq, 3000, causal=causal, dtype=dtype, n_rows=3000)
+    compare_outputs(out, ref)
