@@ -42,6 +42,9 @@ struct Int8Args {
   int32_t nq, n_q_heads, n_kv_heads, group, causal;
   int32_t f16;            // rows are binary16 (k, v hold uint16), no scales
   float scale_log2;
+  int32_t n_split;        // key-range splits per query tile (merged by the last CTA of the tile)
+  int32_t *counters;      // [q tile][kv head] arrivals, self-resetting
+  float *part;            // split partials [q tile][kv head][split][128 rows][4 + 128]
 };
 
 namespace i8 {
@@ -145,12 +148,19 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
   __shared__ int s_fail;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hk = blockIdx.y, G = a.group;
-  const int q0 = blockIdx.x * (BM / G);
+  // grid (KV head, split, query tile): the query tiles at the end of the prompt
+  // (the longest under the causal mask) are launched first
+  const int hk = blockIdx.x, split = blockIdx.y, n_split = gridDim.y, G = a.group;
+  const int qt = gridDim.z - 1 - blockIdx.z;
+  const int q0 = qt * (BM / G);
   const int q_last = min(a.nq, q0 + BM / G) - 1;
   const int64_t pos0 = a.ctx - a.nq;
   const int64_t kv_hi = a.causal ? i64min(a.ctx, pos0 + q_last + 1) : a.ctx;
-  const int n_tiles = static_cast<int>((kv_hi + BN - 1) / BN);
+  const int tiles_all = static_cast<int>((kv_hi + BN - 1) / BN);
+  // this CTA's key tiles t_lo .. t_hi - 1 (local tile j is key tile t_lo + j)
+  const int t_lo = static_cast<int>(static_cast<long long>(tiles_all) * split / n_split);
+  const int n_tiles = static_cast<int>(static_cast<long long>(tiles_all) * (split + 1) / n_split) - t_lo;
+  const int64_t kbase = static_cast<int64_t>(t_lo) * BN;
   float *scl = reinterpret_cast<float *>(smem + SSC);
 
   if (warp == 0) tc::tmem_alloc<TMEM_COLS>(&tmem_slot);
@@ -248,11 +258,11 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
       const uint8_t *src = reinterpret_cast<const uint8_t *>(is_v ? a.v : a.k) + static_cast<int64_t>(hk) * D * 2;
       const int64_t row_stride = static_cast<int64_t>(a.n_kv_heads) * D * 2;
       auto cell_load = [&](int j) -> int64_t {
-        const int64_t t = static_cast<int64_t>(j) * BN + key;
+        const int64_t t = kbase + static_cast<int64_t>(j) * BN + key;
         return (j < n_tiles && t < kv_hi) ? static_cast<int64_t>(__ldg(a.cell_of_pos + t)) : -1;
       };
       auto fetch = [&](int j, int64_t c) {
-        const int64_t t = static_cast<int64_t>(j) * BN + key;
+        const int64_t t = kbase + static_cast<int64_t>(j) * BN + key;
         const bool okc = c >= 0 && c < a.n_cells;
         if (!okc && t < kv_hi && !is_v) set_status(a.status, TQ_ERR_DEVICE_CHECK);   // a zero row
         unsigned char *dst = smem + (is_v ? SV : SK) + (j % NB) * 16384 + (key >> 3) * 2048 + (key & 7) * 16;
@@ -306,12 +316,12 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
       // that would wait for the load): a thread never stalls on a global load.
       static_assert(RING == 4 && LOOK == 3, "register rotation below assumes a 4-deep ring");
       auto cell_load = [&](int j) -> int64_t {       // raw cell id of this thread's key in tile j, or -1
-        const int64_t t = static_cast<int64_t>(j) * BN + key;
+        const int64_t t = kbase + static_cast<int64_t>(j) * BN + key;
         return (j < n_tiles && t < kv_hi) ? static_cast<int64_t>(__ldg(a.cell_of_pos + t)) : -1;
       };
       auto cell_ok = [&](int64_t c) { return c >= 0 && c < a.n_cells; };
       auto fetch = [&](int j, int64_t c) {          // this thread's row of tile j -> ring slot j % RING
-        const int64_t t = static_cast<int64_t>(j) * BN + key;
+        const int64_t t = kbase + static_cast<int64_t>(j) * BN + key;
         const bool ok = cell_ok(c);
         if (!ok && t < kv_hi && !is_v) set_status(a.status, TQ_ERR_DEVICE_CHECK);   // a zero row
         unsigned char *dst = smem + SR + (j % RING) * RSTAGE + (is_v ? BN * D : 0) + key * D;
@@ -395,7 +405,7 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
 #pragma unroll
         for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r0[i]) * sc[2 * i];
       }
-      const int64_t key0 = static_cast<int64_t>(j) * BN;
+      const int64_t key0 = kbase + static_cast<int64_t>(j) * BN;
       const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(BN, row_end - key0))) : 0;
       const bool full_tile = __all_sync(0xffffffffu, nvis == BN);     // no mask in this warp
       if (!full_tile) {
@@ -473,24 +483,88 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
   tc::fence_after_sync();
   const bool failed = s_fail != 0;
   if (failed && tid == 0) set_status(a.status, TQ_ERR_TIMEOUT);
-  if (warp < 4 && !failed) {
-    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
-    const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-    const int h = hk * G + row % G;
-    float *orow = a.out + (static_cast<size_t>(row_ok ? row_q : 0) * a.n_q_heads + h) * D;
+  const int h = hk * G + row % G;
+  if (n_split == 1) {
+    if (warp < 4 && !failed) {
+      const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      float *orow = a.out + (static_cast<size_t>(row_ok ? row_q : 0) * a.n_q_heads + h) * D;
 #pragma unroll
-    for (int c = 0; c < D; c += 32) {
-      uint32_t r[32];
-      tc::tmem_ld32(tmem + lane_off + c, r);
-      tc::tmem_wait_ld();
-      if (row_ok) {
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + lane_off + c, r);
+        tc::tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4 *>(orow + c + i) =
+                n_tiles > 0 ? make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
+                                          __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+  } else {
+    // split key range: store (m, l, O) of every row; the last CTA of this query
+    // tile merges them with log-sum-exp weights
+    __shared__ int s_last;
+    const size_t tile_id = static_cast<size_t>(qt) * a.n_kv_heads + hk;
+    const size_t stride = 4 + D;                // m, l, 2 pad floats: O rows stay 16-byte aligned
+    if (warp < 4) {
+      const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+      float *pr = a.part + ((tile_id * n_split + split) * BM + row) * stride;
+      const bool has = !failed && n_tiles > 0;
+      pr[0] = has ? m_used : -INFINITY;
+      pr[1] = has ? l_sum : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + lane_off + c, r);
+        tc::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4 *>(orow + c + i) =
-              n_tiles > 0 ? make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
-                                        __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4 *>(pr + 4 + c + i) =
+              has ? make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                                __uint_as_float(r[i + 3]))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(&a.counters[tile_id], 1) == n_split - 1);
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      const float *base = a.part + tile_id * n_split * BM * stride;
+      float *wts = reinterpret_cast<float *>(smem + SQ);            // [BM][n_split] weights / L
+      const int rows_valid = min(BM, (a.nq - q0) * G);             // rows of queries < nq
+      if (tid < rows_valid) {
+        float M = -INFINITY;
+        for (int s2 = 0; s2 < n_split; ++s2) M = fmaxf(M, __ldcg(base + (static_cast<size_t>(s2) * BM + tid) * stride));
+        float Ls = 0.f;
+        for (int s2 = 0; s2 < n_split; ++s2) {
+          const float *p = base + (static_cast<size_t>(s2) * BM + tid) * stride;
+          const float m = __ldcg(p);
+          const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
+          wts[tid * n_split + s2] = w;
+          Ls += w * __ldcg(p + 1);
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        for (int s2 = 0; s2 < n_split; ++s2) wts[tid * n_split + s2] *= inv;
+      }
+      __syncthreads();
+      for (int i = tid; i < rows_valid * (D / 4); i += NT) {
+        const int r = i / (D / 4), d = 4 * (i % (D / 4));
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s2 = 0; s2 < n_split; ++s2) {
+          const float w = wts[r * n_split + s2];
+          const float4 x = __ldcg(reinterpret_cast<const float4 *>(base + (static_cast<size_t>(s2) * BM + r) * stride + 4 + d));
+          o.x = fmaf(w, x.x, o.x); o.y = fmaf(w, x.y, o.y); o.z = fmaf(w, x.z, o.z); o.w = fmaf(w, x.w, o.w);
+        }
+        const int qi = q0 + r / G, hh = hk * G + r % G;
+        *reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(qi) * a.n_q_heads + hh) * D + d) = o;
+      }
+      if (tid == 0) a.counters[tile_id] = 0;
     }
   }
   tc::fence_before_sync();
@@ -507,7 +581,7 @@ cudaError_t launch_int8_attn(const Int8Args &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)total);
   if (e != cudaSuccess) return e;
   const int rows = a.nq * a.group;
-  dim3 grid((rows + i8::BM - 1) / i8::BM, a.n_kv_heads);
+  dim3 grid(a.n_kv_heads, a.n_split, (rows + i8::BM - 1) / i8::BM);
   kern<<<grid, i8::NT, total, s>>>(a);
   return cudaGetLastError();
 }
@@ -516,9 +590,43 @@ cudaError_t launch_int8_attn(const Int8Args &a, cudaStream_t s) {
 
 using namespace tq;
 
+namespace tq {
+// Key-range splits per query tile: the count (1 .. 8) whose CTAs fill the last
+// wave of the GPU best (one CTA per SM), the smallest one within 1% of the best,
+// with at least 48 key tiles per split (a split's fixed costs -- Q tile, pipeline
+// fill, partial store and merge -- stay small).  Workspace: status word, then
+// (with splits) the merge counters [q tile][kv head] and the partials.
+struct Int8Layout {
+  int n_split;
+  size_t counters_off, part_off, total;
+};
+static Int8Layout int8_layout(int nq, int n_q_heads, int n_kv_heads, int64_t ctx) {
+  Int8Layout L;
+  const int64_t qt = (static_cast<int64_t>(nq) * (n_q_heads / n_kv_heads) + i8::BM - 1) / i8::BM;
+  const int64_t base = qt * n_kv_heads;
+  const int64_t tiles = (ctx + i8::BN - 1) / i8::BN;
+  const int sms = sm_count();
+  double best = 0.0;
+  double eff[9] = {0.0};
+  for (int sp = 1; sp <= 8; ++sp) {
+    if (sp > 1 && tiles / sp < 48) break;
+    const double waves = static_cast<double>(base * sp) / sms;
+    eff[sp] = waves / ceil(waves);
+    if (eff[sp] > best) best = eff[sp];
+  }
+  L.n_split = 1;
+  for (int sp = 1; sp <= 8; ++sp)
+    if (eff[sp] >= best - 0.01) { L.n_split = sp; break; }
+  L.counters_off = 256;
+  L.part_off = L.counters_off + (sizeof(int32_t) * base + 255) / 256 * 256;
+  L.total = L.n_split > 1 ? L.part_off + sizeof(float) * base * L.n_split * i8::BM * (4 + i8::D) : 256;
+  return L;
+}
+}  // namespace tq
+
 extern "C" size_t tq_int8_prompt_attn_workspace(int nq, int n_q_heads, int n_kv_heads, int head_dim, int64_t ctx) {
   if (nq < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads || head_dim != 128 || ctx < 0) return 0;
-  return 256;    // the status word
+  return int8_layout(nq, n_q_heads, n_kv_heads, ctx).total;
 }
 
 static tq_status prompt_attn_call(const void *k, const uint16_t *k_scale, const void *v, const uint16_t *v_scale,
@@ -533,13 +641,15 @@ static tq_status prompt_attn_call(const void *k, const uint16_t *k_scale, const 
   if (nq < 0 || ctx < 0 || n_cells <= 0 || (causal && nq > ctx) || !isfinite(scale)) return TQ_ERR_INVALID_ARG;
   if (nq == 0) return TQ_OK;
   if (!out || !al(out, 16) || !q || !al(q, 16)) return TQ_ERR_INVALID_ARG;
-  if (!workspace || !al(workspace, 256) || workspace_bytes < 256) return TQ_ERR_WORKSPACE;
+  const Int8Layout WL = int8_layout(nq, n_q_heads, n_kv_heads, ctx);
+  if (!workspace || !al(workspace, 256) || workspace_bytes < WL.total) return TQ_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (ctx == 0) return cudaMemsetAsync(out, 0, sizeof(float) * nq * n_q_heads * head_dim, s) == cudaSuccess
                            ? TQ_OK : TQ_ERR_CUDA;
   if (!k || !v || !al(k, 16) || !al(v, 16) || !cell_of_pos || !al(cell_of_pos, 4)) return TQ_ERR_INVALID_ARG;
   if (!f16 && (!k_scale || !v_scale || !al(k_scale, 2) || !al(v_scale, 2))) return TQ_ERR_INVALID_ARG;
   if (static_cast<int64_t>(nq) * group > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(nq) * group + i8::BM - 1) / i8::BM > 65535 || n_kv_heads > 65535) return TQ_ERR_UNSUPPORTED;
   Int8Args a;
   a.k = static_cast<const int8_t *>(k);
   a.k_scale = k_scale;
@@ -558,6 +668,9 @@ static tq_status prompt_attn_call(const void *k, const uint16_t *k_scale, const 
   a.causal = causal ? 1 : 0;
   a.f16 = f16 ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.n_split = WL.n_split;
+  a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + WL.counters_off);
+  a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + WL.part_off);
   return launch_int8_attn(a, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

@@ -57,7 +57,7 @@ def test_out_of_range_cell_reads_zero_row():
     bad[17] = 1000                                            # beyond n_cells = 100
     g = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
     f16 = lambda x: g(x.view(np.int16)).view(torch.float16)
-    ws = tq.workspace(256)
+    ws = tq.workspace(_lib.tq_int8_prompt_attn_workspace(10, 4, 2, 128, 90))
     out = tq.f16_prompt_attn(f16(kb), f16(vb), g(bad), 90, f16(qb), scale_of(128), ws=ws)
     st = _lib.tq_workspace_status(ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
     assert st == _lib.TQ_ERR_DEVICE_CHECK

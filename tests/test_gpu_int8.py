@@ -57,7 +57,7 @@ def test_out_of_range_cell_reads_zero_row():
     bad = perm.copy()
     bad[17] = 1000                                            # beyond n_cells = 100
     g = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
-    ws = tq.workspace(256)
+    ws = tq.workspace(_lib.tq_int8_prompt_attn_workspace(10, 4, 2, 128, 90))
     out = tq.int8_prompt_attn(g(ki), g(ks.view(np.int16)), g(vi), g(vs.view(np.int16)), g(bad), 90,
                               g(qb.view(np.int16)).view(torch.float16), scale_of(128), ws=ws)
     st = _lib.tq_workspace_status(ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
