@@ -492,12 +492,11 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
           const uint16_t *knp = reinterpret_cast<const uint16_t *>(st + C::K_KN) + dt * NBK;
           const uint16_t *vnp = reinterpret_cast<const uint16_t *>(st + C::K_VN) + dt * NBV;
           const bool live = static_cast<int64_t>(t_lo + j) * BN + dt < kv_hi;
-          float4 w;
-          w.x = live ? __half2float(__ushort_as_half(knp[0])) : 0.f;
-          w.y = (live && NBK > 1) ? __half2float(__ushort_as_half(knp[NBK > 1 ? 1 : 0])) : 0.f;
-          w.z = live ? __half2float(__ushort_as_half(vnp[0])) : 0.f;
-          w.w = (live && NBV > 1) ? __half2float(__ushort_as_half(vnp[NBV > 1 ? 1 : 0])) : 0.f;
-          reinterpret_cast<float4 *>(nrm)[(g & 1) * BN + dt] = w;
+          float *nb = nrm + (g & 1) * 4 * BN + dt;
+          nb[0] = live ? __half2float(__ushort_as_half(knp[0])) : 0.f;
+          nb[BN] = (live && NBK > 1) ? __half2float(__ushort_as_half(knp[NBK > 1 ? 1 : 0])) : 0.f;
+          nb[2 * BN] = live ? __half2float(__ushort_as_half(vnp[0])) : 0.f;
+          nb[3 * BN] = (live && NBV > 1) ? __half2float(__ushort_as_half(vnp[NBV > 1 ? 1 : 0])) : 0.f;
         }
         // K' (two threads per key row, half a row each) once S_{j-1} is done with it
         ok = (j == 0) || tc::mbar_wait(&bars.sf[(g - 1) & 1], ((g - 1) >> 1) & 1);
@@ -571,7 +570,7 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
         okw = __all_sync(0xffffffffu, okw);
         tc::fence_after_sync();
         const uint32_t sbuf = tmem + lane_off + C::SP0 + (g & 1) * C::SPW;
-        const float4 *nr = reinterpret_cast<const float4 *>(nrm) + (g & 1) * BN + half * HB;
+        const float *nr = nrm + (g & 1) * 4 * BN + half * HB;
         const int64_t key0 = static_cast<int64_t>(t_lo + j) * BN + half * HB;
         const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(HB, i64min(row_end, kv_hi) - key0))) : 0;
         float s[HB];
@@ -584,12 +583,18 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
             for (int c0 = 0; c0 < HB; c0 += 32) tc::tmem_ld32(sbuf + b * BN + half * HB + c0, r0 + b * HB + c0);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < HB; ++i) {
-            const float2 n2 = *reinterpret_cast<const float2 *>(nr + i);
-            float x = n2.x * __uint_as_float(r0[i]);
-            if (NBK > 1) x = fmaf(n2.y, __uint_as_float(r0[(NBK > 1 ? HB : 0) + i]), x);
-            s[i] = (i < nvis) ? x : -INFINITY;               // masked keys: weight exactly 0 below
-            mt = fmaxf(mt, s[i]);
+          for (int i4 = 0; i4 < HB; i4 += 4) {
+            const float4 k0 = *reinterpret_cast<const float4 *>(nr + i4);
+            const float4 k1 = *reinterpret_cast<const float4 *>(nr + BN + i4);
+            const float n0[4] = {k0.x, k0.y, k0.z, k0.w}, n1[4] = {k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = i4 + e;
+              float x = n0[e] * __uint_as_float(r0[i]);
+              if (NBK > 1) x = fmaf(n1[e], __uint_as_float(r0[(NBK > 1 ? HB : 0) + i]), x);
+              s[i] = (i < nvis) ? x : -INFINITY;
+              mt = fmaxf(mt, s[i]);
+            }
           }
         }
         // row maximum over both halves of the tile
@@ -642,10 +647,9 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int k0 = 2 * (c16 + i);
-              const float2 vn0 = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(nr + k0) + 2);
-              const float2 vn1 = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(nr + k0 + 1) + 2);
-              const float x0 = s[k0] * (b == 0 ? vn0.x : vn0.y);
-              const float x1 = s[k0 + 1] * (b == 0 ? vn1.x : vn1.y);
+              const float2 vv = *reinterpret_cast<const float2 *>(nr + (2 + b) * BN + k0);
+              const float x0 = s[k0] * vv.x;
+              const float x1 = s[k0 + 1] * vv.y;
               const __half2 h = __floats2half2_rn(x0, x1);
               const float2 hf = __half22float2(h);
               const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
