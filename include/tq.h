@@ -57,7 +57,13 @@ typedef enum { TQ_F32 = 0, TQ_F16 = 1, TQ_BF16 = 2 } tq_dtype;
 /* Decode kernel choice.  LUT: the pages' per-step Q x centroid shared-memory
  * table ([TQ#36] "Q x centroid LUT").  MMA: codes unpacked in registers straight
  * into tensor-core operand fragments.  AUTO picks MMA when it supports the
- * shape, else LUT.  Both compute the same attention. */
+ * shape, else LUT.  Both compute the same attention.
+ * Shapes: MMA takes K and V of one code type, any GQA group (groups other than
+ * 1, 2 and 4 run as group/4, group/2 or group launch heads per KV head, each
+ * re-reading the head's cache planes; at most 256 launch heads per call), and
+ * 1 or 2 blocks per row (K two and V one allowed).  LUT takes mixed types,
+ * groups up to 8 and 1 or 2 blocks per row; it is the only kernel for mixed
+ * K / V code types. */
 typedef enum { TQ_DECODE_AUTO = 0, TQ_DECODE_LUT = 1, TQ_DECODE_MMA = 2 } tq_decode_algo;
 
 typedef void *tq_stream; /* cudaStream_t */

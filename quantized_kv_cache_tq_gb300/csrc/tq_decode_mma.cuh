@@ -260,12 +260,13 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  // launch head hk: the KV head itself, or (batched decode) sequence hk / hkv and
-  // KV head hk % hkv, whose cells start at seq_cell0; q, out and the split
-  // bookkeeping are indexed by the launch head either way
+  // launch head hk serves query heads hk G .. hk G + G - 1 of KV head hk_cache
+  // (kv_rep launch heads per KV head when the GQA group is larger than G); in a
+  // batched decode sequence hk / hkv, whose cells start at seq_cell0.  q, out and
+  // the split bookkeeping are indexed by the launch head.
   const int hk = blockIdx.y, split = blockIdx.x;
   const bool batched = a.n_seq > 0;
-  const int hk_cache = batched ? hk % a.hkv : hk;
+  const int hk_cache = (batched ? hk % a.hkv : hk) / a.kv_rep;
   const int64_t cell0 = batched ? a.seq_cell0[hk / a.hkv] : 0;
   const int64_t len = batched ? a.seq_len[hk / a.hkv] : a.kv_len;
   const int64_t t0 = static_cast<int64_t>(split) * a.chunk;
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
 
   // ---- append ([TQ#36] SET_ROWS of the new token, fused): the CTA whose key
   // range holds the cell (split 0 when the cell lies beyond kv_len) quantises the
-  // token's K and V row blocks of head hk with warp QWARP (4 lanes per block: K
+  // token's K and V row blocks of KV head hk_cache with warp QWARP (4 lanes per block: K
   // blocks first, then V), writes them to the cache and keeps a copy in `patch`;
   // the warp that attends the cell copies it over its staged bytes once
   // `patch_bar` has completed.  Warp QWARP quantises after the prologue, while its
@@ -390,7 +391,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
         const int dim = isk ? a.dk : a.dv;
         const int nbytes = max(0, min(QK, dim - b * QK)) * es;
         const unsigned char *s0 =
-            static_cast<const unsigned char *>(isk ? a.k_src : a.v_src) + (static_cast<int64_t>(hk) * dim + b * QK) * es;
+            static_cast<const unsigned char *>(isk ? a.k_src : a.v_src) + (static_cast<int64_t>(hk_cache) * dim + b * QK) * es;
         for (int off = lane * 16; off < QK * es; off += 32 * 16) {
           const int n = min(max(nbytes - off, 0), 16);
           tc::cp_async16(rowbuf + blk * QK * 4 + off, n > 0 ? s0 + off : s0, n);
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
       const int b = isk ? gq : gq - NBK;
       const int dim = isk ? a.dk : a.dv;
       const void *src = isk ? a.k_src : a.v_src;
-      const int64_t base = static_cast<int64_t>(hk) * dim + b * QK;
+      const int64_t base = static_cast<int64_t>(hk_cache) * dim + b * QK;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int e0 = 4 * l4 + 16 * i;
@@ -449,11 +450,15 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     PackedShare<T> pb;
     quantise_block4<T>(isk ? a.cbk : a.cbv, l4, nv, pb);
     if (qblk) {
-      const int64_t blk = (static_cast<int64_t>(hk) * a.n_cells + cell) * nb + b;
-      uint16_t *gn = const_cast<uint16_t *>(isk ? a.kn : a.vn) + blk;
-      uint8_t *gqs = const_cast<uint8_t *>(isk ? a.kqs : a.vqs) + blk * QSB;
-      uint8_t *gsg = SGB ? const_cast<uint8_t *>(isk ? a.ksg : a.vsg) + blk * SGB : nullptr;
-      store_block4<T>(pb, l4, gn, gqs, gsg);
+      // every launch head of the KV head quantises the row for its own copy; the
+      // first one writes it to the cache
+      if (hk % a.kv_rep == 0) {
+        const int64_t blk = (static_cast<int64_t>(hk_cache) * a.n_cells + cell) * nb + b;
+        uint16_t *gn = const_cast<uint16_t *>(isk ? a.kn : a.vn) + blk;
+        uint8_t *gqs = const_cast<uint8_t *>(isk ? a.kqs : a.vqs) + blk * QSB;
+        uint8_t *gsg = SGB ? const_cast<uint8_t *>(isk ? a.ksg : a.vsg) + blk * SGB : nullptr;
+        store_block4<T>(pb, l4, gn, gqs, gsg);
+      }
       store_block4<T>(pb, l4, reinterpret_cast<uint16_t *>(patch + PN) + gq, patch + PQ + gq * QSB,
                       SGB ? patch + PS + gq * SGB : nullptr);
     }

@@ -347,10 +347,32 @@ static tq_status check_decode_pair(const tq_cache *k, const tq_cache *v, int n_q
   return k->n_kv_heads <= kMaxDecodeKvHeads ? TQ_OK : TQ_ERR_INVALID_ARG;
 }
 
+// Launch heads of a decode call: sequences x KV heads x, on the tensor-core
+// kernel, group / mma_group(group) launch heads per KV head.
+static int64_t decode_launch_heads(int n_kv_heads, int group, int n_seq, int algo) {
+  const int rep = (algo == TQ_DECODE_MMA) ? group / mma_group(group) : 1;
+  return static_cast<int64_t>(n_seq > 0 ? n_seq : 1) * n_kv_heads * rep;
+}
+
+// The tensor-core kernel takes the shape (and its launch heads fit the epoch words).
+static bool decode_mma_ok(const tq_cache *k, const tq_cache *v, int n_q_heads, int n_seq) {
+  const int group = n_q_heads / k->n_kv_heads;
+  return decode_mma_supported(k->type, v->type, group, k->n_blocks, v->n_blocks) &&
+         decode_launch_heads(k->n_kv_heads, group, n_seq, TQ_DECODE_MMA) <= kMaxDecodeKvHeads;
+}
+
 size_t tq_fattn_decode_workspace(const tq_cache *k, const tq_cache *v, int n_q_heads,
                                  int64_t kv_len) {
   if (check_decode_pair(k, v, n_q_heads, kv_len) != TQ_OK) return 0;
-  return decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, TQ_DECODE_AUTO).total;
+  // large enough for either kernel (their launch heads differ for GQA groups
+  // other than 1, 2 and 4)
+  size_t total = decode_layout(k->n_kv_heads, n_q_heads, v->n_blocks, kv_len, TQ_DECODE_LUT).total;
+  if (decode_mma_ok(k, v, n_q_heads, 0)) {
+    const int heads = static_cast<int>(decode_launch_heads(k->n_kv_heads, n_q_heads / k->n_kv_heads, 0, TQ_DECODE_MMA));
+    const size_t m = decode_layout(heads, n_q_heads, v->n_blocks, kv_len, TQ_DECODE_MMA).total;
+    if (m > total) total = m;
+  }
+  return total;
 }
 
 // Decode, optionally with the new token's rows appended first (k_row != null):
@@ -395,12 +417,13 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
     }
     return map_cuda(cudaMemsetAsync(out, 0, sizeof(float) * n_out * v->head_dim, s));
   }
-  const bool mma_ok = decode_mma_supported(k->type, v->type, group, k->n_blocks, v->n_blocks);
+  const bool mma_ok = decode_mma_ok(k, v, n_q_heads, n_seq);
   const bool lut_ok = n_seq == 0 && group <= 8 && k->n_blocks <= 2 && v->n_blocks <= 2;
   int use = algo;
   if (use == TQ_DECODE_AUTO) use = mma_ok ? TQ_DECODE_MMA : TQ_DECODE_LUT;
   if ((use == TQ_DECODE_MMA && !mma_ok) || (use == TQ_DECODE_LUT && !lut_ok)) return TQ_ERR_UNSUPPORTED;
-  const int launch_heads = (n_seq > 0 ? n_seq : 1) * k->n_kv_heads;
+  const int kgroup = (use == TQ_DECODE_MMA) ? mma_group(group) : group;     // query heads per launch head
+  const int launch_heads = static_cast<int>(decode_launch_heads(k->n_kv_heads, group, n_seq, use));
   const DecodeWorkspaceLayout L = decode_layout(launch_heads, n_out, v->n_blocks, kv_len, use);
   if (!ws_ok || workspace_bytes < L.total) return TQ_ERR_WORKSPACE;
   if (append && use != TQ_DECODE_MMA) {      // the LUT kernel: SET_ROWS launches first
@@ -430,14 +453,15 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
   a.chunk = L.chunk;
   a.n_splits = L.n_splits;
   a.n_kv_heads = launch_heads;
-  a.hkv = k->n_kv_heads;
+  a.kv_rep = group / kgroup;
+  a.hkv = k->n_kv_heads * a.kv_rep;          // launch heads per sequence
   a.n_seq = n_seq;
   a.q_type = q_type;
   for (int i = 0; i < n_seq; ++i) {
     a.seq_cell0[i] = seq_cell0[i];
     a.seq_len[i] = seq_len[i];
   }
-  a.group = group;
+  a.group = kgroup;
   a.dk = k->head_dim;
   a.dv = v->head_dim;
   a.nbk = k->n_blocks;
@@ -493,9 +517,11 @@ tq_status tq_fattn_decode(const tq_cache *k, const tq_cache *v, const tq_codeboo
 size_t tq_fattn_decode_batch_workspace(const tq_cache *k, const tq_cache *v, int n_q_heads, int n_seq,
                                        int64_t max_len) {
   if (check_kv_pair(k, v, n_q_heads, 0) != TQ_OK || n_seq < 1 || n_seq > kMaxDecodeSeqs || max_len < 0 ||
-      max_len > k->n_cells || static_cast<int64_t>(n_seq) * k->n_kv_heads > kMaxDecodeKvHeads)
+      max_len > k->n_cells || !decode_mma_ok(k, v, n_q_heads, n_seq))
     return 0;
-  return decode_layout(n_seq * k->n_kv_heads, n_seq * n_q_heads, v->n_blocks, max_len, TQ_DECODE_MMA).total;
+  const int heads = static_cast<int>(decode_launch_heads(k->n_kv_heads, n_q_heads / k->n_kv_heads, n_seq,
+                                                         TQ_DECODE_MMA));
+  return decode_layout(heads, n_seq * n_q_heads, v->n_blocks, max_len, TQ_DECODE_MMA).total;
 }
 
 tq_status tq_fattn_decode_batch(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk, const tq_codebook *cbv,
@@ -504,10 +530,8 @@ tq_status tq_fattn_decode_batch(const tq_cache *k, const tq_cache *v, const tq_c
                                 size_t workspace_bytes, tq_stream stream) {
   tq_status st = check_kv_pair(k, v, n_q_heads, 0);
   if (st != TQ_OK) return st;
-  if (n_seq < 1 || n_seq > kMaxDecodeSeqs || !seq_cell0 || !seq_len ||
-      static_cast<int64_t>(n_seq) * k->n_kv_heads > kMaxDecodeKvHeads)
-    return TQ_ERR_INVALID_ARG;
-  if (algo == TQ_DECODE_LUT) return TQ_ERR_UNSUPPORTED;
+  if (n_seq < 1 || n_seq > kMaxDecodeSeqs || !seq_cell0 || !seq_len) return TQ_ERR_INVALID_ARG;
+  if (algo == TQ_DECODE_LUT || !decode_mma_ok(k, v, n_q_heads, n_seq)) return TQ_ERR_UNSUPPORTED;
   int64_t max_len = 0;
   for (int i = 0; i < n_seq; ++i) {
     // whole 64-cell groups of each sequence lie inside the cache (the kernels
@@ -555,8 +579,7 @@ tq_status tq_fattn_decode_append(const tq_cache *k, const tq_cache *v, const tq_
 // cells 0 .. p_i of the same caches.
 constexpr int kPrefillAsDecodeMaxRows = 8;
 static bool prefill_as_decode(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads) {
-  return nq >= 1 && nq <= kPrefillAsDecodeMaxRows && static_cast<int64_t>(nq) * k->n_kv_heads <= kMaxDecodeKvHeads &&
-         decode_mma_supported(k->type, v->type, n_q_heads / k->n_kv_heads, k->n_blocks, v->n_blocks);
+  return nq >= 1 && nq <= kPrefillAsDecodeMaxRows && decode_mma_ok(k, v, n_q_heads, nq);
 }
 
 size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, int n_q_heads,
@@ -564,7 +587,9 @@ size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, 
   if (check_kv_pair(k, v, n_q_heads, kv_len) != TQ_OK || nq < 0) return 0;
   size_t total = prefill_layout(nq, n_q_heads / k->n_kv_heads, k->n_kv_heads, kv_len, k->n_blocks, v->n_blocks).total;
   if (prefill_as_decode(k, v, nq, n_q_heads)) {
-    const size_t d = decode_layout(nq * k->n_kv_heads, nq * n_q_heads, v->n_blocks, kv_len, TQ_DECODE_MMA).total;
+    const int heads = static_cast<int>(decode_launch_heads(k->n_kv_heads, n_q_heads / k->n_kv_heads, nq,
+                                                           TQ_DECODE_MMA));
+    const size_t d = decode_layout(heads, nq * n_q_heads, v->n_blocks, kv_len, TQ_DECODE_MMA).total;
     if (d > total) total = d;
   }
   return total;

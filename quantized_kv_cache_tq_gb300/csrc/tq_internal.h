@@ -56,7 +56,8 @@ struct DecodeArgs {
   int64_t chunk;
   int32_t n_splits;
   int32_t n_kv_heads;
-  int32_t group;          // query heads per KV head
+  int32_t group;          // query heads per launch head (tensor-core kernel: 1, 2 or 4)
+  int32_t kv_rep;         // launch heads per cache head (query heads per KV head / group)
   int32_t dk, dv;         // logical head dims
   int32_t nbk, nbv;       // 128-blocks of K / V rows
   int32_t part_stride;    // words per (head, split) partial output (128 nbv)
@@ -76,7 +77,8 @@ struct DecodeArgs {
   int32_t test_drop_split;  // 1 + a split whose partial is never stored (0: none); set only by
                             // tq_testing_decode_drop_split, to make the merge's bounded waits run out
   // several sequences in one launch (tq_fattn_decode_batch; n_seq = 0 otherwise):
-  // launch head y = sequence y / hkv, KV head y % hkv; sequence s attends its
+  // launch head y = sequence y / hkv, head y % hkv of the sequence's hkv launch
+  // heads (KV head (y % hkv) / kv_rep); sequence s attends its
   // seq_len[s] cells starting at cell seq_cell0[s]; q, out and the split
   // bookkeeping are indexed by launch head (sequence-major)
   int32_t n_seq;
@@ -139,6 +141,10 @@ DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int6
 
 cudaError_t launch_set_rows(int type, int src_type, const SetRowsArgs &a, cudaStream_t s);
 cudaError_t launch_decode_lut(int ktype, int vtype, const DecodeArgs &a, cudaStream_t s);
+// The tensor-core decode kernel serves 1, 2 or 4 query heads per launch head.
+// A GQA group of another size runs as group / mma_group(group) launch heads per
+// KV head, all of them reading that head's cache planes.
+constexpr int mma_group(int group) { return group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1); }
 bool decode_mma_supported(int ktype, int vtype, int group, int nbk, int nbv);
 cudaError_t launch_decode_mma(int ktype, int vtype, const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode_mma_t2(const DecodeArgs &a, cudaStream_t s);

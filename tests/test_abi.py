@@ -158,3 +158,19 @@ def test_batch_decode_workspace_limits():
     big = L.tq_cache(3, 16, 128, 1, 1024, 1 << 20, 1 << 20, 1 << 20)
     assert L.tq_fattn_decode_batch_workspace(big, big, 16, 17, 64) == 0    # 272 sequence x head pairs
     assert L.tq_fattn_decode_batch_workspace(c, c, 32, 2, 2048) == 0       # longer than the cache
+    # a GQA group of 8 runs as two launch heads of 4 query heads per KV head:
+    # 16 sequences x 8 KV heads x 2 = 256 launch heads fit, 17 sequences do not
+    assert L.tq_fattn_decode_batch_workspace(c, c, 64, 16, 1024) > 0
+    assert L.tq_fattn_decode_batch_workspace(c, c, 64, 17, 1024) == 0
+
+
+def test_decode_workspace_covers_both_kernels_for_large_groups():
+    # group 8 (8 KV x 64 query heads): the tensor-core kernel's 16 launch heads and
+    # the LUT kernel's 8 give different layouts; the query returns the larger
+    L = _lib()
+    c = L.tq_cache(3, 8, 128, 1, 32768, 1 << 20, 1 << 20, 1 << 20)
+    need8 = L.tq_fattn_decode_workspace(c, c, 64, 32768)
+    assert need8 > 0 and need8 % 256 == 0
+    # group 16 needs no more epochs than 256 launch heads: 16 KV heads x 4 = 64
+    c16 = L.tq_cache(3, 16, 128, 1, 4096, 1 << 20, 1 << 20, 1 << 20)
+    assert L.tq_fattn_decode_workspace(c16, c16, 256, 4096) > 0

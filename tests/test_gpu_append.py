@@ -149,3 +149,14 @@ def test_append_lut_path_issues_separate_launches():
     assert st == 0 and same
     assert np.array_equal(out_b, out_a)
     compare_outputs(out_b, ref)
+
+
+@pytest.mark.parametrize("group", [8, 3])
+def test_append_gqa_group_with_several_launch_heads(group):
+    # two (group 8) or three (group 3) launch heads per KV head each own the cell;
+    # the cache row is written once and both outputs agree bit for bit
+    sh = W.AttnShape(f"gqa{group}", 4, 4 * group, 128, 128, 3000, seed=70 + group)
+    out_b, out_a, ref, st, same = _case(sh, 3, 3, 3000, 3000, 2999)
+    assert st == 0 and same
+    assert np.array_equal(out_b, out_a)
+    compare_outputs(out_b, ref)

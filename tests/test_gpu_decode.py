@@ -214,3 +214,39 @@ def test_one_workspace_across_shapes(algo):
         ref = O.decode(kc, vc, sk, sv, O.centroids(3), O.centroids(3), q.cpu().numpy().astype(np.float64), n,
                        scale_of(128))
         compare_outputs(out.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("group", [3, 6, 8, 16])
+def test_gqa_groups_beyond_four(group, algo):
+    # GQA groups the tensor-core kernel serves as several launch heads of 1, 2 or
+    # 4 query heads per KV head (3 -> 3 x 1, 6 -> 3 x 2, 8 -> 2 x 4, 16 -> 4 x 4);
+    # the LUT kernel takes groups up to 8
+    import quantized_kv_cache_tq_gb300 as tq
+    from quantized_kv_cache_tq_gb300 import _lib
+    sh = W.AttnShape(f"gqa{group}", 4, 4 * group, 128, 128, 3000, seed=60 + group)
+    kc, vc, sk, sv = _setup(sh, 3, 3)
+    q = W.decode_query(sh)
+    if algo == "lut" and group > 8:
+        import torch
+        gk, gv = upload(kc), upload(vc)
+        cb = tq.codebook(3, sk)
+        ws = tq.workspace(_lib.tq_fattn_decode_workspace(gk.c, gv.c, sh.n_q_heads, 3000))
+        out = torch.empty(sh.n_q_heads, 128, device="cuda")
+        qg = torch.from_numpy(W.to_f32(q)).cuda()
+        assert _lib.tq_fattn_decode(gk.c, gv.c, cb, cb, qg.data_ptr(), sh.n_q_heads, 3000, 0.1, _algo(algo),
+                                    out.data_ptr(), ws.data_ptr(), ws.numel(), None) == _lib.TQ_ERR_UNSUPPORTED
+        return
+    out, ref = _decode_pair(kc, vc, sk, sv, q, 3000, algo)
+    err, nm = compare_outputs(out, ref)
+    print(f"decode GQA {group} {algo}: max-abs {err:.2e} nmse {nm:.2e}")
+
+
+def test_gqa8_32k_full():
+    # 8 KV x 64 query heads over 32768 cells: 16 launch heads of 4 query heads
+    sh = W.AttnShape("gqa8_32k", 8, 64, 128, 128, 32768, seed=69)
+    kc, vc, sk, sv = _setup(sh, 3, 3)
+    q = W.decode_query(sh)
+    out, ref = _decode_pair(kc, vc, sk, sv, q, sh.kv_len, "mma")
+    err, nm = compare_outputs(out, ref)
+    print(f"decode GQA 8 32K: max-abs {err:.2e} nmse {nm:.2e}")

@@ -67,6 +67,15 @@ def test_batch_of_eight_at_8k():
     print(f"batch 8 x 8K: last max-abs {err:.2e} nmse {nm:.2e}")
 
 
+def test_batch_gqa8():
+    # group 8: two launch heads per (sequence, KV head)
+    lens = [2000, 65, 1024]
+    offs = [0, 2048, 2176]
+    out, ref = _batch(3, 4, 32, 128, 128, lens, offs, 3200, seed=54)
+    for s in range(len(lens)):
+        compare_outputs(out[s], ref[s])
+
+
 def test_batch_rejects_bad_arguments():
     import torch
     import quantized_kv_cache_tq_gb300 as tq

@@ -131,3 +131,12 @@ def test_few_rows_take_the_decode_path(nq, causal, dtype):
     sh = W.decode_32k(4096)
     out, ref = _run(sh, nq, 3000, causal=causal, dtype=dtype, n_rows=3000)
     compare_outputs(out, ref)
+
+
+@pytest.mark.parametrize("nq", [4, 12])
+def test_gqa8_queries(nq):
+    # group 8, D = 128: 4 query rows take the decode path (two launch heads per
+    # KV head and row), 12 the prefill kernel
+    sh = W.AttnShape("gqa8_p", 2, 16, 128, 128, 700, seed=75)
+    out, ref = _run(sh, nq, 700, dtype="f32")
+    compare_outputs(out, ref)
