@@ -319,6 +319,13 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
   // The query loads go out before any bulk copy: issued after them they would
   // queue behind the key/value traffic.  One query block per warp (NW >= G * NBK).
   static_assert(NW >= G * NBK, "one query block per warp");
+  // Programmatic dependent launch: the next launch on the stream may be
+  // scheduled onto SMs that this grid's CTAs leave (it is launched with the
+  // programmatic-serialisation attribute), and every CTA waits for the previous
+  // grid to complete, its writes visible, before its first global access, so
+  // only the launch and the set-up above overlap the previous launch's merge.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   float qv[4] = {0.f, 0.f, 0.f, 0.f};
   if (warp < G * NBK) load_query_block(a, hk, warp, lane, qv);
 
@@ -759,7 +766,7 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
   cfg.blockDim = dim3(WarpStage<T, NBK, NBV>::NT);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   // one cluster per KV head, all resident together; else, when the whole grid
   // fits on the GPU at once, a cooperative launch (every CTA merges a share);
   // else the last-CTA merge
@@ -780,11 +787,17 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
+  // the kernel's first global access waits for the previous grid (see above)
+  attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs += 1;
   e = cudaLaunchKernelEx(&cfg, kern, b);
   if (e == cudaErrorCooperativeLaunchTooLarge) {          // fewer SMs available than the device has
     cudaGetLastError();
     b.coop = 0;
-    cfg.numAttrs = 0;
+    attr[0] = attr[cfg.numAttrs - 1];
+    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, b);
   }
   return e == cudaSuccess ? cudaGetLastError() : e;
