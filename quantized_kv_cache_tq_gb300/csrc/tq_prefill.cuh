@@ -213,67 +213,110 @@ __device__ __forceinline__ void expand_half(const uint8_t *qrow, const uint8_t *
   }
 }
 
-// Q'_b of rows pr = warp + NWARP (u0 + u), u < NR, of the CTA's 128 query rows:
-// q rotated per 128-dim block (signs, the page's butterflies across the warp,
-// scale * log2(e) / sqrt(128) folded in), stored as binary16 hi + lo.  The NR
-// rows' loads are all issued before any of them is used.
-template <int NBK, int NR, bool F32>
-__device__ __forceinline__ void prep_q_rows(const PrefillArgs &a, unsigned char *qsm, int u0, int warp, int lane,
-                                            int q0, int hk, int g_shift, float f) {
+// Q'_b of the CTA's query rows: q rotated per 128-dim block (the K codebook's
+// signs, then the page's butterflies; scale * log2(e) / sqrt(128) folded in),
+// stored as binary16 hi + lo in the core-matrix layout of the S mma's A operand.
+// This warp takes row-block groups gi = warp + NWARP (u0 + u), u < NG: rows
+// 8 (gi % (BM / 8)) .. + 7 of block gi / (BM / 8).  Lane 4 j + l4 holds elements
+// 16 i + 4 l4 + k (i < 8, k < 4) of the group's row j, so the butterflies
+// h = 1, 2, 16, 32, 64 stay in the lane and h = 4, 8 cross lanes, and one store
+// instruction covers 8 rows, which sit in 8 different bank groups (one row per
+// warp put all 32 lanes of a store in one 16-byte bank window).  All NG groups'
+// loads are issued before any of them is used.
+template <int NBK, int NG, bool F32>
+__device__ __forceinline__ void prep_q_groups(const PrefillArgs &a, unsigned char *qsm, int u0, int warp, int lane,
+                                              int q0, int hk, int g_shift, float f, uint32_t smask) {
   constexpr int NW = F32 ? 4 : 2;
+  constexpr int NGRP = BM * NBK / 8;
   constexpr uint32_t QBLK = 32768;
-  const int G = a.group;
-  uint32_t raw[NR][NW];
+  const int G = a.group, j = lane >> 2, l4 = lane & 3;
+  uint32_t raw[NG][8][NW];
 #pragma unroll
-  for (int u = 0; u < NR; ++u) {
-    const int pr = warp + NWARP * (u0 + u);
-    const int r = pr % BM, b = pr / BM;
+  for (int u = 0; u < NG; ++u) {
+    const int gi = warp + NWARP * (u0 + u);
+    const int pr = gi * 8 + j, r = pr % BM, b = pr / BM;
     const int qi = q0 + (r >> g_shift), h = hk * G + (r & (G - 1));
-    const int d = b * QK + 4 * lane;
 #pragma unroll
-    for (int k = 0; k < NW; ++k) raw[u][k] = 0u;
-    if (pr < BM * NBK && qi < a.nq && d + 4 <= a.dk) {
-      const size_t e = (static_cast<size_t>(qi) * a.n_q_heads + h) * a.dk + d;
-      if (F32) {
-        const uint4 x = *reinterpret_cast<const uint4 *>(static_cast<const float *>(a.q) + e);
-        raw[u][0] = x.x; raw[u][1] = x.y; raw[u][2 % NW] = x.z; raw[u][3 % NW] = x.w;
-      } else {
-        const uint2 x = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.q) + e);
-        raw[u][0] = x.x; raw[u][1] = x.y;
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int k = 0; k < NW; ++k) raw[u][i][k] = 0u;
+      const int d = b * QK + 16 * i + 4 * l4;
+      if (gi < NGRP && qi < a.nq && d + 4 <= a.dk) {
+        const size_t e = (static_cast<size_t>(qi) * a.n_q_heads + h) * a.dk + d;
+        if (F32) {
+          const uint4 x = *reinterpret_cast<const uint4 *>(static_cast<const float *>(a.q) + e);
+          raw[u][i][0] = x.x; raw[u][i][1] = x.y; raw[u][i][2 % NW] = x.z; raw[u][i][3 % NW] = x.w;
+        } else {
+          const uint2 x = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.q) + e);
+          raw[u][i][0] = x.x; raw[u][i][1] = x.y;
+        }
       }
     }
   }
 #pragma unroll
-  for (int u = 0; u < NR; ++u) {
-    const int pr = warp + NWARP * (u0 + u);
-    if (pr >= BM * NBK) break;                      // warp-uniform
-    const int r = pr % BM, b = pr / BM;
-    float v[4];
+  for (int u = 0; u < NG; ++u) {
+    const int gi = warp + NWARP * (u0 + u);
+    if (gi >= NGRP) break;                          // warp-uniform
+    const int pr = gi * 8 + j, r = pr % BM, b = pr / BM;
+    float v[8][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (F32) {
-        v[k] = __uint_as_float(raw[u][k % NW]);
-      } else {
-        const uint16_t bits = static_cast<uint16_t>(raw[u][k >> 1] >> (16 * (k & 1)));
-        v[k] = a.q_type == TQ_BF16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float x;
+        if (F32) {
+          x = __uint_as_float(raw[u][i][k % NW]);
+        } else {
+          const uint16_t bits = static_cast<uint16_t>(raw[u][i][k >> 1] >> (16 * (k & 1)));
+          x = a.q_type == TQ_BF16 ? __bfloat162float(__ushort_as_bfloat16(bits)) : __half2float(__ushort_as_half(bits));
+        }
+        v[i][k] = __uint_as_float(__float_as_uint(x) ^ ((smask << (31 - (4 * i + k))) & 0x80000000u));
       }
-    }
-    apply_signs(v, a.cbk, lane);
-    wht128_warp(v, lane);
-    const int d0 = 4 * lane;
-    uint16_t hb[4], lb[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float x = v[k] * f;
-      const __half hh = __float2half_rn(x);
-      hb[k] = __half_as_ushort(hh);
-      lb[k] = __half_as_ushort(__float2half_rn(x - __half2float(hh)));
+    for (int i = 0; i < 8; ++i) {
+      const float a0 = v[i][0] + v[i][1], a1 = v[i][0] - v[i][1];
+      const float a2 = v[i][2] + v[i][3], a3 = v[i][2] - v[i][3];
+      v[i][0] = a0 + a2; v[i][2] = a0 - a2; v[i][1] = a1 + a3; v[i][3] = a1 - a3;
     }
-    const uint32_t off = b * QBLK + ((d0 >> 3) * 16 + (r >> 3)) * 128 + (r & 7) * 16 + (d0 & 7) * 2;
-    *reinterpret_cast<uint2 *>(qsm + off) =
-        make_uint2(hb[0] | (static_cast<uint32_t>(hb[1]) << 16), hb[2] | (static_cast<uint32_t>(hb[3]) << 16));
-    *reinterpret_cast<uint2 *>(qsm + NBK * QBLK + off) =
-        make_uint2(lb[0] | (static_cast<uint32_t>(lb[1]) << 16), lb[2] | (static_cast<uint32_t>(lb[3]) << 16));
+#pragma unroll
+    for (int hb = 1; hb < 8; hb <<= 1)
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (!(i & hb))
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x = v[i][k], y = v[i | hb][k];
+            v[i][k] = x + y;
+            v[i | hb][k] = x - y;
+          }
+#pragma unroll
+    for (int m = 1; m < 4; m <<= 1) {
+      const float sg = (l4 & m) ? -1.f : 1.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float o = __shfl_xor_sync(0xffffffffu, v[i][k], m);
+          v[i][k] = fmaf(sg, v[i][k], o);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint16_t hb[4], lb[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float x = v[i][k] * f;
+        const __half hh = __float2half_rn(x);
+        hb[k] = __half_as_ushort(hh);
+        lb[k] = __half_as_ushort(__float2half_rn(x - __half2float(hh)));
+      }
+      const int dd = 16 * i + 4 * l4;
+      const uint32_t off = b * QBLK + ((dd >> 3) * 16 + (r >> 3)) * 128 + (r & 7) * 16 + (dd & 7) * 2;
+      *reinterpret_cast<uint2 *>(qsm + off) =
+          make_uint2(hb[0] | (static_cast<uint32_t>(hb[1]) << 16), hb[2] | (static_cast<uint32_t>(hb[3]) << 16));
+      *reinterpret_cast<uint2 *>(qsm + NBK * QBLK + off) =
+          make_uint2(lb[0] | (static_cast<uint32_t>(lb[1]) << 16), lb[2] | (static_cast<uint32_t>(lb[3]) << 16));
+    }
   }
 }
 
@@ -387,15 +430,21 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
       for (int i = 0; i < C::VST && i < n_tiles; ++i) issue_v(i);
     }
 
-    // ---- Q' = q rotated per block, binary16 hi + lo (every row of a warp loaded at once)
+    // ---- Q' = q rotated per block, binary16 hi + lo
     {
-      constexpr int RPW = (BM * NBK + NWARP - 1) / NWARP;          // row blocks per warp
+      constexpr int GPW = (BM * NBK / 8 + NWARP - 1) / NWARP;      // row-block groups per warp
       const float f = a.scale_log2 * kInvSqrtQK;
+      const int l4 = lane & 3;
+      uint32_t smask = 0;                                           // K-codebook signs of this lane's elements
+#pragma unroll
+      for (int i = 0; i < 8; ++i) smask |= ((a.cbk.sign_bits[i >> 1] >> (16 * (i & 1) + 4 * l4)) & 0xFu) << (4 * i);
       if (a.q_type == TQ_F32) {
-        prep_q_rows<NBK, (RPW + 1) / 2, true>(a, smem + C::Q, 0, warp, lane, q0, hk, g_shift, f);
-        prep_q_rows<NBK, RPW / 2, true>(a, smem + C::Q, (RPW + 1) / 2, warp, lane, q0, hk, g_shift, f);
+        prep_q_groups<NBK, (GPW + 1) / 2, true>(a, smem + C::Q, 0, warp, lane, q0, hk, g_shift, f, smask);
+        if (GPW / 2 > 0)
+          prep_q_groups<NBK, (GPW / 2 > 0 ? GPW / 2 : 1), true>(a, smem + C::Q, (GPW + 1) / 2, warp, lane, q0, hk,
+                                                                g_shift, f, smask);
       } else {
-        prep_q_rows<NBK, RPW, false>(a, smem + C::Q, 0, warp, lane, q0, hk, g_shift, f);
+        prep_q_groups<NBK, GPW, false>(a, smem + C::Q, 0, warp, lane, q0, hk, g_shift, f, smask);
       }
     }
     tc::fence_async_smem();
