@@ -677,7 +677,13 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
 
   // ---- per-warp results -> this warp's ring (all its copies have landed), CTA merge
   if (timed_out && lane == 0) set_status(a.status, TQ_ERR_TIMEOUT);
-  float *wbuf = reinterpret_cast<float *>(ring);                 // m[G], l[G], o[G][DVP]
+  // m[G], l[G], o[G][WHS]: output dim d of head h at 2G + h WHS + d + (d >> 5), so that
+  // the fragment stores below (dims 16g + 2mt of head c) fall on 32 different banks.
+  // With the plain layout (h 128 + d) every lane with the same parity of g hit one
+  // bank, a 16-way conflict when the warps leave their loops together (1.9 us of a
+  // 32K call).  The CTA merge reads 32 consecutive d, which share d >> 5.
+  constexpr int WHS = DVP + 36;
+  float *wbuf = reinterpret_cast<float *>(ring);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 4);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 8);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
@@ -692,7 +698,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         // columns 2c (hi part of P') and 2c + 1 (lo part) of dims 16g + 2mt, + 1
-        float *o = wbuf + 2 * G + h * DVP + b * 128 + 16 * g + 2 * mt;
+        float *o = wbuf + 2 * G + h * WHS + b * 128 + 16 * g + 2 * mt + 4 * b + (g >> 1);
         o[0] = timed_out ? 0.f : oacc[b][mt][0] + oacc[b][mt][1];
         o[1] = timed_out ? 0.f : oacc[b][mt][2] + oacc[b][mt][3];
       }
@@ -720,7 +726,7 @@ __global__ void __launch_bounds__(WarpStage<T, NBK, NBV>::NT, 1) decode_mma_kern
     for (int w = 0; w < NW; ++w) {
       const float *wb = reinterpret_cast<const float *>(smem + w * WS::RING);
       const float f = (wb[h] == -INFINITY) ? 0.f : fast_exp2(wb[h] - M);
-      o += f * wb[2 * G + h * DVP + d];
+      o += f * wb[2 * G + h * WHS + d + (d >> 5)];
       l += f * wb[G + h];
     }
     if (in_cluster) {
@@ -753,7 +759,7 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
   constexpr uint32_t bytes = smem_bytes<T, G, NBK, NBV>();
   static_assert(bytes <= 227 * 1024, "shared memory");
   // the epilogue: each warp's ring holds its results; the split merge reuses the front
-  static_assert(WarpStage<T, NBK, NBV>::RING >= 4 * (2 * G + G * 128 * NBV), "ring too small for the epilogue");
+  static_assert(WarpStage<T, NBK, NBV>::RING >= 4 * (2 * G + G * (128 * NBV + 36)), "ring too small for the epilogue");
   static_assert(WarpStage<T, NBK, NBV>::NW * WarpStage<T, NBK, NBV>::RING >= 4 * (G * 128 * NBV + 2 * G * 256),
                 "merge region");
   static_assert(WarpStage<T, NBK, NBV>::QR - WarpStage<T, NBK, NBV>::PT >= 4 * (2 * G + G * 128 * NBV),
