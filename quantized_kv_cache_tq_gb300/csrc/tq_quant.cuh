@@ -175,14 +175,15 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
   out.sg = 0;
   if constexpr (TYPE == 4) {
     // word w = 2i + l4/2, element nibble 4*(l4 & 1) + r: code = 8 s + j, j = #{t_k <= |y|}
-    // (3 bits by a three-level search over the 7 thresholds); lanes l4, l4^1 share a word
+    // (3 bits by a three-level search over the 7 thresholds); lanes l4, l4^1 share a word.
+    // The nibbles are packed with constant shifts and the word moved to its half once.
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       uint32_t x = 0;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const float y = v[i][r], ay = fabsf(y);
-        const int sh = 4 * (4 * (l4 & 1) + r);
+        const int sh = 4 * r;
         const uint32_t m2 = ge_mask(ay, thr[3]);                       // j >= 4
         const float ta = sel_f(m2, thr[5], thr[1]);
         const uint32_t m1 = ge_mask(ay, ta);                           // j & 2
@@ -191,6 +192,7 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
         const uint32_t ms = ge_mask(y, 0.f);                           // positive half
         x |= (ms & (8u << sh)) | (m2 & (4u << sh)) | (m1 & (2u << sh)) | (m0 & (1u << sh));
       }
+      x <<= 16 * (l4 & 1);
       out.w[i] = x | __shfl_xor_sync(0xffffffffu, x, 1);
     }
   } else {
