@@ -212,7 +212,7 @@ __device__ __forceinline__ bool merge_block(const DecodeArgs &a, int hk, int g, 
         arrived = false;
         break;
       }
-      __nanosleep(64);
+      __nanosleep(16);
     }
     const float ms = (lane < n) ? tagged_value(wm) : -INFINITY, ls = (lane < n) ? tagged_value(wl) : 0.f;
     const float Mn = fmaxf(M, warp_max(ms));
