@@ -105,7 +105,7 @@ DecodeWorkspaceLayout decode_layout(int n_kv_heads, int n_q_heads, int nbv, int6
 
 // Key-range splits of a prefill launch: when the query tiles x KV heads do not
 // cover the SMs, each query tile's keys are split over up to 16 CTAs (at least
-// two key tiles each) and merged by the last one.
+// two key tiles each); a second kernel merges the splits.
 PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t kv_len, int nbk, int nbv) {
   PrefillWorkspaceLayout L;
   const int64_t qt = (static_cast<int64_t>(nq) * group + 127) / 128;
@@ -118,8 +118,7 @@ PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t
   if (sp < 1) sp = 1;
   L.n_split = static_cast<int>(sp);
   L.sched_off = kWsHeader + kWsEpochBytes;         // the decode epochs stay untouched
-  L.counters_off = L.sched_off + 256;
-  L.part_off = L.counters_off + round_up(sizeof(int32_t) * qt * n_kv_heads, 256);
+  L.part_off = L.sched_off + 256;
   L.total = L.part_off;
   if (L.n_split > 1)
     L.total += round_up(sizeof(float) * qt * n_kv_heads * L.n_split * 128 * (4 + 128 * static_cast<size_t>(nbv)), 256);
@@ -648,7 +647,6 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   a.causal = causal ? 1 : 0;
   a.n_split = L.n_split;
   a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.part_off);
-  a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.counters_off);
   a.sched = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + L.sched_off);
   a.n_qt = static_cast<int32_t>((static_cast<int64_t>(nq) * group + 127) / 128);
   a.n_items = a.n_qt * k->n_kv_heads * L.n_split;
@@ -657,7 +655,9 @@ tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebo
   a.cbv = to_dev(cbv);
   code_byte_tables(cbk, k->type, a.tabk);
   code_byte_tables(cbv, v->type, a.tabv);
-  return map_cuda(launch_prefill(k->type, a, s));
+  cudaError_t e = launch_prefill(k->type, a, s);
+  if (e == cudaSuccess) e = launch_prefill_merge(a, s);       // split partials, if any
+  return map_cuda(e);
 }
 
 tq_status tq_checksum_fnv1a64(const void *host_bytes, size_t n_bytes, uint64_t *out) {

@@ -99,7 +99,6 @@ struct PrefillArgs {
   float *out;
   int32_t *status;
   float *part;            // split partials [q tile][kv head][split][128 rows][4 + 128 nbv]
-  int32_t *counters;      // [q tile][kv head], self-resetting
   int32_t *sched;         // [0] next work item, [1] CTAs done (both reset by the last CTA)
   int64_t n_cells;
   int64_t kv_len;
@@ -153,9 +152,11 @@ cudaError_t launch_decode_mma_t4(const DecodeArgs &a, cudaStream_t s);
 bool prefill_supported(int ktype, int vtype, int group, int nbk, int nbv);
 struct PrefillWorkspaceLayout {
   int n_split;
-  size_t sched_off, counters_off, part_off, total;
+  size_t sched_off, part_off, total;
 };
 PrefillWorkspaceLayout prefill_layout(int nq, int group, int n_kv_heads, int64_t kv_len, int nbk, int nbv);
+// merge of a prefill launch's key-range splits (a no-op without splits)
+cudaError_t launch_prefill_merge(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill(int ktype, const PrefillArgs &a, cudaStream_t s);
 // tq_fattn_decode that also zeroes the workspace's split counters on the stream
 // just before the kernel, once every argument has been checked.

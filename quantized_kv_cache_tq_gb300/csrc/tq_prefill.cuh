@@ -328,7 +328,6 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ int s_fail;
-  __shared__ int s_last;
   __shared__ int s_item;
   // exchange between the two softmax warps of a row (value per row, flag per warp),
   // double-buffered by the parity of the exchange count
@@ -757,7 +756,8 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
         rotate_store_rows<true>(stg, 128, a, 32 * (warp & 3), q0, hk, b, lane);
       }
     } else {
-      // split key range: store (m, l, O) of every row; the last CTA of this query tile merges
+      // split key range: store (m, l, O) of every row; a second kernel merges the splits
+      // of every query tile once this launch is done (tq_prefill_merge.cu)
       const size_t tile_id = static_cast<size_t>(qt) * a.n_kv_heads + hk;
       const size_t stride = 4 + DVP;             // m, l, 2 pad floats: O rows stay 16-byte aligned
       float *part = a.part + (tile_id * n_split + split) * BM * stride;
@@ -780,45 +780,6 @@ __global__ void __launch_bounds__(NT, 1) prefill_kernel(const PrefillArgs a) {
                                   __uint_as_float(r[i + 3]))
                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-      }
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) s_last = (atomicAdd(&a.counters[tile_id], 1) == n_split - 1);
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        const float *base = a.part + tile_id * n_split * BM * stride;
-        float *wts = reinterpret_cast<float *>(smem + C::KSTG);       // [BM][n_split] weights / L
-        float *acc = reinterpret_cast<float *>(smem + C::Q);          // [BM][DVP] merged rows
-        if (tid < min(BM, (a.nq - q0) * G)) {
-          float M = -INFINITY;
-          for (int s2 = 0; s2 < n_split; ++s2)
-            M = fmaxf(M, __ldcg(base + (static_cast<size_t>(s2) * BM + tid) * stride));
-          float L = 0.f;
-          for (int s2 = 0; s2 < n_split; ++s2) {
-            const float *p = base + (static_cast<size_t>(s2) * BM + tid) * stride;
-            const float m = __ldcg(p);
-            const float w = (m == -INFINITY) ? 0.f : exp2f(m - M);
-            wts[tid * n_split + s2] = w;
-            L += w * __ldcg(p + 1);
-          }
-          const float inv = (L > 0.f ? 1.f / L : 0.f) * kInvSqrtQK;
-          for (int s2 = 0; s2 < n_split; ++s2) wts[tid * n_split + s2] *= inv;
-        }
-        __syncthreads();
-        const int rows_valid = min(BM, (a.nq - q0) * G);          // rows of queries < nq
-        for (int i = tid; i < rows_valid * DVP; i += NT) {
-          const int r = i / DVP, d = i % DVP;
-          float o = 0.f;
-          for (int s2 = 0; s2 < n_split; ++s2)
-            o += wts[r * n_split + s2] * __ldcg(base + (static_cast<size_t>(s2) * BM + r) * stride + 4 + d);
-          acc[i] = o;
-        }
-        __syncthreads();
-        if (warp < NSM && half < NBV)           // merged rows of V block b (weights include 1/sqrt(128))
-          rotate_store_rows<false>(acc + 32 * (warp & 3) * DVP + half * 128, DVP, a, 32 * (warp & 3), q0, hk, half,
-                                   lane);
-        if (tid == 0) a.counters[tile_id] = 0;
       }
     }
     g0 += n_tiles;
@@ -847,9 +808,6 @@ cudaError_t launch_one(const PrefillArgs &a, cudaStream_t s) {
   static_assert(C::TOTAL + 4 * 2 * 2 * BM + 512 <= 227 * 1024, "shared memory (dynamic + static)");
   static_assert(C::COLS_NEEDED <= 512, "tensor memory");
   static_assert(C::BN % 64 == 0 && C::HB % 32 == 0, "key tile");
-  // the merge reuses the Q region for BM x DVP floats and the K staging ring for the weights
-  static_assert(2 * NBK * C::QBLK >= BM * C::DVP * 4, "merge buffer");
-  static_assert(C::KST * C::KSTAGE >= BM * 16 * 4, "merge weights");
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, NBK, NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::TOTAL);
   if (e != cudaSuccess) return e;
