@@ -244,8 +244,7 @@ cudaError_t launch_kt_vt(const DecodeArgs &a, cudaStream_t s) {
   size_t bytes = L.total;
   const size_t merge_need = L.lut + sizeof(float) * merge_smem_floats(a.group, a.nbv, a.n_splits);
   if (merge_need > bytes) bytes = merge_need;
-  cudaError_t e = cudaFuncSetAttribute(decode_lut_kernel<KT, VT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(decode_lut_kernel<KT, VT>), (int)bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_splits, a.n_kv_heads);

@@ -765,7 +765,7 @@ cudaError_t launch_one(const DecodeArgs &a, cudaStream_t s) {
   static_assert(WarpStage<T, NBK, NBV>::QR - WarpStage<T, NBK, NBV>::PT >= 4 * (2 * G + G * 128 * NBV),
                 "P-tile region too small for the CTA partial");
   auto kern = decode_mma_kernel<T, G, NBK, NBV, SV>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), (int)bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_splits, a.n_kv_heads);

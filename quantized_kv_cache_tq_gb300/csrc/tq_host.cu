@@ -36,6 +36,34 @@ int sm_count() {
 
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+
+// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes), once per kernel,
+// size and device (a driver call on every launch cost about 0.8 us of host time per
+// eager decode call).  The attribute lives as long as the device's primary context:
+// a process that resets the device (cudaDeviceReset) must not reuse the library.
+cudaError_t set_dynamic_smem(const void *kern, int bytes) {
+  struct Entry {
+    int dev, bytes;
+    const void *kern;
+  };
+  static std::mutex mu;
+  static Entry cache[128];
+  static int n_cache = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cache; ++i)
+      if (cache[i].dev == dev && cache[i].kern == kern && cache[i].bytes == bytes) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (n_cache < 128) cache[n_cache++] = Entry{dev, bytes, kern};
+  return cudaSuccess;
+}
+
 // Whether `kern` can run as clusters of `csize` CTAs (threads, smem each) with
 // at least `want` clusters resident at once.  Cached per device and kernel.
 bool cluster_merge_ok(const void *kern, int csize, int threads, size_t smem, int want) {

@@ -578,7 +578,7 @@ cudaError_t launch_int8_attn(const Int8Args &a, cudaStream_t s) {
   static_assert(i8::Lay<false>::TOTAL <= 227 * 1024 && i8::Lay<true>::TOTAL <= 227 * 1024, "shared memory");
   auto kern = a.f16 ? i8::prompt_attn_kernel<true> : i8::prompt_attn_kernel<false>;
   const uint32_t total = a.f16 ? i8::Lay<true>::TOTAL : i8::Lay<false>::TOTAL;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)total);
+  cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), (int)total);
   if (e != cudaSuccess) return e;
   const int rows = a.nq * a.group;
   dim3 grid(a.n_kv_heads, a.n_split, (rows + i8::BM - 1) / i8::BM);

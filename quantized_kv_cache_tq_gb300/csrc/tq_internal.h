@@ -133,6 +133,7 @@ constexpr int kMaxDecodeKvHeads = 256;
 
 int sm_count();
 bool cluster_merge_ok(const void *kern, int csize, int threads, size_t smem, int want);
+cudaError_t set_dynamic_smem(const void *kern, int bytes);
 // prmt byte tables of a codebook's binary16 code values: t[0], t[1] low bytes of
 // codes 0..3 / 4..7, t[2], t[3] high bytes (turbo4: magnitudes 0..7).
 void code_byte_tables(const tq_codebook *cb, int type, uint32_t t[4]);

@@ -808,8 +808,7 @@ cudaError_t launch_one(const PrefillArgs &a, cudaStream_t s) {
   static_assert(C::TOTAL + 4 * 2 * 2 * BM + 512 <= 227 * 1024, "shared memory (dynamic + static)");
   static_assert(C::COLS_NEEDED <= 512, "tensor memory");
   static_assert(C::BN % 64 == 0 && C::HB % 32 == 0, "key tile");
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, NBK, NBV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)C::TOTAL);
+  cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(prefill_kernel<T, NBK, NBV>), (int)C::TOTAL);
   if (e != cudaSuccess) return e;
   // persistent: at most one CTA per SM (each CTA holds most of an SM's shared memory)
   const int grid = min(a.n_items, sm_count());
