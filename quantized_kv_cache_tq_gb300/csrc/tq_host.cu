@@ -37,10 +37,13 @@ int sm_count() {
 static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 
-// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes), once per kernel,
-// size and device (a driver call on every launch cost about 0.8 us of host time per
-// eager decode call).  The attribute lives as long as the device's primary context:
-// a process that resets the device (cudaDeviceReset) must not reuse the library.
+// Raise the kernel's MaxDynamicSharedMemorySize attribute to at least `bytes`,
+// calling the driver only when the size is above what was set before on this
+// device (a driver call on every launch cost about 0.8 us of host time per eager
+// decode call).  The attribute is one value per kernel and is only ever raised,
+// so launches of any smaller size stay valid.  It lives as long as the device's
+// primary context: a process that resets the device (cudaDeviceReset) must not
+// reuse the library.
 cudaError_t set_dynamic_smem(const void *kern, int bytes) {
   struct Entry {
     int dev, bytes;
@@ -52,15 +55,18 @@ cudaError_t set_dynamic_smem(const void *kern, int bytes) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < n_cache; ++i)
-      if (cache[i].dev == dev && cache[i].kern == kern && cache[i].bytes == bytes) return cudaSuccess;
-  }
+  std::lock_guard<std::mutex> lock(mu);
+  int slot = -1;
+  for (int i = 0; i < n_cache; ++i)
+    if (cache[i].dev == dev && cache[i].kern == kern) {
+      if (cache[i].bytes >= bytes) return cudaSuccess;
+      slot = i;
+      break;
+    }
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lock(mu);
-  if (n_cache < 128) cache[n_cache++] = Entry{dev, bytes, kern};
+  if (slot >= 0) cache[slot].bytes = bytes;
+  else if (n_cache < 128) cache[n_cache++] = Entry{dev, bytes, kern};
   return cudaSuccess;
 }
 
@@ -287,7 +293,14 @@ static tq_status check_cache(const tq_cache *c) {
   return TQ_OK;
 }
 
-static tq_status map_cuda(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+// A failed launch or call leaves its error in the runtime's last-error slot, where
+// the caller's next CUDA call (or another library's launch check) would report it
+// as its own: clear it here, the status says what happened.
+static tq_status map_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return TQ_OK;
+  cudaGetLastError();
+  return TQ_ERR_CUDA;
+}
 
 }  // namespace tq
 
@@ -525,9 +538,11 @@ static tq_status decode_call(const tq_cache *k, const tq_cache *v, const tq_code
     const int es = (src_type == TQ_F32) ? 4 : 2;
     a.row_async = (k->head_dim * es) % 16 == 0 && (v->head_dim * es) % 16 == 0;
   }
-  if (clear_counters &&
-      cudaMemsetAsync(static_cast<char *>(workspace) + L.counters_off, 0, L.ml_off - L.counters_off, s) != cudaSuccess)
-    return TQ_ERR_CUDA;
+  if (clear_counters) {
+    const cudaError_t ec = cudaMemsetAsync(static_cast<char *>(workspace) + L.counters_off, 0,
+                                           L.ml_off - L.counters_off, s);
+    if (ec != cudaSuccess) return map_cuda(ec);
+  }
   cudaError_t e = (use == TQ_DECODE_MMA) ? launch_decode_mma(k->type, v->type, a, s)
                                          : launch_decode_lut(k->type, v->type, a, s);
   return map_cuda(e);
@@ -722,7 +737,7 @@ tq_status tq_workspace_status(void *workspace, size_t workspace_bytes, int32_t *
   if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess ||
       cudaMemsetAsync(workspace, 0, sizeof(v), s) != cudaSuccess)
-    return TQ_ERR_CUDA;
+    return map_cuda(cudaErrorUnknown);
   *status_out = v;
   return TQ_OK;
 }

@@ -644,8 +644,11 @@ static tq_status prompt_attn_call(const void *k, const uint16_t *k_scale, const 
   const Int8Layout WL = int8_layout(nq, n_q_heads, n_kv_heads, ctx);
   if (!workspace || !al(workspace, 256) || workspace_bytes < WL.total) return TQ_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (ctx == 0) return cudaMemsetAsync(out, 0, sizeof(float) * nq * n_q_heads * head_dim, s) == cudaSuccess
-                           ? TQ_OK : TQ_ERR_CUDA;
+  if (ctx == 0) {
+    if (cudaMemsetAsync(out, 0, sizeof(float) * nq * n_q_heads * head_dim, s) == cudaSuccess) return TQ_OK;
+    cudaGetLastError();               // the status reports it; leave no stale error behind
+    return TQ_ERR_CUDA;
+  }
   if (!k || !v || !al(k, 16) || !al(v, 16) || !cell_of_pos || !al(cell_of_pos, 4)) return TQ_ERR_INVALID_ARG;
   if (!f16 && (!k_scale || !v_scale || !al(k_scale, 2) || !al(v_scale, 2))) return TQ_ERR_INVALID_ARG;
   if (static_cast<int64_t>(nq) * group > 0x7fffffffLL) return TQ_ERR_INVALID_ARG;
@@ -671,7 +674,9 @@ static tq_status prompt_attn_call(const void *k, const uint16_t *k_scale, const 
   a.n_split = WL.n_split;
   a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + WL.counters_off);
   a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + WL.part_off);
-  return launch_int8_attn(a, s) == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  if (launch_int8_attn(a, s) == cudaSuccess) return TQ_OK;
+  cudaGetLastError();                 // the status reports it; leave no stale error behind
+  return TQ_ERR_CUDA;
 }
 
 extern "C" tq_status tq_int8_prompt_attn(const int8_t *k, const uint16_t *k_scale, const int8_t *v,

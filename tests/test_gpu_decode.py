@@ -250,3 +250,14 @@ def test_gqa8_32k_full():
     out, ref = _decode_pair(kc, vc, sk, sv, q, sh.kv_len, "mma")
     err, nm = compare_outputs(out, ref)
     print(f"decode GQA 8 32K: max-abs {err:.2e} nmse {nm:.2e}")
+
+
+def test_lut_launch_sizes_alternate():
+    # the LUT kernel's dynamic shared memory depends on the split count: calls whose
+    # sizes go large, small, large again all launch (the size attribute only grows)
+    sh = W.decode_32k()
+    kc, vc, sk, sv = _setup(sh, 3, 3, n_rows=3000)
+    q = W.decode_query(sh)
+    for n in (3000, 64, 3000, 700, 64):
+        out, ref = _decode_pair(kc, vc, sk, sv, q, n, "lut")
+        compare_outputs(out, ref)
