@@ -43,6 +43,7 @@ struct Int8Args {
   int32_t f16;            // rows are binary16 (k, v hold uint16), no scales
   float scale_log2;
   int32_t n_split;        // key-range splits per query tile (merged by the last CTA of the tile)
+  int32_t qt_fastest;     // grid order: query tiles fastest (else KV heads fastest)
   int32_t *counters;      // [q tile][kv head] arrivals, self-resetting
   float *part;            // split partials [q tile][kv head][split][128 rows][4 + 128]
 };
@@ -150,8 +151,13 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // grid (KV head, split, query tile): the query tiles at the end of the prompt
   // (the longest under the causal mask) are launched first
-  const int hk = blockIdx.x, split = blockIdx.y, n_split = gridDim.y, G = a.group;
-  const int qt = gridDim.z - 1 - blockIdx.z;
+  // launch order (longest query tiles first either way): query tiles fastest when their
+  // key counts are about equal, so that the CTAs in flight share (KV head, key range)
+  // and its rows stay in L2; else KV heads fastest, so that the shortest query tiles
+  // of every head are the last wave
+  const int hk = a.qt_fastest ? blockIdx.y : blockIdx.x;
+  const int split = a.qt_fastest ? blockIdx.z : blockIdx.y, n_split = a.n_split, G = a.group;
+  const int qt = a.qt_fastest ? gridDim.x - 1 - blockIdx.x : gridDim.z - 1 - blockIdx.z;
   const int q0 = qt * (BM / G);
   const int q_last = min(a.nq, q0 + BM / G) - 1;
   const int64_t pos0 = a.ctx - a.nq;
@@ -581,7 +587,8 @@ cudaError_t launch_int8_attn(const Int8Args &a, cudaStream_t s) {
   cudaError_t e = set_dynamic_smem(reinterpret_cast<const void *>(kern), (int)total);
   if (e != cudaSuccess) return e;
   const int rows = a.nq * a.group;
-  dim3 grid(a.n_kv_heads, a.n_split, (rows + i8::BM - 1) / i8::BM);
+  const unsigned n_qt = static_cast<unsigned>((rows + i8::BM - 1) / i8::BM);
+  const dim3 grid = a.qt_fastest ? dim3(n_qt, a.n_kv_heads, a.n_split) : dim3(a.n_kv_heads, a.n_split, n_qt);
   kern<<<grid, i8::NT, total, s>>>(a);
   return cudaGetLastError();
 }
@@ -672,6 +679,8 @@ static tq_status prompt_attn_call(const void *k, const uint16_t *k_scale, const 
   a.f16 = f16 ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_split = WL.n_split;
+  // the shortest causal query tile sees about ctx - nq + its rows of keys, the longest ctx
+  a.qt_fastest = !causal || 4 * (ctx - nq + i8::BM / group) >= 3 * ctx;
   a.counters = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + WL.counters_off);
   a.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + WL.part_off);
   if (launch_int8_attn(a, s) == cudaSuccess) return TQ_OK;
