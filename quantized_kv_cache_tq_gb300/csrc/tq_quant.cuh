@@ -84,18 +84,6 @@ __device__ __forceinline__ int sg_bit(int rr) {
   return rr < 16 ? 4 * (rr & 7) + 2 + (rr >> 3) : 4 * ((rr - 16) & 7) + ((rr - 16) >> 3);
 }
 
-// all-ones if a >= b (an unordered compare gives zero), else zero
-__device__ __forceinline__ uint32_t ge_mask(float a, float b) {
-  uint32_t m;
-  asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(a), "f"(b));
-  return m;
-}
-
-// m all-ones ? a : b, for a mask m from ge_mask
-__device__ __forceinline__ float sel_f(uint32_t m, float a, float b) {
-  return __uint_as_float((m & __float_as_uint(a)) | (~m & __float_as_uint(b)));
-}
-
 // One lane's share of a packed block: the norm (binary16 bits), qs words
 // (turbo2/3: words 2 l4 and 2 l4 + 1 in w[0], w[1]; turbo4: words 2 i + l4/2 in
 // w[i], stored by the even lanes) and, for turbo3, signs word l4.
@@ -169,8 +157,9 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
   for (int k = 0; k < HALF - 1; ++k)
     thr[k] = ss > 0.f ? 0.5f * (cb.c[HALF + k] + cb.c[HALF + k + 1]) * nrm_scale : INFINITY;
 
-  // Decisions as all-ones / zero masks (set.ge), folded into the packed words
-  // with masked ORs; |y| >= t_k against the ascending thresholds.
+  // Decisions |y| >= t_k against the ascending thresholds (and y >= 0 for the sign) as
+  // predicates, combined with predicate logic and folded into the packed words with
+  // predicated ORs: no mask or select per decision (an unordered compare is false).
   out.norm = __half_as_ushort(__float2half_rn(sqrtf(ss)));
   out.sg = 0;
   if constexpr (TYPE == 4) {
@@ -184,13 +173,16 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
       for (int r = 0; r < 4; ++r) {
         const float y = v[i][r], ay = fabsf(y);
         const int sh = 4 * r;
-        const uint32_t m2 = ge_mask(ay, thr[3]);                       // j >= 4
-        const float ta = sel_f(m2, thr[5], thr[1]);
-        const uint32_t m1 = ge_mask(ay, ta);                           // j & 2
-        const float tb = sel_f(m2, sel_f(m1, thr[6], thr[4]), sel_f(m1, thr[2], thr[0]));
-        const uint32_t m0 = ge_mask(ay, tb);                           // j & 1
-        const uint32_t ms = ge_mask(y, 0.f);                           // positive half
-        x |= (ms & (8u << sh)) | (m2 & (4u << sh)) | (m1 & (2u << sh)) | (m0 & (1u << sh));
+        // j >= 4, then j & 2 against t5 or t1, then j & 1 against t6, t4, t2 or t0; sign
+        asm("{\n .reg .pred q0, q1, q2, qs;\n .reg .f32 ta, tb, tc;\n"
+            " setp.ge.f32 q2, %1, %5;\n selp.f32 ta, %7, %3, q2;\n setp.ge.f32 q1, %1, ta;\n"
+            " selp.f32 tb, %8, %6, q1;\n selp.f32 tc, %4, %2, q1;\n selp.f32 tb, tb, tc, q2;\n"
+            " setp.ge.f32 q0, %1, tb;\n setp.ge.f32 qs, %9, 0f00000000;\n"
+            " @qs or.b32 %0, %0, %10;\n @q2 or.b32 %0, %0, %11;\n @q1 or.b32 %0, %0, %12;\n"
+            " @q0 or.b32 %0, %0, %13;\n}"
+            : "+r"(x)
+            : "f"(ay), "f"(thr[0]), "f"(thr[1]), "f"(thr[2]), "f"(thr[3]), "f"(thr[4]), "f"(thr[5]), "f"(thr[6]),
+              "f"(y), "r"(8u << sh), "r"(4u << sh), "r"(2u << sh), "r"(1u << sh));
       }
       x <<= 16 * (l4 & 1);
       out.w[i] = x | __shfl_xor_sync(0xffffffffu, x, 1);
@@ -207,15 +199,21 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
       for (int r = 0; r < 4; ++r) {
         const float y = v[i][r], ay = fabsf(y);
         const int pos = qs2_bit(4 * l4 + r);
-        const uint32_t ms = ge_mask(y, 0.f);
         if constexpr (TYPE == 3) {
-          // j = #{t0, t1, t2 <= |y|}: bit 1 = (|y| >= t1), bit 0 = odd count
-          const uint32_t m0 = ge_mask(ay, thr[0]), m1 = ge_mask(ay, thr[1]), m2 = ge_mask(ay, thr[2]);
-          x |= ((m0 ^ m1 ^ m2) & (1u << pos)) | (m1 & (2u << pos));
-          ws[i >> 1] |= ms & (1u << sg_bit(16 * (i & 1) + 4 * l4 + r));
+          // j = #{t0, t1, t2 <= |y|}: bit 1 = (|y| >= t1), bit 0 = odd count; sign: y >= 0
+          const uint32_t b0 = 1u << pos, b1 = 2u << pos, bs = 1u << sg_bit(16 * (i & 1) + 4 * l4 + r);
+          asm("{\n .reg .pred q0, q1, q2, qs, qx;\n"
+              " setp.ge.f32 q0, %2, %3;\n setp.ge.f32 q1, %2, %4;\n setp.ge.f32 q2, %2, %5;\n"
+              " setp.ge.f32 qs, %6, 0f00000000;\n xor.pred qx, q0, q1;\n xor.pred qx, qx, q2;\n"
+              " @qx or.b32 %0, %0, %7;\n @q1 or.b32 %0, %0, %8;\n @qs or.b32 %1, %1, %9;\n}"
+              : "+r"(x), "+r"(ws[i >> 1])
+              : "f"(ay), "f"(thr[0]), "f"(thr[1]), "f"(thr[2]), "f"(y), "r"(b0), "r"(b1), "r"(bs));
         } else {
-          const uint32_t m0 = ge_mask(ay, thr[0]);
-          x |= (m0 & (1u << pos)) | (ms & (2u << pos));
+          const uint32_t b0 = 1u << pos, b1 = 2u << pos;
+          asm("{\n .reg .pred q0, qs;\n setp.ge.f32 q0, %1, %2;\n setp.ge.f32 qs, %3, 0f00000000;\n"
+              " @q0 or.b32 %0, %0, %4;\n @qs or.b32 %0, %0, %5;\n}"
+              : "+r"(x)
+              : "f"(ay), "f"(thr[0]), "f"(y), "r"(b0), "r"(b1));
         }
       }
       x |= __shfl_xor_sync(0xffffffffu, x, 1);
