@@ -174,3 +174,32 @@ def test_decode_workspace_covers_both_kernels_for_large_groups():
     # group 16 needs no more epochs than 256 launch heads: 16 KV heads x 4 = 64
     c16 = L.tq_cache(3, 16, 128, 1, 4096, 1 << 20, 1 << 20, 1 << 20)
     assert L.tq_fattn_decode_workspace(c16, c16, 256, 4096) > 0
+
+
+def test_prefill_split_choice_in_workspace_size():
+    # The prefill workspace holds (m, l, O') of 128 rows per query tile and split
+    # (rows of 4 + 128 nbv floats) after a 1536-byte header.  On the 4K workload
+    # (8 KV x 16 query heads, D = 256, 4096 cells; 152 SMs) the split count minimises
+    # rounds x (key tiles per item + 6): nq = 64 -> 1 query tile x 16 splits, 200 -> 4 x 4,
+    # 512 -> 8 x 2 (one round of 128 items, not 8 x 3 in two), and the query tiles of
+    # nq >= 2048 fill the SMs and are not split.
+    L = _lib()
+    c = _fake_cache(L, h=8, d=256, n=4096)
+    tiles_x_splits = {64: 16, 200: 16, 512: 16}
+    for nq, ts in tiles_x_splits.items():
+        part = 4 * ts * 8 * 128 * (4 + 256)
+        assert L.tq_fattn_prefill_workspace(c, c, nq, 16, 4096) == 1536 + (part + 255) // 256 * 256, nq
+    for nq in (2048, 4096):
+        assert L.tq_fattn_prefill_workspace(c, c, nq, 16, 4096) == 1536
+
+
+def test_int8_split_choice_in_workspace_size():
+    # int8 prompt attention (8 KV x 32 query heads, 2048 queries): ctx 4096 has too
+    # few key tiles to split (status word only); ctx 40000 and 140000 take 5 splits,
+    # the first count within 1% of the best wave efficiency on 152 SMs.  Layout:
+    # status word, merge counters of the 64 x 8 query tiles, partials.
+    L = _lib()
+    assert L.tq_int8_prompt_attn_workspace(2048, 32, 8, 128, 4096) == 256
+    part = 4 * 512 * 5 * 128 * (4 + 128)
+    for ctx in (40000, 140000):
+        assert L.tq_int8_prompt_attn_workspace(2048, 32, 8, 128, ctx) == 256 + 4 * 512 + part
