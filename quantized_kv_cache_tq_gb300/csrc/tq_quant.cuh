@@ -84,6 +84,40 @@ __device__ __forceinline__ int sg_bit(int rr) {
   return rr < 16 ? 4 * (rr & 7) + 2 + (rr >> 3) : 4 * ((rr - 16) & 7) + ((rr - 16) >> 3);
 }
 
+// Decisions of element r of a lane's group of four (the bits of element r at 4 r, as
+// immediates): predicates |y| >= t_k and y >= 0, predicate logic, predicated ORs.
+// turbo3: bit 0 = odd count of t0, t1, t2 <= |y|, bit 1 = |y| >= t1; sign bit in xs.
+template <int R>
+__device__ __forceinline__ void decide3(float ay, float y, const float *thr, uint32_t &x, uint32_t &xs) {
+  asm("{\n .reg .pred q0, q1, q2, qs, qx;\n"
+      " setp.ge.f32 q0, %2, %3;\n setp.ge.f32 q1, %2, %4;\n setp.ge.f32 q2, %2, %5;\n"
+      " setp.ge.f32 qs, %6, 0f00000000;\n xor.pred qx, q0, q1;\n xor.pred qx, qx, q2;\n"
+      " @qx or.b32 %0, %0, %7;\n @q1 or.b32 %0, %0, %8;\n @qs or.b32 %1, %1, %7;\n}"
+      : "+r"(x), "+r"(xs)
+      : "f"(ay), "f"(thr[0]), "f"(thr[1]), "f"(thr[2]), "f"(y), "n"(1u << (4 * R)), "n"(2u << (4 * R)));
+}
+// turbo2: bit 0 = |y| >= t0, bit 1 = y >= 0
+template <int R>
+__device__ __forceinline__ void decide2(float ay, float y, const float *thr, uint32_t &x) {
+  asm("{\n .reg .pred q0, qs;\n setp.ge.f32 q0, %1, %2;\n setp.ge.f32 qs, %3, 0f00000000;\n"
+      " @q0 or.b32 %0, %0, %4;\n @qs or.b32 %0, %0, %5;\n}"
+      : "+r"(x)
+      : "f"(ay), "f"(thr[0]), "f"(y), "n"(1u << (4 * R)), "n"(2u << (4 * R)));
+}
+// turbo4: j >= 4, then j & 2 against t5 or t1, then j & 1 against t6, t4, t2 or t0; sign bit 3
+template <int R>
+__device__ __forceinline__ void decide4(float ay, float y, const float *thr, uint32_t &x) {
+  asm("{\n .reg .pred q0, q1, q2, qs;\n .reg .f32 ta, tb, tc;\n"
+      " setp.ge.f32 q2, %1, %5;\n selp.f32 ta, %7, %3, q2;\n setp.ge.f32 q1, %1, ta;\n"
+      " selp.f32 tb, %8, %6, q1;\n selp.f32 tc, %4, %2, q1;\n selp.f32 tb, tb, tc, q2;\n"
+      " setp.ge.f32 q0, %1, tb;\n setp.ge.f32 qs, %9, 0f00000000;\n"
+      " @qs or.b32 %0, %0, %10;\n @q2 or.b32 %0, %0, %11;\n @q1 or.b32 %0, %0, %12;\n"
+      " @q0 or.b32 %0, %0, %13;\n}"
+      : "+r"(x)
+      : "f"(ay), "f"(thr[0]), "f"(thr[1]), "f"(thr[2]), "f"(thr[3]), "f"(thr[4]), "f"(thr[5]), "f"(thr[6]),
+        "f"(y), "n"(8u << (4 * R)), "n"(4u << (4 * R)), "n"(2u << (4 * R)), "n"(1u << (4 * R)));
+}
+
 // One lane's share of a packed block: the norm (binary16 bits), qs words
 // (turbo2/3: words 2 l4 and 2 l4 + 1 in w[0], w[1]; turbo4: words 2 i + l4/2 in
 // w[i], stored by the even lanes) and, for turbo3, signs word l4.
@@ -169,21 +203,10 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       uint32_t x = 0;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float y = v[i][r], ay = fabsf(y);
-        const int sh = 4 * r;
-        // j >= 4, then j & 2 against t5 or t1, then j & 1 against t6, t4, t2 or t0; sign
-        asm("{\n .reg .pred q0, q1, q2, qs;\n .reg .f32 ta, tb, tc;\n"
-            " setp.ge.f32 q2, %1, %5;\n selp.f32 ta, %7, %3, q2;\n setp.ge.f32 q1, %1, ta;\n"
-            " selp.f32 tb, %8, %6, q1;\n selp.f32 tc, %4, %2, q1;\n selp.f32 tb, tb, tc, q2;\n"
-            " setp.ge.f32 q0, %1, tb;\n setp.ge.f32 qs, %9, 0f00000000;\n"
-            " @qs or.b32 %0, %0, %10;\n @q2 or.b32 %0, %0, %11;\n @q1 or.b32 %0, %0, %12;\n"
-            " @q0 or.b32 %0, %0, %13;\n}"
-            : "+r"(x)
-            : "f"(ay), "f"(thr[0]), "f"(thr[1]), "f"(thr[2]), "f"(thr[3]), "f"(thr[4]), "f"(thr[5]), "f"(thr[6]),
-              "f"(y), "r"(8u << sh), "r"(4u << sh), "r"(2u << sh), "r"(1u << sh));
-      }
+      decide4<0>(fabsf(v[i][0]), v[i][0], thr, x);
+      decide4<1>(fabsf(v[i][1]), v[i][1], thr, x);
+      decide4<2>(fabsf(v[i][2]), v[i][2], thr, x);
+      decide4<3>(fabsf(v[i][3]), v[i][3], thr, x);
       x <<= 16 * (l4 & 1);
       out.w[i] = x | __shfl_xor_sync(0xffffffffu, x, 1);
     }
@@ -192,30 +215,27 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
     // turbo3: 2-bit j in qs, sign in the signs plane; turbo2: 2-bit code 2 s + j in qs.
     uint32_t wq[8];
     uint32_t ws[4] = {0u, 0u, 0u, 0u};
+    // element 4 l4 + r of a qs word sits at bit qb + 4 r (qb = qs2_bit(4 l4)); its sign
+    // at bit sb[i & 1] + 4 r of its signs word (sb = sg_bit(16 (i & 1) + 4 l4))
+    const int qb = 16 * (l4 & 1) + 2 * (l4 >> 1);
+    const int sb0 = 2 + 16 * (l4 & 1) + (l4 >> 1), sb1 = 16 * (l4 & 1) + (l4 >> 1);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       uint32_t x = 0;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float y = v[i][r], ay = fabsf(y);
-        const int pos = qs2_bit(4 * l4 + r);
-        if constexpr (TYPE == 3) {
-          // j = #{t0, t1, t2 <= |y|}: bit 1 = (|y| >= t1), bit 0 = odd count; sign: y >= 0
-          const uint32_t b0 = 1u << pos, b1 = 2u << pos, bs = 1u << sg_bit(16 * (i & 1) + 4 * l4 + r);
-          asm("{\n .reg .pred q0, q1, q2, qs, qx;\n"
-              " setp.ge.f32 q0, %2, %3;\n setp.ge.f32 q1, %2, %4;\n setp.ge.f32 q2, %2, %5;\n"
-              " setp.ge.f32 qs, %6, 0f00000000;\n xor.pred qx, q0, q1;\n xor.pred qx, qx, q2;\n"
-              " @qx or.b32 %0, %0, %7;\n @q1 or.b32 %0, %0, %8;\n @qs or.b32 %1, %1, %9;\n}"
-              : "+r"(x), "+r"(ws[i >> 1])
-              : "f"(ay), "f"(thr[0]), "f"(thr[1]), "f"(thr[2]), "f"(y), "r"(b0), "r"(b1), "r"(bs));
-        } else {
-          const uint32_t b0 = 1u << pos, b1 = 2u << pos;
-          asm("{\n .reg .pred q0, qs;\n setp.ge.f32 q0, %1, %2;\n setp.ge.f32 qs, %3, 0f00000000;\n"
-              " @q0 or.b32 %0, %0, %4;\n @qs or.b32 %0, %0, %5;\n}"
-              : "+r"(x)
-              : "f"(ay), "f"(thr[0]), "f"(y), "r"(b0), "r"(b1));
-        }
+      if constexpr (TYPE == 3) {
+        uint32_t xs = 0;
+        decide3<0>(fabsf(v[i][0]), v[i][0], thr, x, xs);
+        decide3<1>(fabsf(v[i][1]), v[i][1], thr, x, xs);
+        decide3<2>(fabsf(v[i][2]), v[i][2], thr, x, xs);
+        decide3<3>(fabsf(v[i][3]), v[i][3], thr, x, xs);
+        ws[i >> 1] |= xs << ((i & 1) ? sb1 : sb0);
+      } else {
+        decide2<0>(fabsf(v[i][0]), v[i][0], thr, x);
+        decide2<1>(fabsf(v[i][1]), v[i][1], thr, x);
+        decide2<2>(fabsf(v[i][2]), v[i][2], thr, x);
+        decide2<3>(fabsf(v[i][3]), v[i][3], thr, x);
       }
+      x <<= qb;
       x |= __shfl_xor_sync(0xffffffffu, x, 1);
       x |= __shfl_xor_sync(0xffffffffu, x, 2);
       wq[i] = x;
