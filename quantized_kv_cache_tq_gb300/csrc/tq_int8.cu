@@ -67,7 +67,7 @@ struct Lay {
   static constexpr uint32_t SK = SQ + 32768;    // K'      NB x [key/8][d/8]      NB x 16 KB
   static constexpr uint32_t SV = SK + NB * 16384;   // V'  NB x [key/8][d/8]      NB x 16 KB
   static constexpr uint32_t SR = SV + NB * 16384;   // raw RING x [K|V][key][128 B] (int8 only)
-  static constexpr uint32_t SSC = SR + (F16 ? 0 : RING * RSTAGE);   // scales  NB x [key][k, v] floats
+  static constexpr uint32_t SSC = SR + (F16 ? 0 : RING * RSTAGE);   // scales  NB x ([BN] k, [BN] v) floats
   static constexpr uint32_t TOTAL = SSC + NB * BN * 2 * 4;
 };
 constexpr int TMEM_COLS = 512;                  // O: 128 columns, S / P': NB x 64 columns (NB <= 6)
@@ -279,8 +279,8 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
       };
       // constant scales: k * scale * log2(e), v * 1, for every buffer
       for (int i = gt; i < NB * BN; i += 128) {
-        scl[2 * i] = a.scale_log2;
-        scl[2 * i + 1] = 1.f;
+        scl[(i / BN) * 2 * BN + i % BN] = a.scale_log2;
+        scl[(i / BN) * 2 * BN + BN + i % BN] = 1.f;
       }
       int64_t cb[RING16];                         // cb[t % RING16]: cell of tile t
 #pragma unroll
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
             *reinterpret_cast<uint4 *>(dst + (2 * i + 1) * 128) = o1;      // dims 16 i + 8 .. 16 i + 15
           }
           // k scales pre-multiplied by scale * log2(e): the softmax does one multiply per score
-          scl[((j % NB) * BN + key) * 2 + (is_v ? 1 : 0)] = is_v ? sc_j : sc_j * a.scale_log2;
+          scl[(j % NB) * 2 * BN + (is_v ? BN : 0) + key] = is_v ? sc_j : sc_j * a.scale_log2;
           tc::fence_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars.cv[j % NB]);
@@ -409,7 +409,13 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
         tc::tmem_ld32(sbuf + 32, r0 + 32);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < BN; ++i) s[i] = __uint_as_float(r0[i]) * sc[2 * i];
+        for (int i4 = 0; i4 < BN; i4 += 4) {
+          const float4 k4 = *reinterpret_cast<const float4 *>(sc + i4);     // k scales of keys i4 .. i4 + 3
+          s[i4] = __uint_as_float(r0[i4]) * k4.x;
+          s[i4 + 1] = __uint_as_float(r0[i4 + 1]) * k4.y;
+          s[i4 + 2] = __uint_as_float(r0[i4 + 2]) * k4.z;
+          s[i4 + 3] = __uint_as_float(r0[i4 + 3]) * k4.w;
+        }
       }
       const int64_t key0 = kbase + static_cast<int64_t>(j) * BN;
       const int nvis = row_ok ? static_cast<int>(i64max(0, i64min(BN, row_end - key0))) : 0;
@@ -456,8 +462,9 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
           const int k0 = 32 * ch + 2 * i;
           const float p0 = tc::ex2(s[k0] - m_ref), p1 = tc::ex2(s[k0 + 1] - m_ref);     // masked: 0
           ps[i & 3] += p0 + p1;
-          const float x0 = p0 * sc[2 * k0 + 1];
-          const float x1 = p1 * sc[2 * (k0 + 1) + 1];
+          const float2 v2 = *reinterpret_cast<const float2 *>(sc + BN + k0);    // v scales of keys k0, k0 + 1
+          const float x0 = p0 * v2.x;
+          const float x1 = p1 * v2.y;
           const __half2 h = __floats2half2_rn(x0, x1);
           const float2 hf = __half22float2(h);
           const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
