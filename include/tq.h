@@ -297,7 +297,9 @@ size_t tq_fattn_prefill_workspace(const tq_cache *k, const tq_cache *v, int nq, 
  * shape ([HIP#28] "1. Graph-safe decode" sends up to two query rows down the
  * decode path; a 128-row prefill tile would be mostly empty up to eight), each
  * query row as one sequence of a batched decode; the workspace size returned
- * below covers both.
+ * below covers both.  When the query tiles do not fill the GPU, the key range
+ * of each is split; the call then issues a second kernel on `stream` that
+ * merges the splits (both are captured alike in a CUDA graph).
  * Errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_WORKSPACE, TQ_ERR_CUDA. */
 tq_status tq_fattn_prefill(const tq_cache *k, const tq_cache *v, const tq_codebook *cbk,
                            const tq_codebook *cbv, const void *q, int q_type, int nq,

@@ -3,10 +3,11 @@
 // ([HIP#28] "2. Inline-dequant TILE prefill": expand the packed cache while it
 // is loaded into on-chip tiles, never write an f16 copy of the cache).
 //
-// One CTA = one KV head x 128 query rows (128/G queries x the G query heads of
-// the GQA group, row r = query (r / G), head (r % G)) x one range of key tiles
-// (BN = 64 keys for 256-dim K rows, 128 for 128-dim rows).  Warp roles,
-// connected by mbarriers only (no CTA barrier inside the key loop):
+// Persistent CTAs (at most one per SM) take work items from an atomic queue: one
+// KV head x 128 query rows (128/G queries x the G query heads of the GQA group,
+// row r = query (r / G), head (r % G)) x one range of key tiles (BN = 64 keys for
+// 256-dim K rows, 128 for 128-dim rows).  Warp roles, connected by mbarriers
+// only (no CTA barrier inside the key loop):
 //   control warp (one thread): issues S_j = Q'K'_j^T into tensor memory as soon
 //     as K'_j is expanded, then O += P'_{j-1} V'_{j-1} once the softmax warps
 //     have written P'_{j-1} -- the tensor cores compute S_{j+1} while the
@@ -25,11 +26,11 @@
 //     memory over S_j, where the PV mma reads it as its A operand.
 // Precision: Q' and P' are split into binary16 hi + lo parts and both go
 // through the tensor cores; K'/V' are exact; accumulation is fp32.
-// Query tiles are scheduled longest first (the causal tiles near the end of the
-// prompt attend the most keys).  Few query tiles (short prompts, verify
-// batches) split the key range over several CTAs; the last CTA to finish a
-// query tile merges the partial (max, sum, O) rows (4 + 128 nbv floats each)
-// with log-sum-exp weights.
+// Work items are queued longest first (the causal tiles near the end of the
+// prompt attend the most keys).  When the query tiles do not fill the SMs, each
+// query tile's key range is split over several items; they store their
+// (max, sum, O) rows (4 + 128 nbv floats each) and a second kernel merges them
+// with log-sum-exp weights (tq_prefill_merge.cu).
 // Epilogue: o = S H (O / l) / sqrt(128) per 128-dim block (V codebook), fp32.
 //
 // Shared-memory operands (SWIZZLE_NONE core matrices of 8 rows x 16 B):
