@@ -35,6 +35,28 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Two fp32 values per instruction (the f32x2 forms of add, sub and mul on sm_100 and
+// later).  Each half is rounded to nearest exactly as the scalar operation, so a
+// packed computation gives the same bits as the scalar one; what it saves is issue
+// slots.  No multiply is fused into an add here.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n"
+      " sub.rn.f32x2 z, x, y;\n mov.b64 {%0, %1}, z;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+// max of three (one instruction on sm_100 and later; exact, like two fmaxf)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t warp_or(uint32_t v, int width) {
   for (int m = 1; m < width; m <<= 1) v |= __shfl_xor_sync(0xffffffffu, v, m);
   return v;

@@ -411,10 +411,12 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
 #pragma unroll
         for (int i4 = 0; i4 < BN; i4 += 4) {
           const float4 k4 = *reinterpret_cast<const float4 *>(sc + i4);     // k scales of keys i4 .. i4 + 3
-          s[i4] = __uint_as_float(r0[i4]) * k4.x;
-          s[i4 + 1] = __uint_as_float(r0[i4 + 1]) * k4.y;
-          s[i4 + 2] = __uint_as_float(r0[i4 + 2]) * k4.z;
-          s[i4 + 3] = __uint_as_float(r0[i4 + 3]) * k4.w;
+          const float2 a0 = mul2(make_float2(__uint_as_float(r0[i4]), __uint_as_float(r0[i4 + 1])), make_float2(k4.x, k4.y));
+          const float2 a1 = mul2(make_float2(__uint_as_float(r0[i4 + 2]), __uint_as_float(r0[i4 + 3])), make_float2(k4.z, k4.w));
+          s[i4] = a0.x;
+          s[i4 + 1] = a0.y;
+          s[i4 + 2] = a1.x;
+          s[i4 + 3] = a1.y;
         }
       }
       const int64_t key0 = kbase + static_cast<int64_t>(j) * BN;
@@ -428,7 +430,9 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
       // four independent chains for the maximum (and the sum below)
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+      for (int i = 0; i < BN; i += 8)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mx[c] = max3(mx[c], s[i + c], s[i + c + 4]);
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const bool raise = mt > m_used + 8.f || (m_used == -INFINITY && mt > -INFINITY);
       const float fct = (raise && m_used != -INFINITY) ? exp2f(m_used - mt) : 1.f;
@@ -453,6 +457,7 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
       // at a time.  Every scale of the tile is finite (0 beyond kv_hi and for
       // rejected cells); a row with nothing visible yet has m_used = -inf and p = 0.
       const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+      const float2 m_ref2 = make_float2(m_ref, m_ref);
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ch = 0; ch < BN / 32; ++ch) {
@@ -460,14 +465,14 @@ __global__ void __launch_bounds__(NT, 1) prompt_attn_kernel(const Int8Args a) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int k0 = 32 * ch + 2 * i;
-          const float p0 = tc::ex2(s[k0] - m_ref), p1 = tc::ex2(s[k0 + 1] - m_ref);     // masked: 0
+          const float2 e = sub2(make_float2(s[k0], s[k0 + 1]), m_ref2);
+          const float p0 = tc::ex2(e.x), p1 = tc::ex2(e.y);                    // masked: 0
           ps[i & 3] += p0 + p1;
           const float2 v2 = *reinterpret_cast<const float2 *>(sc + BN + k0);    // v scales of keys k0, k0 + 1
-          const float x0 = p0 * v2.x;
-          const float x1 = p1 * v2.y;
-          const __half2 h = __floats2half2_rn(x0, x1);
-          const float2 hf = __half22float2(h);
-          const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+          const float2 x = mul2(make_float2(p0, p1), v2);
+          const __half2 h = __floats2half2_rn(x.x, x.y);
+          const float2 lo = sub2(x, __half22float2(h));
+          const __half2 l = __floats2half2_rn(lo.x, lo.y);
           ph[i] = *reinterpret_cast<const uint32_t *>(&h);
           pl[i] = *reinterpret_cast<const uint32_t *>(&l);
         }

@@ -152,37 +152,57 @@ __device__ __forceinline__ void quantise_block4(const DevCodebook &cb, int l4, f
   ss += __shfl_xor_sync(0xffffffffu, ss, 1);
   ss += __shfl_xor_sync(0xffffffffu, ss, 2);
 
-  // butterflies inside the lane: h = 1, 2 (r bits) and h = 16, 32, 64 (i bits)
+  // butterflies inside the lane on pairs P[i][r] = (v[i][r], v[i + 4][r]), i < 4: the
+  // stages h = 1, 2 (r bits) and h = 16, 32 (i bits 0, 1) combine two pairs elementwise
+  // (packed f32x2), h = 64 (i bit 2) the two halves of a pair.  Each element sees the
+  // same operations in the same order as one stage at a time on scalars.
+  float2 P[4][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a0 = v[i][0] + v[i][1], a1 = v[i][0] - v[i][1];
-    const float a2 = v[i][2] + v[i][3], a3 = v[i][2] - v[i][3];
-    v[i][0] = a0 + a2; v[i][2] = a0 - a2; v[i][1] = a1 + a3; v[i][3] = a1 - a3;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) P[i][r] = make_float2(v[i][r], v[i + 4][r]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a0 = add2(P[i][0], P[i][1]), a1 = sub2(P[i][0], P[i][1]);
+    const float2 a2 = add2(P[i][2], P[i][3]), a3 = sub2(P[i][2], P[i][3]);
+    P[i][0] = add2(a0, a2); P[i][2] = sub2(a0, a2); P[i][1] = add2(a1, a3); P[i][3] = sub2(a1, a3);
   }
 #pragma unroll
-  for (int hb = 1; hb < 8; hb <<= 1)
+  for (int hb = 1; hb < 4; hb <<= 1)
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 4; ++i)
       if (!(i & hb))
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const float x = v[i][r], y = v[i | hb][r];
-          v[i][r] = x + y;
-          v[i | hb][r] = x - y;
+          const float2 x = P[i][r], y = P[i | hb][r];
+          P[i][r] = add2(x, y);
+          P[i | hb][r] = sub2(x, y);
         }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) P[i][r] = make_float2(P[i][r].x + P[i][r].y, P[i][r].x - P[i][r].y);
   // across the 4 lanes: h = 4 (lane ^ 1), h = 8 (lane ^ 2); element j takes
   // o = x[j ^ h] and becomes (j & h) ? o - x[j] : x[j] + o
 #pragma unroll
   for (int m = 1; m < 4; m <<= 1) {
     const float sg = (l4 & m) ? -1.f : 1.f;
+    const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const float o = __shfl_xor_sync(0xffffffffu, v[i][r], m);
-        v[i][r] = fmaf(sg, v[i][r], o);
+        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, P[i][r].x, m), __shfl_xor_sync(0xffffffffu, P[i][r].y, m));
+        P[i][r] = fma2(sg2, P[i][r], o);
       }
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      v[i][r] = P[i][r].x;
+      v[i + 4][r] = P[i][r].y;
+    }
 
   // thresholds between positive centroids, scaled to the unnormalised domain
   const float nrm_scale = sqrtf(ss * 128.f);

@@ -22,20 +22,34 @@ __global__ void __launch_bounds__(256) set_rows_kernel(const SetRowsArgs a) {
   bool ok = false;
   float v[8][4];
   if (active) {
-    b = static_cast<int>(blk_id % a.n_blocks);
-    const int64_t rh = blk_id / a.n_blocks;
-    h = static_cast<int>(rh % a.n_kv_heads);
-    row = rh / a.n_kv_heads;
+    if (total <= 0x7fffffff) {                 // 32-bit division when the ids fit
+      const uint32_t id = static_cast<uint32_t>(blk_id), nb = a.n_blocks, nh = a.n_kv_heads;
+      const uint32_t rh = id / nb;
+      b = static_cast<int>(id - rh * nb);
+      row = rh / nh;
+      h = static_cast<int>(rh - static_cast<uint32_t>(row) * nh);
+    } else {
+      b = static_cast<int>(blk_id % a.n_blocks);
+      const int64_t rh = blk_id / a.n_blocks;
+      h = static_cast<int>(rh % a.n_kv_heads);
+      row = rh / a.n_kv_heads;
+    }
     cell = a.cell_ids[row];
     ok = cell >= 0 && cell < a.n_cells;
     if (!ok && l4 == 0) set_status(a.dev_status, TQ_ERR_DEVICE_CHECK);
   }
   const int64_t base = (row * a.n_kv_heads + h) * a.head_dim + b * QK;
+  const int valid = a.head_dim - b * QK;       // elements of the row from this block on
+  if (ok && valid >= QK) {                     // a whole block: eight unconditional loads
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e0 = 4 * l4 + 16 * i;
-    if (ok) quant_load4<SRC>(a.src, base + e0, a.head_dim - b * QK - e0, v[i]);
-    else v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
+    for (int i = 0; i < 8; ++i) quant_load4<SRC>(a.src, base + 4 * l4 + 16 * i, 4, v[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e0 = 4 * l4 + 16 * i;
+      if (ok) quant_load4<SRC>(a.src, base + e0, valid - e0, v[i]);
+      else v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
+    }
   }
 
   // every lane takes part in the packing shuffles; only valid blocks store
