@@ -327,6 +327,11 @@ def test_sparse_v_by_hand():
     # a slack of 50 moves the cut to 0.05, still between e^-10 and e^-1
     o2, _, _ = O.sparse_v_attention(q, k, v, 1.0, 1e-3, slack=50.0)
     assert np.array_equal(o2, o_skip)
+    # a slack of 400 moves it to 0.4, above e^-1: key 2 leaves the V sum as well, and
+    # the bound takes both left-out keys (the normaliser still counts every key)
+    o3, _, b3 = O.sparse_v_attention(q, k, v, 1.0, 1e-3, slack=400.0)
+    assert np.allclose(o3[0], v[0] / w.sum(), atol=1e-15)
+    assert np.allclose(b3[0], (w[1] * np.abs(v[1]) + w[2] * np.abs(v[2])) / w.sum(), atol=1e-15)
 
 
 def test_decode_sparse_v_matches_per_head_attention():
@@ -555,3 +560,89 @@ def test_empty_key_range_gives_zero_output():
     out = O.decode(kc, vc, sk, sv, c, c, q, 0, 0.1)
     assert out.shape == (4, 128) and not out.any()
     assert not O.prefill(kc, vc, sk, sv, c, c, q.reshape(1, 4, 192), 0, 0.1, causal=False).any()
+
+
+def test_sparse_v_slack_reaches_decode_and_empty_keys():
+    # decode_sparse_v hands its slack to every head: a slack that lifts the cut above
+    # most weights changes the result exactly as the per-head call with that slack
+    shape = W.AttnShape("t", 2, 4, 128, 128, 40, seed=6)
+    c = O.centroids(3)
+    sk, sv = W.codebook_signs(shape)
+    kr, vr = W.kv_inputs(shape)
+    kc = O.empty_cache(3, 2, 128, 64)
+    vc = O.empty_cache(3, 2, 128, 64)
+    O.set_rows(kc, kr, np.arange(40), sk, c)
+    O.set_rows(vc, vr, np.arange(40), sv, c)
+    q = W.decode_query(shape) * 4
+    scale = 1 / math.sqrt(128)
+    o1, _, _ = O.decode_sparse_v(kc, vc, sk, sv, c, c, q, 40, scale, 1e-2)
+    o2, _, b2 = O.decode_sparse_v(kc, vc, sk, sv, c, c, q, 40, scale, 1e-2, slack=50.0)
+    kh = O.dequantize_cache(kc, sk, c, 40)
+    vh = O.dequantize_cache(vc, sv, c, 40)
+    for h in range(4):
+        ref, _, rb = O.sparse_v_attention(q[h:h + 1], kh[h // 2], vh[h // 2], scale, 1e-2, slack=50.0)
+        assert np.allclose(o2[h], ref[0], atol=1e-14) and np.allclose(b2[h], rb[0], atol=1e-14)
+    assert not np.allclose(o1, o2)                        # the cut at 0.5 leaves more keys out
+    # no keys: zero output and zero bound
+    z = O.sparse_v_attention(q[:1], np.zeros((0, 128)), np.zeros((0, 128)), scale, 1e-3)
+    assert all(x.shape == (1, 128) and not x.any() for x in z)
+
+
+def test_lse_partial_pieces():
+    # (m, l, o) of a key range: m the maximum score, l = sum exp(s - m), o the
+    # softmax-weighted values of that range alone
+    q = W.normal(12, 1, 3 * 16).reshape(3, 16)
+    k = W.normal(12, 2, 30 * 16).reshape(30, 16)
+    v = W.normal(12, 3, 30 * 8).reshape(30, 8)
+    m, l, o = O.lse_partial(q, k, v, 0.3)
+    s = 0.3 * (q @ k.T)
+    assert np.array_equal(m, s.max(axis=1))
+    assert np.allclose(l, np.exp(s - s.max(axis=1, keepdims=True)).sum(axis=1), rtol=1e-15)
+    assert np.allclose(o, O.softmax_attention(q, k, v, 0.3), atol=1e-14)
+
+
+def test_set_rows_keeps_f64_inputs_exact():
+    # the rotated values set_rows reports are R x / |x| of the f64 rows as given (no
+    # rounding of the source to a narrower type on the way)
+    c = O.centroids(3)
+    sb = W.sign_bits(3, W.S_SIGNS_K)
+    src = W.normal(3, 4, 3 * 2 * 128).reshape(3, 2, 128) * (1 + 2.0 ** -40)
+    cache = O.empty_cache(3, 2, 128, 8)
+    y = O.set_rows(cache, src, np.array([5, 1, 6]), sb, c)
+    ref = src @ O.rotation(sb).T / np.linalg.norm(src, axis=-1, keepdims=True)
+    assert np.allclose(y[:, :, 0], ref, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("mode", ["int8", "f16", "prefill"])
+def test_rows_subset_is_the_full_rows_and_zero_elsewhere(mode):
+    # the rows= argument of the multi-query functions: the chosen rows equal the
+    # full computation, every other row is zero
+    nq, hq, d = 5, 4, 128
+    rows = np.array([1, 4])
+    q = W.normal(13, W.S_Q, nq * hq * d).reshape(nq, hq, d)
+    if mode == "prefill":
+        shape = W.AttnShape("t", 2, hq, d, d, 24, seed=13)
+        c = O.centroids(3)
+        sk, sv = W.codebook_signs(shape)
+        kr, vr = W.kv_inputs(shape)
+        kc = O.empty_cache(3, 2, d, 32)
+        vc = O.empty_cache(3, 2, d, 32)
+        O.set_rows(kc, kr, np.arange(24), sk, c)
+        O.set_rows(vc, vr, np.arange(24), sv, c)
+        run = lambda r: O.prefill(kc, vc, sk, sv, c, c, q, 24, 0.1, causal=True, rows=r)
+    else:
+        n_cells = 24
+        raw = W.gaussian_with_outliers(13, W.S_K, W.S_K_OUT, n_cells, 2, d)
+        rawv = W.gaussian_with_outliers(13, W.S_V, W.S_V_OUT, n_cells, 2, d)
+        perm = W.permutation(13, W.S_PERM, n_cells)
+        if mode == "int8":
+            ki, ks = W.int8_rows(raw)
+            vi, vs = W.int8_rows(rawv)
+            run = lambda r: O.int8_prompt_attn(ki, ks, vi, vs, perm, 20, q, 0.1, causal=True, rows=r)
+        else:
+            kb, vb = W.to_f16_bits(raw), W.to_f16_bits(rawv)
+            run = lambda r: O.f16_prompt_attn(kb, vb, perm, 20, q, 0.1, causal=True, rows=r)
+    full, sub = run(None), run(rows)
+    assert np.array_equal(sub[rows], full[rows])
+    others = np.setdiff1d(np.arange(nq), rows)
+    assert not sub[others].any() and full[others].any()
