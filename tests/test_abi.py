@@ -219,3 +219,68 @@ def test_int8_split_choice_in_workspace_size():
     part = 4 * 512 * 5 * 128 * (4 + 128)
     for ctx in (40000, 140000):
         assert L.tq_int8_prompt_attn_workspace(2048, 32, 8, 128, ctx) == 256 + 4 * 512 + part
+
+
+def test_set_rows_prefill_and_prompt_attention_checks_reject_before_launch():
+    # more host checks: each call below returns before any device work
+    L = _lib()
+    cb = L.tq_codebook_init(3, [1, 2, 3, 4])
+    good = _fake_cache(L)
+    # SET_ROWS: source rows 16-byte aligned, cell ids 8-byte aligned, status word 4-byte aligned
+    assert L.tq_set_rows(good, cb, (1 << 23) + 8, L.TQ_F32, 1 << 24, 4, None, None) == L.TQ_ERR_INVALID_ARG
+    assert L.tq_set_rows(good, cb, 1 << 23, L.TQ_F32, (1 << 24) + 4, 4, None, None) == L.TQ_ERR_INVALID_ARG
+    assert L.tq_set_rows(good, cb, 1 << 23, L.TQ_F32, 1 << 24, 4, (1 << 25) + 2, None) == L.TQ_ERR_INVALID_ARG
+    # prefill (nq = 64 > 8, so not the batched-decode route): query type, counts, scale, alignment, workspace
+    k, v = _fake_cache(L), _fake_cache(L)
+    need = L.tq_fattn_prefill_workspace(k, v, 64, 4, 64)
+    assert need > 0
+
+    def pf(q=1 << 23, q_type=L.TQ_F32, nq=64, kv_len=64, scale=0.1, causal=1, out=1 << 24, ws=1 << 25, wsb=need):
+        return L.tq_fattn_prefill(k, v, cb, cb, q, q_type, nq, 4, kv_len, scale, causal, out, ws, wsb, None)
+
+    assert pf(q_type=7) == L.TQ_ERR_INVALID_ARG
+    assert pf(nq=-1) == L.TQ_ERR_INVALID_ARG
+    assert pf(nq=64, kv_len=63) == L.TQ_ERR_INVALID_ARG          # causal rows need nq <= kv_len
+    assert pf(scale=float("nan")) == L.TQ_ERR_INVALID_ARG
+    assert pf(scale=float("inf")) == L.TQ_ERR_INVALID_ARG
+    assert pf(nq=0) == L.TQ_OK
+    assert pf(q=(1 << 23) + 4) == L.TQ_ERR_INVALID_ARG
+    assert pf(out=0) == L.TQ_ERR_INVALID_ARG
+    assert pf(wsb=need - 1) == L.TQ_ERR_WORKSPACE
+    assert pf(ws=(1 << 25) + 64) == L.TQ_ERR_WORKSPACE
+    # int8 / binary16 prompt attention
+    ctx, nq = 40000, 2048
+    wneed = L.tq_int8_prompt_attn_workspace(nq, 32, 8, 128, ctx)
+    assert wneed > 256
+    assert L.tq_int8_prompt_attn_workspace(nq, 30, 8, 128, ctx) == 0       # heads not a multiple
+    assert L.tq_int8_prompt_attn_workspace(nq, 32, 8, 64, ctx) == 0        # head_dim other than 128
+    assert L.tq_int8_prompt_attn_workspace(-1, 32, 8, 128, ctx) == 0
+
+    def i8(k=1 << 23, ks=1 << 24, v=1 << 25, vs=1 << 26, n_cells=ctx, cells=1 << 27, ctx_=ctx, q=1 << 28, nq_=nq,
+           hq=32, hkv=8, d=128, scale=0.1, causal=1, out=1 << 29, ws=1 << 30, wsb=wneed):
+        return L.tq_int8_prompt_attn(k, ks, v, vs, n_cells, cells, ctx_, q, nq_, hq, hkv, d, scale, causal, out,
+                                     ws, wsb, None)
+
+    assert i8(hq=30) == L.TQ_ERR_INVALID_ARG
+    assert i8(hq=24) == L.TQ_ERR_UNSUPPORTED                           # GQA group 3
+    assert i8(d=64) == L.TQ_ERR_UNSUPPORTED
+    assert i8(nq_=-1) == L.TQ_ERR_INVALID_ARG
+    assert i8(ctx_=-1) == L.TQ_ERR_INVALID_ARG
+    assert i8(n_cells=0) == L.TQ_ERR_INVALID_ARG
+    assert i8(nq_=nq, ctx_=nq - 1) == L.TQ_ERR_INVALID_ARG              # causal rows need nq <= ctx
+    assert i8(scale=float("nan")) == L.TQ_ERR_INVALID_ARG
+    assert i8(nq_=0) == L.TQ_OK
+    assert i8(out=(1 << 29) + 4) == L.TQ_ERR_INVALID_ARG
+    assert i8(q=0) == L.TQ_ERR_INVALID_ARG
+    assert i8(wsb=wneed - 1) == L.TQ_ERR_WORKSPACE
+    assert i8(ws=(1 << 30) + 128) == L.TQ_ERR_WORKSPACE
+    assert i8(k=(1 << 23) + 8) == L.TQ_ERR_INVALID_ARG
+    assert i8(cells=0) == L.TQ_ERR_INVALID_ARG
+    assert i8(cells=(1 << 27) + 2) == L.TQ_ERR_INVALID_ARG
+    assert i8(ks=0) == L.TQ_ERR_INVALID_ARG                            # int8 rows need their scales
+    assert i8(vs=(1 << 26) + 1) == L.TQ_ERR_INVALID_ARG
+    # binary16 rows have no scales; the other checks are shared
+    f16 = lambda **kw: L.tq_f16_prompt_attn(kw.get("k", 1 << 23), 1 << 25, ctx, 1 << 27, ctx, 1 << 28, nq, 32, 8,
+                                            128, 0.1, 1, 1 << 29, 1 << 30, kw.get("wsb", wneed), None)
+    assert f16(k=(1 << 23) + 8) == L.TQ_ERR_INVALID_ARG
+    assert f16(wsb=wneed - 1) == L.TQ_ERR_WORKSPACE
